@@ -1,0 +1,416 @@
+#!/usr/bin/env python3
+"""Throughput of the GB300 fp16 NT GEMM, C[M,N] = A[M,K] · B[N,K]ᵀ.
+
+One step = one call of the C-ABI entry point `gemm_f16_nt` on the whole
+workload (default: M = N = K = 8192, the shape the Tilus matmul-hopper tutorial
+measures in every version; inputs uniform in [-1, 1], rounded to fp16, seeded).
+The timed region holds only that kernel, back to back on one stream, with the
+operands resident in HBM; A, B and C together (384 MiB at 8192³) are larger
+than the 129 MB L2, so no step finds its operands in L2 from the step before.
+
+Printed: one JSON line with the throughput (TFLOP/s = 2·M·N·K / time), the
+roofline fraction of the GEMM kernel against the measured dense 16-bit tensor
+peak, an end-to-end figure through the same C ABI from pinned host memory, the
+clocks seen during the timed region, and the CPU oracle timed on a bounded
+sample of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 (under torchrun, one process per GPU) every rank runs an independent
+replica of the workload: the product is a single-GPU library and the multiply
+needs no exchange between GPUs.  The slowest rank's time sets the figure.
+`--impl reference` times the CPU oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from dense_fp16_gemm_gb300 import inputs  # noqa: E402
+
+METRIC = "fp16 NT GEMM TFLOP/s and % of GB300 dense fp16 tensor peak"
+UNIT = "TFLOP/s"
+KERNEL_SOURCES = ["dense_fp16_gemm_gb300/csrc/gemm_f16_nt.cu", "dense_fp16_gemm_gb300/csrc/ptx.cuh",
+                  "dense_fp16_gemm_gb300/csrc/sched.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_f16_nt_8192_traffic.md")
+FALLBACK_PEAK_TFLOPS = 1900.0   # one earlier GB300 bf16 burst measurement
+SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, device=None):
+    if dist is None:
+        return
+    if device is not None and dist.get_backend() == "nccl":
+        dist.barrier(device_ids=[device.index])
+    else:
+        dist.barrier()
+
+
+def reduce_time_and_work(dist, seconds: float, work: float, device=None):
+    """(max seconds over ranks, sum of work over ranks)."""
+    if dist is None:
+        return seconds, work
+    import torch
+    dev = device if (device is not None and dist.get_backend() == "nccl") else "cpu"
+    t = torch.tensor([seconds], dtype=torch.float64, device=dev)
+    w = torch.tensor([work], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(w, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(w.item())
+
+
+# ---------------------------------------------------------------------------
+# peaks, traffic record, clocks
+# ---------------------------------------------------------------------------
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0) or 0), "measured"
+    except Exception:
+        return FALLBACK_PEAK_TFLOPS, 0.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source and this workload; else None."""
+    try:
+        text = open(TRAFFIC_FILE).read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    if fields.get("workload") != workload:
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={SMI_FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", str(period_ms)],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [l.strip().split(",") for l in self.f.read().splitlines() if l.strip()]
+        self.f.close()
+        os.unlink(self.f.name)
+        return rows
+
+
+def summarize_clocks(rows):
+    sm, smax, power, reasons = [], [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for r in rows:
+        r = [x.strip() for x in r]
+        if len(r) < 9:
+            continue
+        try:
+            sm.append(float(r[1]))
+            smax.append(float(r[2]))
+            power.append(float(r[3]))
+        except ValueError:
+            continue
+        for name, v in zip(names, r[5:9]):
+            if v.lower() == "active":
+                reasons.add(name)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    loaded = [s for s, p in zip(sm, power) if p > 0.5 * max(power)] or sm
+    return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+            "reasons": sorted(reasons), "samples": len(sm),
+            "power_w_max": max(power)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg (the reported baseline)
+# ---------------------------------------------------------------------------
+
+def cpu_oracle_sample(w, A, B, target_s: float = 15.0):
+    """Time the oracle on the first R rows of C, R sized for about target_s."""
+    import oracle
+    threads = oracle.default_threads()
+    r0 = max(threads, 1)
+    t0 = time.perf_counter()
+    oracle.gemm_f16_nt(A[:r0], B, threads=threads)
+    dt = time.perf_counter() - t0
+    rows = int(min(w.M, max(r0, r0 * target_s / max(dt, 1e-3))))
+    rows = max(threads, rows - rows % threads)
+    t0 = time.perf_counter()
+    oracle.gemm_f16_nt(A[:rows], B, threads=threads)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * w.N * w.K
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of C ({rows}x{w.N}x{w.K}, {flops:.3e} flop) "
+                      f"in {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def workload_config(w):
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+            "layout": "A[M,K] B[N,K] C[M,N] row-major, C = A·Bᵀ",
+            "accumulate": "f32", "inputs": f"A {w.dist_a}, B {w.dist_b}, seeds {w.seed_a},{w.seed_b}",
+            "l2": f"operands larger than L2: A+B+C = {w.compulsory_bytes / 2**20:.0f} MiB > 129 MB",
+            "parallelism": "replicas"}
+
+
+def run_ours(args, w):
+    import torch
+
+    import dense_fp16_gemm_gb300 as g
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist = init_dist(world, "nccl")
+
+    A, B = inputs.operands(w)
+    Ad = torch.from_numpy(A).to(device)
+    Bd = torch.from_numpy(B).to(device)
+    Cd = torch.full((w.M, w.N), float("nan"), dtype=torch.float16, device=device)
+    stream = torch.cuda.current_stream(device)
+    handle = stream.cuda_stream
+    lib = g.library()
+
+    def step():
+        st = lib.gemm_f16_nt(w.M, w.N, w.K, Ad.data_ptr(), w.K, Bd.data_ptr(), w.K,
+                             Cd.data_ptr(), w.N, handle)
+        if st != 0:
+            raise g.GemmError(st, "gemm_f16_nt")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    if g.device_status(stream) != 0:
+        raise SystemExit("bench.py: watchdog word set during warm-up")
+    if torch.isnan(Cd).any().item():
+        raise SystemExit("bench.py: C has unwritten elements after warm-up")
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    times, launch_ms = [], []
+    for rep in range(args.repeat):
+        if rep and args.cooldown > 0:
+            time.sleep(args.cooldown)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        barrier(dist, device)
+        torch.cuda.synchronize(device)
+        t_start.record(stream)
+        for i in range(args.steps):
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize(device)
+        barrier(dist, device)
+        times.append(t_start.elapsed_time(t_end) / 1e3)
+        launch_ms.extend(a.elapsed_time(b) for a, b in evs)
+    clocks = summarize_clocks(sampler.stop()) if sampler else None
+    if g.device_status(stream) != 0:
+        raise SystemExit("bench.py: watchdog word set during the timed region")
+
+    t_med = statistics.median(times)
+    t_max, total_flops = reduce_time_and_work(dist, t_med, float(w.flops * args.steps), device)
+    value = total_flops / t_max / 1e12
+
+    # roofline of the GEMM kernel: algorithmic flops per launch / mean launch time
+    mean_launch_s = statistics.mean(launch_ms) / 1e3
+    achieved = w.flops / mean_launch_s / 1e12
+    peak, peak_sustained, peak_src = measured_peak()
+
+    # end to end through the same C ABI from pinned host memory
+    e2e_steps = max(1, min(args.steps, 10))
+    Ah = torch.from_numpy(A).pin_memory()
+    Bh = torch.from_numpy(B).pin_memory()
+    Ch = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
+
+    def e2e_step():
+        Ad.copy_(Ah, non_blocking=True)
+        Bd.copy_(Bh, non_blocking=True)
+        step()
+        Ch.copy_(Cd, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(dist, device)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_t, e2e_work = reduce_time_and_work(dist, e0.elapsed_time(e1) / 1e3,
+                                           float(w.flops * e2e_steps), device)
+    if torch.isnan(Ch).any().item():
+        raise SystemExit("bench.py: end-to-end result has unwritten elements")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_sample(w, A, B, args.cpu_seconds)
+
+    if rank == 0:
+        traffic = recorded_traffic(w.name)
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t_max / args.steps * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic", "config": workload_config(w),
+            "pct_of_peak": round(100.0 * achieved / peak, 2),
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                         "unit": UNIT, "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "peak_source": f"{peak_src} bf16 dense burst (fp16 runs at the bf16 rate)",
+                         "frac_of_sustained": round(achieved / peak_sustained, 4) if peak_sustained else None,
+                         "kernel": "gemm_f16_nt_kernel<KCfg<2,256,6>>"},
+            "e2e": {"value": round(e2e_work / e2e_t / 1e12, 2), "unit": UNIT,
+                    "h2d_bytes_per_step": int(A.nbytes + B.nbytes), "d2h_bytes_per_step": int(Ch.numel() * 2)},
+            "gpu_launches": args.steps * args.repeat,
+            "clocks": clocks,
+            "timing": {"repeats": args.repeat, "cooldown_s": args.cooldown,
+                       "per_repeat_ms_per_step": [round(t / args.steps * 1e3, 4) for t in times]},
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    A, B = inputs.operands(w)
+    threads = oracle.default_threads()
+    # each step: a bounded sample of the workload, the first R rows of C
+    probe = max(threads, 1)
+    t0 = time.perf_counter()
+    oracle.gemm_f16_nt(A[:probe], B, threads=threads)
+    dt = time.perf_counter() - t0
+    per_step_target = max(0.5, args.cpu_seconds / max(args.steps + args.warmup, 1))
+    rows = int(min(w.M, max(probe, probe * per_step_target / max(dt, 1e-3))))
+    rows = max(threads, rows - rows % threads)
+    for _ in range(args.warmup):
+        oracle.gemm_f16_nt(A[:rows], B, threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemm_f16_nt(A[:rows], B, threads=threads)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * w.N * w.K * args.steps
+    value = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"each step: rows 0..{rows - 1} of C ({rows}x{w.N}x{w.K})"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gemm_8192", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--repeat", type=int, default=3, help="timed regions per process (median)")
+    ap.add_argument("--cooldown", type=float, default=1.0, help="seconds of idle before each repeat")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU oracle sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, _, _ = dist_env()
+    if args.gpus != world and world > 1:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    w = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

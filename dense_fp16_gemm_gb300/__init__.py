@@ -1,1 +1,198 @@
-"""GB300-native dense fp16 NT GEMM (placeholder; binding follows)."""
+"""GB300-native dense fp16 NT GEMM:  C[M,N] = A[M,K] · B[N,K]ᵀ.
+
+fp16 inputs, fp32 accumulation on the sm_103a tensor cores (tcgen05, TMEM),
+fp16 output rounded to nearest even.  Every step runs in the CUDA library
+``_build/libgemm_f16_nt.so`` (built from ``csrc/`` by ``_build_ext.build``);
+this module only marshals arguments to its C ABI (declared in
+``include/gemm_f16_nt.h``).  There is no CPU or other fallback: without the
+library or without a compute-capability-10.3 GPU every call raises.
+
+The operation is the one the Tilus matmul-hopper tutorial computes: A is
+[m_size, k_size], B is [n_size, k_size] read transposed, fp32 accumulator,
+cast to fp16 ("3. Warp Specialization", §The Full Kernel).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build_ext
+
+__all__ = ["gemm_f16_nt", "gemm_f16_nt_ptr", "device_status", "plan", "tile_coord",
+           "fast_divmod", "GemmError", "Options", "Plan", "library", "STATUS"]
+
+STATUS = {
+    0: "GEMM_OK",
+    1: "GEMM_ERR_INVALID_VALUE",
+    2: "GEMM_ERR_MISALIGNED",
+    3: "GEMM_ERR_UNSUPPORTED_DEVICE",
+    4: "GEMM_ERR_LAUNCH",
+    5: "GEMM_ERR_TIMEOUT",
+}
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = int(status)
+        self.name = STATUS.get(self.status, "unknown")
+        msg = library().gemm_f16_nt_status_string(self.status).decode()
+        super().__init__(f"{what}: {msg}" if what else msg)
+
+
+class Options(ctypes.Structure):
+    """gemm_f16_nt_options_t (zero = default in every field)."""
+    _fields_ = [("cta_group", ctypes.c_int32), ("swizzle", ctypes.c_int32),
+                ("max_clusters", ctypes.c_int32), ("inject_stall", ctypes.c_int32),
+                ("timeout_ns", ctypes.c_uint64)]
+
+
+class Plan(ctypes.Structure):
+    """gemm_f16_nt_plan_t."""
+    _fields_ = [("cta_group", ctypes.c_int32), ("tile_m", ctypes.c_int32),
+                ("tile_n", ctypes.c_int32), ("block_k", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("m_tiles", ctypes.c_int32),
+                ("n_tiles", ctypes.c_int32), ("k_blocks", ctypes.c_int32),
+                ("num_tiles", ctypes.c_int64), ("clusters", ctypes.c_int32),
+                ("grid_ctas", ctypes.c_int32), ("swizzle", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int32), ("tmem_cols", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+_lib = None
+_i64, _i32, _u32, _p = ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32, ctypes.c_void_p
+
+
+def library(path: str | None = None):
+    """Load the C-ABI library (building it first if the sources are newer)."""
+    global _lib
+    if _lib is None:
+        if path is None:
+            if not _build_ext.up_to_date():
+                _build_ext.build()
+            path = _build_ext.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(f"GEMM CUDA library not found at {path}")
+        lib = ctypes.CDLL(path)
+        sig = [_i64, _i64, _i64, _p, _i64, _p, _i64, _p, _i64, _p]
+        lib.gemm_f16_nt.argtypes = sig
+        lib.gemm_f16_nt.restype = ctypes.c_int
+        lib.gemm_f16_nt_ex.argtypes = sig + [ctypes.POINTER(Options)]
+        lib.gemm_f16_nt_ex.restype = ctypes.c_int
+        lib.gemm_f16_nt_device_status.argtypes = [_p, ctypes.POINTER(_u32)]
+        lib.gemm_f16_nt_device_status.restype = ctypes.c_int
+        lib.gemm_f16_nt_status_string.argtypes = [_i32]
+        lib.gemm_f16_nt_status_string.restype = ctypes.c_char_p
+        lib.gemm_f16_nt_plan.argtypes = [_i64, _i64, _i64, _i32, _i32, ctypes.POINTER(Options),
+                                         ctypes.POINTER(Plan)]
+        lib.gemm_f16_nt_plan.restype = ctypes.c_int
+        lib.gemm_f16_nt_tile_coord.argtypes = [_i64, _i32, _i32, _i32, ctypes.POINTER(_i32),
+                                               ctypes.POINTER(_i32)]
+        lib.gemm_f16_nt_tile_coord.restype = ctypes.c_int
+        lib.gemm_f16_nt_fast_divmod.argtypes = [_u32, _u32, ctypes.POINTER(_u32),
+                                                ctypes.POINTER(_u32)]
+        lib.gemm_f16_nt_fast_divmod.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise GemmError(status, what)
+
+
+def gemm_f16_nt_ptr(M: int, N: int, K: int, a_ptr: int, lda: int, b_ptr: int, ldb: int,
+                    c_ptr: int, ldc: int, stream: int = 0, options: Options | None = None) -> None:
+    """Raw call: device pointers (ints), leading dimensions in elements, a
+    cudaStream_t handle (int).  Raises GemmError on a non-OK status."""
+    lib = library()
+    if options is None:
+        st = lib.gemm_f16_nt(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, stream)
+    else:
+        st = lib.gemm_f16_nt_ex(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, stream,
+                                ctypes.byref(options))
+    _check(st, "gemm_f16_nt")
+
+
+def _rows(t, name):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.float16 or t.dim() != 2:
+        raise TypeError(f"{name} must be a 2-D float16 tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must have unit stride along its last dimension")
+    if t.shape[0] > 1:
+        ld = t.stride(0)
+    else:  # a single row: the pitch is never used to address memory
+        ld = max(t.shape[1], 1)
+        ld += (-ld) % 8
+    return t.data_ptr(), ld
+
+
+def gemm_f16_nt(A, B, C=None, *, stream=None, options: Options | None = None):
+    """C = A @ B.T for CUDA float16 tensors A [M, K] and B [N, K].
+
+    C, if given, is an [M, N] float16 view (its row stride may exceed N) and is
+    overwritten; otherwise a new contiguous tensor is returned.  The call is
+    asynchronous on `stream` (default: torch's current stream)."""
+    import torch
+    M, K = A.shape
+    N, K2 = B.shape
+    if K2 != K:
+        raise ValueError(f"A is [{M}, {K}] but B is [{N}, {K2}]")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    if tuple(C.shape) != (M, N):
+        raise ValueError(f"C must be [{M}, {N}]")
+    if stream is None:
+        stream = torch.cuda.current_stream(A.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    pa, lda = _rows(A, "A")
+    pb, ldb = _rows(B, "B")
+    pc, ldc = _rows(C, "C")
+    with torch.cuda.device(A.device):
+        gemm_f16_nt_ptr(M, N, K, pa, lda, pb, ldb, pc, ldc, handle, options)
+    return C
+
+
+def device_status(stream=None) -> int:
+    """Synchronise `stream`, then read and clear the device watchdog word.
+    Returns the word (0 = no wait expired); raises GemmError on CUDA errors."""
+    handle = 0
+    if stream is not None:
+        handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    flags = _u32(0)
+    st = library().gemm_f16_nt_device_status(handle, ctypes.byref(flags))
+    if st not in (0, 5):
+        raise GemmError(st, "gemm_f16_nt_device_status")
+    return int(flags.value)
+
+
+def plan(M: int, N: int, K: int, num_sms: int = 152, max_clusters: int = 0,
+         options: Options | None = None) -> dict:
+    """The launch plan for a problem (host computation only, no GPU needed)."""
+    out = Plan()
+    st = library().gemm_f16_nt_plan(M, N, K, num_sms, max_clusters,
+                                    ctypes.byref(options) if options is not None else None,
+                                    ctypes.byref(out))
+    _check(st, "gemm_f16_nt_plan")
+    return out.as_dict()
+
+
+def tile_coord(linear: int, m_tiles: int, n_tiles: int, swizzle: int):
+    m, n = _i32(0), _i32(0)
+    st = library().gemm_f16_nt_tile_coord(linear, m_tiles, n_tiles, swizzle, ctypes.byref(m),
+                                          ctypes.byref(n))
+    _check(st, "gemm_f16_nt_tile_coord")
+    return m.value, n.value
+
+
+def fast_divmod(n: int, d: int):
+    q, r = _u32(0), _u32(0)
+    st = library().gemm_f16_nt_fast_divmod(n, d, ctypes.byref(q), ctypes.byref(r))
+    _check(st, "gemm_f16_nt_fast_divmod")
+    return q.value, r.value

@@ -1,0 +1,775 @@
+// GB300 (sm_103a) dense fp16 NT GEMM:  C[M,N] = A[M,K] · B[N,K]ᵀ, fp32 accumulation.
+//
+// One persistent kernel, warp-specialised:
+//   warp 0      TMA producer: fills an S-stage shared-memory ring (A tile + B
+//               tile per stage, 128-byte swizzled) gated by full/empty mbarriers;
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (kind::f16, fp32
+//               accumulate) into tensor memory, frees ring slots with
+//               tcgen05.commit, and hands finished accumulators to the epilogue;
+//   warps 2-5   epilogue: tcgen05.ld → fp32→fp16 round-to-nearest-even →
+//               swizzled shared-memory staging → TMA store, clipped at M/N.
+// Two TMEM accumulator buffers let the epilogue of one tile overlap the main
+// loop of the next.  In the default configuration a cluster of two CTAs runs
+// 2-SM MMAs (cta_group::2) on a 256×256 tile: each CTA loads its own 128 rows of
+// A and one half of the B tile, and the pair's single MMA reads both halves, so
+// the shared operand crosses L2 once per pair.
+//
+// Design lineage (prior art, re-derived for tcgen05): the Tilus matmul-hopper
+// tutorial's V2 ring buffer ("2. Multi-Stage Software Pipelining"), V3 role
+// split and full/empty barriers ("3. Warp Specialization", §Producer-Consumer
+// Barriers), V4 raster ("4. Pipeline Abstraction and Two Consumer Warp Groups",
+// §Tile Rasterization) and V6 cluster pairing, persistent loop and TMA-store
+// epilogue ("6. Register Reallocation, Multicast, and a Persistent Kernel",
+// §Cluster Multicast, §Persistent Tile Loop, §Shared-Memory Epilogue).  The
+// accumulator lives in TMEM instead of registers, so V6's register
+// reallocation (§The Register Budget Problem) has no counterpart here.
+//
+// Every wait on an mbarrier is bounded by a watchdog (default 1 s): on expiry
+// the CTA sets a flag that ends every role's loop, records the expired wait in a
+// device word, waits (bounded) for its own copies and MMAs in flight, releases
+// its tensor memory and exits.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "gemm_f16_nt.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+
+#define G16_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace g16 {
+
+constexpr int kBlockM = 128;   // accumulator rows per CTA = TMEM lanes
+constexpr int kBlockK = 64;    // k per stage: 64 fp16 = one 128-byte swizzle row
+constexpr int kUmmaK = 16;     // k per tcgen05.mma of kind::f16
+constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kEpiWarps = 4;
+constexpr int kEpiCols = 64;                       // columns per staged store (128-byte rows)
+constexpr int kOutBufBytes = 32 * kEpiCols * 2;    // one warp's 32×64 fp16 staging tile
+constexpr int kOutBufs = 2;                        // double-buffered per warp
+constexpr int kDefaultSwizzle = 8;
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;
+
+// watchdog word layout: bit 0 = a wait expired, bit 7+s = wait site s expired
+enum : uint32_t {
+    kSiteProducerEmpty = 1,
+    kSiteMmaFull = 2,
+    kSiteMmaAccFree = 3,
+    kSiteEpiAccFull = 4,
+    kSiteProducerDrain = 5,
+    kSiteMmaDrain = 6,
+};
+
+__device__ uint32_t g_watchdog_word;
+
+template <int CG, int BN, int STAGES>
+struct KCfg {
+    static constexpr int kCG = CG;
+    static constexpr int kBN = BN;                   // columns of C per tile
+    static constexpr int kStages = STAGES;
+    static constexpr int kTileM = kBlockM * CG;      // rows of C per tile
+    static constexpr int kBRows = BN / CG;           // B rows this CTA loads per stage
+    static constexpr int kABytes = kBlockM * kBlockK * 2;
+    static constexpr int kBBytes = kBRows * kBlockK * 2;
+    static constexpr int kTxBytes = (kABytes + kBBytes) * CG;  // bytes per stage on the leader's barrier
+    static constexpr int kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128
+                                   : 2 * BN <= 256 ? 256 : 512;
+    static constexpr int kRingBytes = STAGES * (kABytes + kBBytes);
+    static constexpr int kOutBytes = kEpiWarps * kOutBufs * kOutBufBytes;
+    static constexpr int kCtlBytes = 256;
+    static constexpr int kSmemBytes = 1024 + kRingBytes + kOutBytes + kCtlBytes;
+    // tcgen05 instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B
+    // fp16 (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N>>3 at bit 17,
+    // M>>4 at bit 24.
+    static constexpr uint32_t kIdesc =
+        (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t(kTileM >> 4) << 24);
+
+    static_assert(2 * BN <= 512, "two accumulator buffers must fit in the 512 TMEM columns");
+    static_assert(BN % kEpiCols == 0, "epilogue works in 64-column chunks");
+    static_assert(kBRows <= 256, "a TMA box is at most 256 rows");
+    static_assert(kSmemBytes <= 232448, "dynamic shared memory limit per CTA");
+};
+
+template <int STAGES>
+struct Ctl {
+    uint64_t full[STAGES];      // stage loaded (TMA bytes landed)   — leader CTA's copy is used
+    uint64_t empty[STAGES];     // stage consumed (MMAs done)        — each CTA's own copy
+    uint64_t acc_full[2];       // accumulator ready for the epilogue
+    uint64_t acc_empty[2];      // accumulator drained               — leader CTA's copy is used
+    uint64_t mma_done;          // all MMAs retired (teardown)
+    uint32_t tmem_base;
+    uint32_t abort_flag;
+};
+
+struct Params {
+    CUtensorMap tmA;   // A: dims {K, M}, box {64, 128}
+    CUtensorMap tmB;   // B: dims {K, N}, box {64, BN/CG}
+    CUtensorMap tmC;   // C: dims {N8, M}, box {64, 32}; only when N8 > 0
+    Raster raster;
+    uint32_t num_tiles;
+    uint32_t num_kb;
+    int32_t M;
+    int32_t N;
+    int32_t N8;        // N rounded down to a multiple of 8 (16 bytes)
+    uint16_t* C;       // for the last N - N8 columns, written with plain stores
+    int64_t ldc;
+    uint64_t timeout_ns;
+    uint32_t* watchdog;
+    int32_t inject_stall;
+};
+
+// ---------------------------------------------------------------------------
+// bounded waits
+// ---------------------------------------------------------------------------
+
+struct Watch {
+    uint64_t limit_ns;
+    volatile uint32_t* abort_flag;   // this CTA's flag
+    uint32_t peer_abort;             // shared::cluster address of the peer's flag, 0 if none
+    uint32_t* word;
+};
+
+__device__ __noinline__ void raise_abort(const Watch w, uint32_t site) {
+    *w.abort_flag = 1u;
+    if (w.peer_abort) ptx::st_cluster_u32(w.peer_abort, 1u);
+    atomicOr(w.word, 1u | (1u << (7u + site)));
+}
+
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Watch w, uint32_t site) {
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((i & 7u) == 0) {
+            if (*w.abort_flag) return false;
+            if (ptx::globaltimer() - t0 > w.limit_ns) {
+                raise_abort(w, site);
+                return false;
+            }
+        }
+    }
+}
+
+// Wait for the phase of parity `parity` to complete; false if the watchdog
+// fired (here or elsewhere in the CTA).
+__device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, const Watch& w, uint32_t site) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, w, site);
+}
+
+// Teardown wait after an abort: ignores the abort flag, bounded by the limit.
+__device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((i & 7u) == 0 && ptx::globaltimer() - t0 > limit_ns) return false;
+    }
+}
+
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+    const uint64_t t0 = ptx::globaltimer();
+    while (ptx::globaltimer() - t0 < ns) {
+    }
+}
+
+// Shared-memory matrix descriptor for a K-major tile written by TMA with
+// 128-byte swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle atoms stacked
+// along M/N.  Start address >> 4 in bits 0-13, leading-byte offset (unused for
+// swizzled K-major) in 16-29, stride-byte offset 1024 >> 4 in 32-45, descriptor
+// version 1 in bits 46-47, swizzle mode 2 (128 B) in bits 61-63.  Advancing K by
+// 16 fp16 inside the 128-byte row adds 32 bytes (2 in the start field).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+    return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
+           (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+
+template <class Cfg>
+__global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_constant__ Params p) {
+    constexpr int CG = Cfg::kCG;
+    constexpr int BN = Cfg::kBN;
+    constexpr int S = Cfg::kStages;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;   // 128-byte swizzle atoms need 1 KB alignment
+    const uint32_t sA = base;
+    const uint32_t sB = sA + S * Cfg::kABytes;
+    const uint32_t sOut = sB + S * Cfg::kBBytes;
+    Ctl<S>* ctl = reinterpret_cast<Ctl<S>*>(smem_raw + (base - raw) + Cfg::kRingBytes + Cfg::kOutBytes);
+
+    const uint32_t warp = __shfl_sync(0xffffffffu, threadIdx.x >> 5, 0);
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t rank = CG == 2 ? ptx::cluster_ctarank() : 0u;
+    const uint32_t cluster = CG == 2 ? ptx::cluster_id_x() : blockIdx.x;
+    const uint32_t nclusters = CG == 2 ? ptx::nclusters_x() : gridDim.x;
+
+    const uint32_t full0 = ptx::smem_u32(&ctl->full[0]);
+    const uint32_t empty0 = ptx::smem_u32(&ctl->empty[0]);
+    const uint32_t accf0 = ptx::smem_u32(&ctl->acc_full[0]);
+    const uint32_t acce0 = ptx::smem_u32(&ctl->acc_empty[0]);
+    const uint32_t mma_done = ptx::smem_u32(&ctl->mma_done);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(full0 + 8 * s, 1);     // the leader's expect-tx arrive
+            ptx::mbar_init(empty0 + 8 * s, 1);    // one tcgen05.commit
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(accf0 + 8 * b, 1);                  // one tcgen05.commit
+            ptx::mbar_init(acce0 + 8 * b, kEpiWarps * CG);     // every epilogue warp of the pair
+        }
+        ptx::mbar_init(mma_done, 1);
+        ctl->abort_flag = 0u;
+        ptx::fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&p.tmA);
+        ptx::prefetch_tensormap(&p.tmB);
+        if (p.N8 > 0) ptx::prefetch_tensormap(&p.tmC);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc<CG>(ptx::smem_u32(&ctl->tmem_base), Cfg::kTmemCols);
+        ptx::tmem_relinquish<CG>();
+    }
+    ptx::tc_fence_before();
+    if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(&ctl->tmem_base);
+
+    Watch w;
+    w.limit_ns = p.timeout_ns;
+    w.abort_flag = &ctl->abort_flag;
+    w.peer_abort = CG == 2 ? ptx::mapa(ptx::smem_u32(&ctl->abort_flag), rank ^ 1u) : 0u;
+    w.word = p.watchdog;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && !p.inject_stall) {
+            // Completion bytes of both CTAs' loads go to the leader's full barrier.
+            const uint32_t full_tgt = CG == 2 ? ptx::mapa(full0, 0) : full0;
+            uint32_t stage = 0, phase = 0, issued = 0;
+            bool ok = true;
+            for (uint32_t t = cluster; ok && t < p.num_tiles; t += nclusters) {
+                uint32_t mt, nt;
+                raster_coord(p.raster, t, mt, nt);
+                const int32_t m0 = int32_t(mt * Cfg::kTileM + rank * kBlockM);
+                const int32_t n0 = int32_t(nt * BN + rank * Cfg::kBRows);
+                for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait(empty0 + 8 * stage, phase ^ 1u, w, kSiteProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    if (rank == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * stage, Cfg::kTxBytes);
+                    const int32_t k0 = int32_t(kb * kBlockK);
+                    const uint32_t bar = full_tgt + 8 * stage;
+                    if constexpr (CG == 2) {
+                        ptx::tma_load_2d_pair(sA + stage * Cfg::kABytes, &p.tmA, k0, m0, bar);
+                        ptx::tma_load_2d_pair(sB + stage * Cfg::kBBytes, &p.tmB, k0, n0, bar);
+                    } else {
+                        ptx::tma_load_2d(sA + stage * Cfg::kABytes, &p.tmA, k0, m0, bar);
+                        ptx::tma_load_2d(sB + stage * Cfg::kBBytes, &p.tmB, k0, n0, bar);
+                    }
+                    ++issued;
+                    if (++stage == uint32_t(S)) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok && issued) {
+                // Let the copies already issued land before the CTA can exit.
+                if (rank == 0) {
+                    uint32_t s = stage, ph = phase;
+                    const uint32_t n = issued < uint32_t(S) ? issued : uint32_t(S);
+                    for (uint32_t i = 0; i < n; ++i) {
+                        if (s == 0) {
+                            s = S - 1;
+                            ph ^= 1u;
+                        } else {
+                            --s;
+                        }
+                        if (!wait_drain(full0 + 8 * s, ph, p.timeout_ns))
+                            atomicOr(p.watchdog, 1u | (1u << (7u + kSiteProducerDrain)));
+                    }
+                } else {
+                    spin_ns(200000);   // this CTA's bytes complete on the peer's barrier
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && rank == 0) {
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (uint32_t t = cluster; ok && t < p.num_tiles; t += nclusters) {
+                if (!wait(acce0 + 8 * acc, acc_phase ^ 1u, w, kSiteMmaAccFree)) break;
+                ptx::tc_fence_after();
+                const uint32_t d = tmem_base + acc * uint32_t(BN);
+                for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait(full0 + 8 * stage, phase, w, kSiteMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint64_t ad = sdesc_sw128(sA + stage * Cfg::kABytes);
+                    const uint64_t bd = sdesc_sw128(sB + stage * Cfg::kBBytes);
+#pragma unroll
+                    for (int k = 0; k < kBlockK / kUmmaK; ++k) {
+                        const uint64_t koff = uint64_t((k * kUmmaK * 2) >> 4);
+                        ptx::mma_f16<CG>(d, ad + koff, bd + koff, Cfg::kIdesc, (kb | uint32_t(k)) != 0u);
+                    }
+                    // Free this ring slot in every CTA of the pair once these MMAs retire.
+                    if constexpr (CG == 2) ptx::mma_commit_pair(empty0 + 8 * stage, 0x3);
+                    else ptx::mma_commit(empty0 + 8 * stage);
+                    if (++stage == uint32_t(S)) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if constexpr (CG == 2) ptx::mma_commit_pair(accf0 + 8 * acc, 0x3);
+                else ptx::mma_commit(accf0 + 8 * acc);
+                acc ^= 1u;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            // Every MMA must have retired before the tensor memory is released.
+            if constexpr (CG == 2) ptx::mma_commit_pair(mma_done, 0x1);
+            else ptx::mma_commit(mma_done);
+            if (!wait_drain(mma_done, 0, p.timeout_ns)) atomicOr(p.watchdog, 1u | (1u << (7u + kSiteMmaDrain)));
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const uint32_t q = warp & 3u;                      // TMEM lane quarter this warp may read
+        const uint32_t lane_off = (q * 32u) << 16;
+        const uint32_t out0 = sOut + (warp - 2u) * kOutBufs * kOutBufBytes;
+        const uint32_t acce_tgt = CG == 2 ? ptx::mapa(acce0, 0) : acce0;
+        uint32_t acc = 0, acc_phase = 0, ob = 0;
+        for (uint32_t t = cluster; t < p.num_tiles; t += nclusters) {
+            uint32_t mt, nt;
+            raster_coord(p.raster, t, mt, nt);
+            const int32_t row0 = int32_t(mt * Cfg::kTileM + rank * kBlockM + q * 32u);
+            const int32_t col0 = int32_t(nt * BN);
+            uint32_t ok = 0;
+            if (lane == 0) ok = wait(accf0 + 8 * acc, acc_phase, w, kSiteEpiAccFull) ? 1u : 0u;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const uint32_t tacc = tmem_base + lane_off + acc * uint32_t(BN);
+#pragma unroll 1
+            for (int c = 0; c < BN / kEpiCols; ++c) {
+                uint32_t lo[32], hi[32];
+                ptx::tmem_ld_32x32b_x32(tacc + uint32_t(c * kEpiCols), lo);
+                ptx::tmem_ld_32x32b_x32(tacc + uint32_t(c * kEpiCols + 32), hi);
+                ptx::tmem_wait_ld();
+                if (c == BN / kEpiCols - 1) {
+                    // The whole accumulator is in registers: hand the buffer back.
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (CG == 2) ptx::mbar_arrive_cluster(acce_tgt + 8 * acc);
+                        else ptx::mbar_arrive(acce0 + 8 * acc);
+                    }
+                }
+                uint32_t h[32];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) h[j] = ptx::pack_f16x2_rn(lo[2 * j], lo[2 * j + 1]);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) h[16 + j] = ptx::pack_f16x2_rn(hi[2 * j], hi[2 * j + 1]);
+
+                // The staging buffer about to be written was last read by the
+                // store issued two chunks ago.
+                if (lane == 0) ptx::bulk_wait_group_read<1>();
+                __syncwarp();
+                const uint32_t buf = out0 + ob * kOutBufBytes;
+                const uint32_t row = buf + lane * 128u;
+#pragma unroll
+                for (uint32_t j = 0; j < 8; ++j)   // 16-byte chunk j of this row, 128-byte swizzle
+                    ptx::st_shared_v4(row + ((j ^ (lane & 7u)) << 4), h[4 * j], h[4 * j + 1],
+                                      h[4 * j + 2], h[4 * j + 3]);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                const int32_t cx = col0 + c * kEpiCols;
+                if (lane == 0) {
+                    // The tensor map spans only the 16-byte-aligned columns [0, N8).
+                    if (row0 < p.M && cx < p.N8) ptx::tma_store_2d(&p.tmC, cx, row0, buf);
+                    ptx::bulk_commit_group();
+                }
+                if (p.N8 < p.N && cx <= p.N8 && p.N8 < cx + kEpiCols) {
+                    // The last N - N8 (< 8) columns: this lane's row, straight from registers.
+                    const int32_t r = row0 + int32_t(lane);
+                    if (r < p.M) {
+                        uint16_t* dst = p.C + int64_t(r) * p.ldc;
+                        for (int32_t e = p.N8; e < p.N; ++e) {
+                            // element idx of this lane's staged row (16-byte chunk idx/8, swizzled)
+                            const uint32_t idx = uint32_t(e - cx);
+                            dst[e] = ptx::ld_shared_u16(row + ((((idx >> 3) ^ (lane & 7u)) << 4) |
+                                                               ((idx & 7u) << 1)));
+                        }
+                    }
+                }
+                ob ^= 1u;
+            }
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        if (lane == 0) ptx::bulk_wait_group_all();
+        __syncwarp();
+    }
+
+    ptx::tc_fence_before();
+    if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 1) ptx::tmem_dealloc<CG>(tmem_base, Cfg::kTmemCols);
+}
+
+// K == 0: the empty sum, +0 over the M×N window.
+__global__ void zero_fill_kernel(uint16_t* C, int64_t M, int64_t N, int64_t ldc) {
+    const int64_t total = M * N;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t m = i / N, n = i - m * N;
+        C[m * ldc + n] = 0;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+using Cfg2 = KCfg<2, 256, 6>;   // CTA pair, 256×256 tile, 6-stage ring
+using Cfg1 = KCfg<1, 256, 4>;   // single CTA, 128×256 tile, 4-stage ring
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+    bool ready = false;
+    gemm_status_t status = GEMM_OK;
+    int sms = 0;
+    int max_clusters2 = 0;   // resident CTA pairs for Cfg2
+    int max_ctas1 = 0;       // resident CTAs for Cfg1
+    uint32_t* watchdog = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+gemm_status_t setup_device(int dev, DeviceState& st) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    if (cudaFuncSetAttribute(gemm_f16_nt_kernel<Cfg2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg2::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_f16_nt_kernel<Cfg1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg1::kSmemBytes) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    // How many CTA pairs can be resident at once (cluster placement may leave
+    // some SMs unpaired).
+    {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = Cfg2::kSmemBytes;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_f16_nt_kernel<Cfg2>, &cfg) != cudaSuccess || n < 1) {
+            cudaGetLastError();
+            n = sms / 2;
+        }
+        st.max_clusters2 = n < sms / 2 ? n : sms / 2;
+    }
+    {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_f16_nt_kernel<Cfg1>, kThreads,
+                                                          Cfg1::kSmemBytes) != cudaSuccess ||
+            per_sm < 1) {
+            cudaGetLastError();
+            per_sm = 1;
+        }
+        st.max_ctas1 = sms;   // one CTA per SM: each holds all 512 TMEM columns
+    }
+    void* wd = nullptr;
+    if (cudaGetSymbolAddress(&wd, g_watchdog_word) != cudaSuccess || !wd) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    st.watchdog = static_cast<uint32_t*>(wd);
+    st.sms = sms;
+    return GEMM_OK;
+}
+
+gemm_status_t current_device(DeviceState** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return GEMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& st = g_dev[dev];
+    if (!st.ready) {
+        st.status = setup_device(dev, st);
+        st.ready = true;
+    }
+    if (st.status != GEMM_OK) return st.status;
+    *out = &st;
+    return GEMM_OK;
+}
+
+gemm_status_t check_args(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
+                         const uint16_t* B, int64_t ldb, const uint16_t* C, int64_t ldc) {
+    const int64_t lim = int64_t(1) << 31;
+    if (M < 0 || N < 0 || K < 0 || M >= lim || N >= lim || K >= lim) return GEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return GEMM_OK;
+    const int64_t ld_lim = int64_t(1) << 39;   // TMA strides stay below 2^40 bytes
+    if (!C || ldc < N || ldc >= ld_lim) return GEMM_ERR_INVALID_VALUE;
+    if (K > 0) {
+        if (!A || !B || lda < K || ldb < K || lda >= ld_lim || ldb >= ld_lim) return GEMM_ERR_INVALID_VALUE;
+        if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15) ||
+            (lda & 7) || (ldb & 7))
+            return GEMM_ERR_MISALIGNED;
+    }
+    if ((reinterpret_cast<uintptr_t>(C) & 15) || (ldc & 7)) return GEMM_ERR_MISALIGNED;
+    return GEMM_OK;
+}
+
+gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t max_resident,
+                        const gemm_f16_nt_options_t* o, gemm_f16_nt_plan_t* pl) {
+    const int64_t lim = int64_t(1) << 31;
+    if (!pl || M < 0 || N < 0 || K < 0 || M >= lim || N >= lim || K >= lim || num_sms < 1)
+        return GEMM_ERR_INVALID_VALUE;
+    const int cg = (o && o->cta_group) ? o->cta_group : 2;
+    const int sw = (o && o->swizzle) ? o->swizzle : kDefaultSwizzle;
+    if ((cg != 1 && cg != 2) || sw < 1 || sw > 64 || (o && o->max_clusters < 0))
+        return GEMM_ERR_INVALID_VALUE;
+    memset(pl, 0, sizeof(*pl));
+    pl->cta_group = cg;
+    pl->tile_m = kBlockM * cg;
+    pl->tile_n = cg == 2 ? Cfg2::kBN : Cfg1::kBN;
+    pl->block_k = kBlockK;
+    pl->stages = cg == 2 ? Cfg2::kStages : Cfg1::kStages;
+    pl->smem_bytes = cg == 2 ? Cfg2::kSmemBytes : Cfg1::kSmemBytes;
+    pl->tmem_cols = cg == 2 ? Cfg2::kTmemCols : Cfg1::kTmemCols;
+    const int64_t mt = cdiv(M, pl->tile_m), nt = cdiv(N, pl->tile_n);
+    const int64_t tiles = mt * nt;
+    if (tiles >= lim || mt * sw >= lim) return GEMM_ERR_INVALID_VALUE;
+    pl->m_tiles = int32_t(mt);
+    pl->n_tiles = int32_t(nt);
+    pl->k_blocks = int32_t(cdiv(K, kBlockK));
+    pl->num_tiles = tiles;
+    pl->swizzle = int32_t(nt > 0 && sw > nt ? nt : sw);
+    int64_t resident = max_resident > 0 ? max_resident : (cg == 2 ? num_sms / 2 : num_sms);
+    if (resident < 1) resident = 1;
+    if (o && o->max_clusters > 0 && o->max_clusters < resident) resident = o->max_clusters;
+    const int64_t clusters = tiles < resident ? tiles : resident;
+    pl->clusters = int32_t(clusters);
+    pl->grid_ctas = int32_t(clusters * cg);
+    return GEMM_OK;
+}
+
+gemm_status_t encode_2d(CUtensorMap* tm, const void* ptr, uint64_t inner, uint64_t outer,
+                        uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer) {
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {pitch_elems * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_LAUNCH;
+}
+
+template <class Cfg>
+gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t K, const uint16_t* A,
+                     int64_t lda, const uint16_t* B, int64_t ldb, uint16_t* C, int64_t ldc,
+                     cudaStream_t stream, const gemm_f16_nt_options_t* o, uint32_t* watchdog) {
+    Params p;
+    memset(&p, 0, sizeof(p));
+    gemm_status_t s;
+    // A TMA store clips the innermost dimension in 16-byte units, so the map for
+    // C covers only the first N8 = N - N % 8 columns; the kernel writes the rest
+    // with plain stores and no byte past column N-1 is ever written.
+    const int64_t N8 = N & ~int64_t(7);
+    if ((s = encode_2d(&p.tmA, A, uint64_t(K), uint64_t(M), uint64_t(lda), kBlockK, kBlockM)) != GEMM_OK ||
+        (s = encode_2d(&p.tmB, B, uint64_t(K), uint64_t(N), uint64_t(ldb), kBlockK, Cfg::kBRows)) != GEMM_OK ||
+        (N8 > 0 && (s = encode_2d(&p.tmC, C, uint64_t(N8), uint64_t(M), uint64_t(ldc), kEpiCols, 32)) != GEMM_OK))
+        return s;
+    p.N8 = int32_t(N8);
+    p.C = C;
+    p.ldc = ldc;
+    p.raster = make_raster(uint32_t(pl.m_tiles), uint32_t(pl.n_tiles), uint32_t(pl.swizzle));
+    p.num_tiles = uint32_t(pl.num_tiles);
+    p.num_kb = uint32_t(pl.k_blocks);
+    p.M = int32_t(M);
+    p.N = int32_t(N);
+    p.timeout_ns = (o && o->timeout_ns) ? o->timeout_ns : kDefaultTimeoutNs;
+    p.watchdog = watchdog;
+    p.inject_stall = o ? o->inject_stall : 0;
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(uint32_t(pl.grid_ctas), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = stream;
+    if (Cfg::kCG == 2) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    if (cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<Cfg>, p) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    return GEMM_OK;
+}
+
+gemm_status_t run(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B,
+                  int64_t ldb, uint16_t* C, int64_t ldc, void* stream_v, const gemm_f16_nt_options_t* o) {
+    gemm_status_t s = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+    if (s != GEMM_OK) return s;
+    if (o && ((o->cta_group != 0 && o->cta_group != 1 && o->cta_group != 2) || o->swizzle < 0 ||
+              o->swizzle > 64 || o->max_clusters < 0))
+        return GEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return GEMM_OK;
+    DeviceState* st = nullptr;
+    if ((s = current_device(&st)) != GEMM_OK) return s;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    if (K == 0) {
+        const int64_t total = M * N;
+        int64_t blocks = cdiv(total, 256);
+        if (blocks > int64_t(st->sms) * 8) blocks = int64_t(st->sms) * 8;
+        zero_fill_kernel<<<dim3(uint32_t(blocks)), dim3(256), 0, stream>>>(C, M, N, ldc);
+        if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+        return GEMM_OK;
+    }
+    const int cg = (o && o->cta_group) ? o->cta_group : 2;
+    gemm_f16_nt_plan_t pl;
+    if ((s = make_plan(M, N, K, st->sms, cg == 2 ? st->max_clusters2 : st->max_ctas1, o, &pl)) != GEMM_OK)
+        return s;
+    if (cg == 2) return launch<Cfg2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, o, st->watchdog);
+    return launch<Cfg1>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, o, st->watchdog);
+}
+
+}  // namespace g16
+
+// ---------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------
+
+G16_EXPORT gemm_status_t gemm_f16_nt(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
+                                     const uint16_t* B, int64_t ldb, uint16_t* C, int64_t ldc,
+                                     void* stream) {
+    return g16::run(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr);
+}
+
+G16_EXPORT gemm_status_t gemm_f16_nt_ex(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
+                                        const uint16_t* B, int64_t ldb, uint16_t* C, int64_t ldc,
+                                        void* stream, const gemm_f16_nt_options_t* opts) {
+    return g16::run(M, N, K, A, lda, B, ldb, C, ldc, stream, opts);
+}
+
+G16_EXPORT gemm_status_t gemm_f16_nt_device_status(void* stream, uint32_t* flags) {
+    g16::DeviceState* st = nullptr;
+    gemm_status_t s = g16::current_device(&st);
+    if (s != GEMM_OK) return s;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, st->watchdog, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(st->watchdog, 0, sizeof(v)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    if (flags) *flags = v;
+    return v ? GEMM_ERR_TIMEOUT : GEMM_OK;
+}
+
+G16_EXPORT const char* gemm_f16_nt_status_string(int32_t status) {
+    switch (status) {
+        case GEMM_OK: return "GEMM_OK";
+        case GEMM_ERR_INVALID_VALUE: return "GEMM_ERR_INVALID_VALUE: size or leading dimension out of range, or NULL pointer";
+        case GEMM_ERR_MISALIGNED: return "GEMM_ERR_MISALIGNED: pointers must be 16-byte aligned and leading dimensions multiples of 8";
+        case GEMM_ERR_UNSUPPORTED_DEVICE: return "GEMM_ERR_UNSUPPORTED_DEVICE: needs a compute capability 10.3 GPU";
+        case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH: a CUDA runtime or driver call failed";
+        case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: a pipeline wait ran into the device watchdog";
+        default: return "unknown gemm_status_t";
+    }
+}
+
+G16_EXPORT gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms,
+                                          int32_t max_clusters, const gemm_f16_nt_options_t* opts,
+                                          gemm_f16_nt_plan_t* plan) {
+    return g16::make_plan(M, N, K, num_sms, max_clusters, opts, plan);
+}
+
+G16_EXPORT gemm_status_t gemm_f16_nt_tile_coord(int64_t linear, int32_t m_tiles, int32_t n_tiles,
+                                                int32_t swizzle, int32_t* m_tile, int32_t* n_tile) {
+    if (m_tiles < 1 || n_tiles < 1 || swizzle < 1 || swizzle > 64 || !m_tile || !n_tile)
+        return GEMM_ERR_INVALID_VALUE;
+    const int64_t total = int64_t(m_tiles) * n_tiles;
+    const int64_t sw = swizzle < n_tiles ? swizzle : n_tiles;
+    if (total >= (int64_t(1) << 31) || int64_t(m_tiles) * sw >= (int64_t(1) << 31) || linear < 0 ||
+        linear >= total)
+        return GEMM_ERR_INVALID_VALUE;
+    g16::Raster r = g16::make_raster(uint32_t(m_tiles), uint32_t(n_tiles), uint32_t(swizzle));
+    uint32_t m, n;
+    g16::raster_coord(r, uint32_t(linear), m, n);
+    *m_tile = int32_t(m);
+    *n_tile = int32_t(n);
+    return GEMM_OK;
+}
+
+G16_EXPORT gemm_status_t gemm_f16_nt_fast_divmod(uint32_t n, uint32_t d, uint32_t* q, uint32_t* r) {
+    if (d < 1 || d > (1u << 31) || n >= (1u << 31) || !q || !r) return GEMM_ERR_INVALID_VALUE;
+    g16::FastDiv f = g16::make_fastdiv(d);
+    const uint32_t qq = g16::fastdiv_q(f, n);
+    *q = qq;
+    *r = n - qq * d;
+    return GEMM_OK;
+}

@@ -5,7 +5,9 @@ multiply.  Both the CUDA path's tests and benchmark and the CPU oracle read the
 arrays it makes, so the two sides always see the same fp16 bit patterns.
 
 Recipe: values are drawn in float32 from numpy's PCG64 generator seeded per
-operand, then rounded to float16 with numpy's round-to-nearest-even cast.
+operand (uniform: a float32 in [0, 1) scaled to [lo, hi); normal: standard
+normal float32 times sigma plus mean; integers: uniform on {lo..hi}), then
+rounded to float16 with numpy's round-to-nearest-even cast.
 
 The workloads follow the shapes the tutorial measures (Tilus matmul-hopper
 tutorial, "6. Register Reallocation, Multicast, and a Persistent Kernel",
@@ -67,12 +69,14 @@ def draw(shape, dist: tuple, seed: int, ld: int | None = None) -> np.ndarray:
     rng = np.random.Generator(np.random.PCG64(seed))
     kind = dist[0]
     if kind == "uniform":
-        x = rng.uniform(dist[1], dist[2], size=(rows, cols)).astype(np.float32)
+        x = rng.random(size=(rows, cols), dtype=np.float32)      # [0, 1)
+        x *= np.float32(dist[2] - dist[1])
+        x += np.float32(dist[1])
     elif kind == "normal":
         x = rng.standard_normal(size=(rows, cols), dtype=np.float32)
         x = (x * np.float32(dist[2]) + np.float32(dist[1])).astype(np.float32)
     elif kind == "int":
-        x = rng.integers(dist[1], dist[2] + 1, size=(rows, cols)).astype(np.float32)
+        x = rng.integers(dist[1], dist[2] + 1, size=(rows, cols), dtype=np.int8).astype(np.float32)
     else:
         raise ValueError(f"unknown distribution {kind!r}")
     h = x.astype(np.float16)

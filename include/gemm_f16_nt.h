@@ -1,0 +1,190 @@
+/*
+ * gemm_f16_nt.h — C ABI of the GB300 (sm_103a) dense fp16 NT matrix multiply.
+ *
+ *     C[M,N] = A[M,K] · B[N,K]ᵀ      fp16 inputs, fp32 accumulation, fp16 output
+ *
+ * The operation is the one the Tilus "matmul-hopper" tutorial builds up in its
+ * versions 2–6: A is an [m_size, k_size] fp16 matrix, B an [n_size, k_size]
+ * fp16 matrix read transposed, the accumulator is fp32 and C is the fp16 cast
+ * of it ("3. Warp Specialization", §The Full Kernel; "4. Pipeline Abstraction
+ * and Two Consumer Warp Groups", §The Full Kernel; "6. Register Reallocation,
+ * Multicast, and a Persistent Kernel", opening list: fp32 accumulation kept).
+ * The tutorial's kernels take three sizes and three contiguous pointers; this
+ * ABI adds leading dimensions and a stream.
+ *
+ * Numbers: fp16 values are IEEE-754 binary16 bit patterns (uint16_t).  The sum
+ * over k is carried in fp32 on the tensor cores; the fp32 → fp16 cast rounds to
+ * nearest, ties to even, overflowing to ±inf.  Results agree with an fp64
+ * reference rounded once to fp16 within 2 fp16 ulps + 1e-4·sqrt(K) per
+ * element, and exactly when every partial sum is an fp32-exact integer.
+ *
+ * Threading: every entry point may be called from any host thread.  Each GEMM
+ * call is asynchronous on the given stream.
+ */
+#ifndef GEMM_F16_NT_H_
+#define GEMM_F16_NT_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_VALUE = 1,      /* a size or leading dimension is out of range, or a pointer is NULL */
+    GEMM_ERR_MISALIGNED = 2,         /* a pointer or row pitch breaks the 16-byte rule below */
+    GEMM_ERR_UNSUPPORTED_DEVICE = 3, /* no CUDA device, or the current device is not compute capability 10.3 */
+    GEMM_ERR_LAUNCH = 4,             /* the CUDA runtime or driver refused a call (set-up or launch) */
+    GEMM_ERR_TIMEOUT = 5             /* the device watchdog word is set (see gemm_f16_nt_device_status) */
+} gemm_status_t;
+
+/*
+ * gemm_f16_nt — C = A · Bᵀ on the current CUDA device.
+ *
+ *   M, N, K   sizes, each in [0, 2^31).
+ *   A         device pointer, element (m, k) at A[m*lda + k], m < M, k < K.
+ *   lda       row pitch of A in elements, lda >= max(K, 1).
+ *   B         device pointer, element (n, k) at B[n*ldb + k], n < N, k < K.
+ *   ldb       row pitch of B in elements, ldb >= max(K, 1).
+ *   C         device pointer, element (m, n) at C[m*ldc + n], m < M, n < N.
+ *   ldc       row pitch of C in elements, ldc >= max(N, 1).
+ *   stream    a cudaStream_t (NULL = the legacy default stream).
+ *
+ * Layout and alignment: all three matrices are row-major.  A, B and C must be
+ * 16-byte aligned and lda, ldb, ldc multiples of 8 elements (16 bytes): the
+ * tensor-memory-accelerator copies that move the tiles require it.  There is
+ * no slower path for other layouts: such calls return GEMM_ERR_MISALIGNED.
+ *
+ * Semantics: C is overwritten (no alpha/beta).  Only the M×N window is
+ * written; columns N..ldc-1 of each row of C are never touched.  M == 0 or
+ * N == 0 is a no-op.  K == 0 writes +0 to the whole M×N window (the empty sum).
+ * C must not overlap A or B (not checked).
+ *
+ * Ownership: the caller owns A, B and C and keeps them alive until the work on
+ * `stream` completes.  The library keeps no pointer after the call returns.
+ * The first call on a device performs one-time set-up on that device (device
+ * query, kernel attributes, the watchdog word's address); later calls do none.
+ *
+ * Errors: invalid arguments are reported before anything is enqueued, and C is
+ * left unchanged.  The call returns after enqueueing; a fault during execution
+ * surfaces at the caller's next synchronisation, and a watchdog expiry (a
+ * pipeline wait that did not finish within the time limit) sets the device
+ * watchdog word read by gemm_f16_nt_device_status.
+ */
+gemm_status_t gemm_f16_nt(int64_t M, int64_t N, int64_t K,
+                          const uint16_t *A, int64_t lda,
+                          const uint16_t *B, int64_t ldb,
+                          uint16_t *C, int64_t ldc,
+                          void *stream);
+
+/*
+ * Tuning and test options for gemm_f16_nt_ex.  Zero in any field selects the
+ * default that gemm_f16_nt uses.
+ *
+ *   cta_group     2: a CTA pair computes one 256×256 tile with 2-SM MMAs and
+ *                 each CTA loads half of the shared B tile (default);
+ *                 1: one CTA computes a 128×256 tile on its own.
+ *   swizzle       width, in N tiles, of the groups of the tile raster; tiles
+ *                 in a group are visited row-major so that concurrently
+ *                 running tiles share B columns in L2 (Tilus tutorial
+ *                 "4. Pipeline Abstraction and Two Consumer Warp Groups",
+ *                 §Tile Rasterization).  Range 1..64.
+ *   max_clusters  upper bound on the persistent grid, in CTA pairs (or CTAs
+ *                 for cta_group 1); 0 = as many as can be resident.
+ *   timeout_ns    watchdog limit for any single pipeline wait, in ns
+ *                 (default 1 s).
+ *   inject_stall  test hook: if nonzero the TMA producers issue nothing, so
+ *                 every consumer wait runs into the watchdog; the kernel then
+ *                 sets the watchdog word, releases its tensor memory and
+ *                 exits without writing C.
+ */
+typedef struct {
+    int32_t cta_group;
+    int32_t swizzle;
+    int32_t max_clusters;
+    int32_t inject_stall;
+    uint64_t timeout_ns;
+} gemm_f16_nt_options_t;
+
+/* gemm_f16_nt with options (opts may be NULL).  Same arguments, layout,
+ * ownership and errors as gemm_f16_nt; an option out of range returns
+ * GEMM_ERR_INVALID_VALUE. */
+gemm_status_t gemm_f16_nt_ex(int64_t M, int64_t N, int64_t K,
+                             const uint16_t *A, int64_t lda,
+                             const uint16_t *B, int64_t ldb,
+                             uint16_t *C, int64_t ldc,
+                             void *stream, const gemm_f16_nt_options_t *opts);
+
+/*
+ * gemm_f16_nt_device_status — read and clear the current device's watchdog word.
+ *
+ * Synchronises `stream`, copies the word into *flags (may be NULL) and resets
+ * it to 0.  Returns GEMM_ERR_TIMEOUT if it was nonzero, GEMM_OK if it was 0,
+ * GEMM_ERR_LAUNCH if the synchronisation or copy failed (for example after an
+ * earlier fault), GEMM_ERR_UNSUPPORTED_DEVICE without a usable device.
+ * Bit 0 of the word: a wait expired.  Bit 7+s: wait site s expired, with
+ * s = 1 producer waiting for a free ring slot, 2 MMA issuer waiting for a
+ * filled slot, 3 MMA issuer waiting for a free accumulator, 4 epilogue waiting
+ * for a finished accumulator, 5 producer teardown waiting for its copies,
+ * 6 MMA teardown waiting for its MMAs.  The word is shared by every call on
+ * that device.
+ */
+gemm_status_t gemm_f16_nt_device_status(void *stream, uint32_t *flags);
+
+/* A static, human-readable name for a gemm_status_t value. */
+const char *gemm_f16_nt_status_string(int32_t status);
+
+/* ---- host-only helpers (no CUDA call; used by the scheduler and its tests) ---- */
+
+/*
+ * The launch plan gemm_f16_nt would use for a problem on a device with
+ * `num_sms` SMs and room for `max_clusters` resident clusters (0 = num_sms/2
+ * pairs, or num_sms CTAs for cta_group 1).  Returns GEMM_ERR_INVALID_VALUE for
+ * sizes out of range.
+ */
+typedef struct {
+    int32_t cta_group;     /* 1 or 2 */
+    int32_t tile_m;        /* rows of C per tile (128 · cta_group) */
+    int32_t tile_n;        /* columns of C per tile */
+    int32_t block_k;       /* k per pipeline stage */
+    int32_t stages;        /* shared-memory ring depth */
+    int32_t m_tiles;       /* cdiv(M, tile_m) */
+    int32_t n_tiles;       /* cdiv(N, tile_n) */
+    int32_t k_blocks;      /* cdiv(K, block_k) */
+    int64_t num_tiles;     /* m_tiles · n_tiles */
+    int32_t clusters;      /* persistent clusters launched */
+    int32_t grid_ctas;     /* clusters · cta_group */
+    int32_t swizzle;       /* raster group width actually used */
+    int32_t smem_bytes;    /* dynamic shared memory per CTA */
+    int32_t tmem_cols;     /* tensor-memory columns allocated per CTA */
+} gemm_f16_nt_plan_t;
+
+gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms,
+                               int32_t max_clusters,
+                               const gemm_f16_nt_options_t *opts,
+                               gemm_f16_nt_plan_t *plan);
+
+/*
+ * The tile raster: linear tile index -> (m_tile, n_tile).  N tiles are taken
+ * in groups of `swizzle` columns (the last group may be narrower); inside a
+ * group tiles go row-major.  A bijection of [0, m_tiles·n_tiles) onto the
+ * grid (Tilus tutorial "4. Pipeline Abstraction and Two Consumer Warp
+ * Groups", §Tile Rasterization).  This is the same function the kernel runs.
+ */
+gemm_status_t gemm_f16_nt_tile_coord(int64_t linear, int32_t m_tiles, int32_t n_tiles,
+                                     int32_t swizzle, int32_t *m_tile, int32_t *n_tile);
+
+/*
+ * The multiply-shift division the kernel uses for divisors fixed per launch
+ * (Granlund & Montgomery, "Division by Invariant Integers using
+ * Multiplication", 1994, round-up variant): quotient and remainder of n / d for
+ * 0 <= n < 2^31, 1 <= d < 2^31.
+ */
+gemm_status_t gemm_f16_nt_fast_divmod(uint32_t n, uint32_t d, uint32_t *q, uint32_t *r);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_F16_NT_H_ */

@@ -1,0 +1,205 @@
+"""Parity of the sm_103a GEMM (through the C ABI) with the CPU oracle.
+
+Every case compares the GPU result element by element with the oracle on the
+same seeded fp16 inputs, under |C_gpu - C_ref| <= 2 ulp16(|C_ref|) + 1e-4 sqrt(K)
+(bit-exact for small-integer inputs).  C is pre-filled with NaN so an element
+the kernel fails to write shows up, and padding columns/rows of every buffer
+must come back untouched.  After each case the device watchdog word must be 0.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from dense_fp16_gemm_gb300 import inputs
+from tests.gpu_util import empty_out, to_device, to_host
+from tests.tolerance import check_bitexact, check_close
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import dense_fp16_gemm_gb300 as g  # noqa: E402
+
+
+@pytest.fixture(autouse=True)
+def _needs_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+    assert g.device_status() == 0, "watchdog word set after the case"
+
+
+def run(A, B, *, lda=None, ldb=None, ldc=None, extra_rows=0, options=None, stream=None):
+    M, K = A.shape
+    N, _ = B.shape
+    Ad = to_device(A, lda)
+    Bd = to_device(B, ldb)
+    Cd, Cbuf = empty_out(M, N, ldc, extra_rows)
+    g.gemm_f16_nt(Ad, Bd, Cd, options=options, stream=stream)
+    torch.cuda.synchronize()
+    # margins: padding columns and extra rows of C untouched (still NaN)
+    pad = to_host(Cbuf)
+    assert np.isnan(pad[:M, N:].astype(np.float32)).all(), "padding columns of C were written"
+    assert np.isnan(pad[M:, :].astype(np.float32)).all(), "rows past M were written"
+    return to_host(Cd)
+
+
+def opts(cg, **kw):
+    return g.Options(cta_group=cg, **kw)
+
+
+SMALL = [(128, 256, 64), (256, 256, 256), (1, 1, 1), (1, 1, 8), (7, 9, 3), (300, 520, 328),
+         (513, 1025, 200), (1000, 700, 1000), (129, 257, 65), (64, 8, 4096), (255, 511, 63),
+         (2, 1000, 130)]
+
+
+@pytest.mark.parametrize("cg", [2, 1])
+@pytest.mark.parametrize("M,N,K", SMALL)
+def test_small_shapes(M, N, K, cg):
+    A = inputs.draw((M, K), inputs.U, 11 + M)
+    B = inputs.draw((N, K), inputs.U, 13 + N)
+    C = run(A, B, options=opts(cg))
+    check_close(C, oracle.gemm_f16_nt(A, B), K, f"{M}x{N}x{K} cg{cg}")
+
+
+@pytest.mark.parametrize("cg,max_clusters,swizzle", [(2, 1, 1), (2, 3, 3), (2, 5, 8), (2, 7, 64),
+                                                     (1, 1, 2), (1, 5, 8), (1, 11, 1)])
+def test_persistent_loop_many_tiles_per_cta(cg, max_clusters, swizzle):
+    # every CTA walks many tiles: ring phases and both TMEM buffers wrap many times
+    M, N, K = 1100, 2100, 520
+    A = inputs.draw((M, K), inputs.U, 21)
+    B = inputs.draw((N, K), inputs.U, 22)
+    C = run(A, B, options=opts(cg, max_clusters=max_clusters, swizzle=swizzle))
+    check_close(C, oracle.gemm_f16_nt(A, B), K, f"persistent cg{cg} mc{max_clusters} sw{swizzle}")
+
+
+@pytest.mark.parametrize("cg", [2, 1])
+def test_leading_dimensions_and_margins(cg):
+    # N % 8 != 0: the last columns are not a whole 16-byte unit of C's rows
+    M, N, K = 333, 601, 250
+    A = inputs.draw((M, K), inputs.U, 31)
+    B = inputs.draw((N, K), inputs.U, 32)
+    C = run(A, B, lda=K + 6 + 24, ldb=K + 6 + 8, ldc=N + 47, extra_rows=5, options=opts(cg))
+    check_close(C, oracle.gemm_f16_nt(A, B), K, "pitched")
+
+
+@pytest.mark.parametrize("cg", [2, 1])
+def test_integer_inputs_bit_exact_small(cg):
+    M, N, K = 700, 900, 3000
+    A = inputs.draw((M, K), inputs.I2, 41)
+    B = inputs.draw((N, K), inputs.I2, 42)
+    check_bitexact(run(A, B, options=opts(cg)), oracle.gemm_f16_nt(A, B), "int small")
+
+
+def test_identity_and_permutation_exact():
+    K = 512
+    A = inputs.draw((384, K), inputs.U, 51)
+    eye = np.eye(K, dtype=np.float16)
+    check_bitexact(run(A, eye), A, "identity")
+    pi = np.random.default_rng(3).permutation(K)
+    P = np.zeros((K, K), dtype=np.float16)
+    P[np.arange(K), pi] = 1.0
+    check_bitexact(run(A, P), A[:, pi], "permutation")
+
+
+def test_k_zero_writes_positive_zero():
+    M, N = 300, 200
+    Cd, Cbuf = empty_out(M, N, extra_rows=3)
+    Ad = torch.empty((M, 0), dtype=torch.float16, device="cuda:0")
+    Bd = torch.empty((N, 0), dtype=torch.float16, device="cuda:0")
+    g.gemm_f16_nt(Ad, Bd, Cd)
+    torch.cuda.synchronize()
+    c = to_host(Cd)
+    assert np.all(c.view(np.uint16) == 0)
+    assert np.isnan(to_host(Cbuf)[M:].astype(np.float32)).all()
+
+
+def test_empty_output_is_a_noop():
+    Cd, _ = empty_out(0, 64)
+    g.gemm_f16_nt(torch.empty((0, 64), dtype=torch.float16, device="cuda:0"),
+                  torch.empty((64, 64), dtype=torch.float16, device="cuda:0"), Cd)
+    torch.cuda.synchronize()
+
+
+def test_misaligned_device_pointer_rejected():
+    A = torch.zeros((64, 72), dtype=torch.float16, device="cuda:0")
+    B = torch.zeros((64, 64), dtype=torch.float16, device="cuda:0")
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_f16_nt(A[:, 1:65], B)          # starts 2 bytes into a row
+    assert e.value.status == 2
+
+
+def test_repeat_is_deterministic_and_other_stream():
+    M, N, K = 1024, 768, 1536
+    A = inputs.draw((M, K), inputs.U, 61)
+    B = inputs.draw((N, K), inputs.U, 62)
+    c1 = run(A, B)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        c2 = run(A, B, stream=s)
+    assert np.array_equal(c1.view(np.uint16), c2.view(np.uint16))
+
+
+def test_output_error_scale_unit_variance_k8192():
+    # Tilus tutorial, "6. Register Reallocation, Multicast, and a Persistent
+    # Kernel", §Shared-Memory Epilogue (Note): with fp32 accumulation and
+    # unit-variance outputs at K = 8192 the mean absolute error is 0.00014.
+    M, N, K = 512, 512, 8192
+    s = K ** -0.25
+    A = inputs.draw((M, K), ("normal", 0.0, s), 71)
+    B = inputs.draw((N, K), ("normal", 0.0, s), 72)
+    C = run(A, B).astype(np.float64)
+    S = oracle.gemm_f16_nt_f64(A, B)
+    mae = np.abs(C - S).mean()
+    assert 1.0e-4 < mae < 1.8e-4, mae
+    check_close(C.astype(np.float16), oracle.gemm_f16_nt(A, B), K, "unit variance")
+
+
+# ---------------------------------------------------------------------------
+# the benchmark workloads at full size
+# ---------------------------------------------------------------------------
+
+def sample_points(M, N, n_random=3000, seed=0):
+    """Corners, tile edges (multiples of 128/256 and their neighbours) and random
+    positions."""
+    rng = np.random.default_rng(seed)
+    edge_r = sorted({0, 1, M - 1, M - 2} | {min(max(v + d, 0), M - 1)
+                                               for v in range(0, M, 128) for d in (-1, 0)})
+    edge_c = sorted({0, 1, N - 1, N - 2} | {min(max(v + d, 0), N - 1)
+                                               for v in range(0, N, 256) for d in (-1, 0)})
+    rr = rng.choice(edge_r, 400)
+    cc = rng.choice(edge_c, 400)
+    rows = np.concatenate([rr, rng.integers(0, M, n_random), [0, 0, M - 1, M - 1]])
+    cols = np.concatenate([cc, rng.integers(0, N, n_random), [0, N - 1, 0, N - 1]])
+    return rows, cols
+
+
+def run_workload(name):
+    w = inputs.WORKLOADS[name]
+    A, B = inputs.operands(w)
+    Ad, Bd = to_device(A), to_device(B)
+    Cd, _ = empty_out(w.M, w.N)
+    g.gemm_f16_nt(Ad, Bd, Cd)
+    torch.cuda.synchronize()
+    return w, A, B, Cd
+
+
+@pytest.mark.parametrize("name", ["gemm_256", "gemm_4096", "ragged_4000x3000x5000"])
+def test_workload_full_check(name):
+    w, A, B, Cd = run_workload(name)
+    C = to_host(Cd)
+    check_close(C, oracle.gemm_f16_nt(A, B), w.K, name)
+
+
+def test_workload_ragged_integers_bit_exact():
+    w, A, B, Cd = run_workload("ragged_int_4000x3000x5000")
+    check_bitexact(to_host(Cd), oracle.gemm_f16_nt(A, B), w.name)
+
+
+@pytest.mark.parametrize("name", ["gemm_8192", "mlp_up_16384x14336x4096"])
+def test_workload_sampled(name):
+    w, A, B, Cd = run_workload(name)
+    C = to_host(Cd)
+    assert not np.isnan(C.astype(np.float32)).any(), "unwritten (NaN) elements in C"
+    rows, cols = sample_points(w.M, w.N)
+    ref, _ = oracle.gemm_f16_nt_points(A, B, rows, cols)
+    check_close(C[rows, cols], ref, w.K, name)

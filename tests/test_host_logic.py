@@ -1,0 +1,175 @@
+"""Host-side logic of the C-ABI library, on the CPU (no GPU needed).
+
+Covers: every function declared in include/*.h is exported; the tile raster is a
+bijection and reproduces the tutorial's worked wave example; the multiply-shift
+division; the launch plan; argument validation returns its error codes before
+any device work.
+"""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import dense_fp16_gemm_gb300 as g
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for fn in os.listdir(inc):
+        if fn.endswith(".h"):
+            text = open(os.path.join(inc, fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(gemm_f16_nt\w*)\s*\(", text))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = g.library()
+    names = declared_functions()
+    assert "gemm_f16_nt" in names and len(names) >= 7, names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_strings():
+    lib = g.library()
+    for code, name in g.STATUS.items():
+        assert lib.gemm_f16_nt_status_string(code).decode().startswith(name)
+    assert b"unknown" in lib.gemm_f16_nt_status_string(99)
+
+
+# ---------------------------------------------------------------------------
+# scheduler
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("d", list(range(1, 300)) + [1000, 4095, 4096, 4097, 65535, 65536,
+                                                      (1 << 30) - 1, 1 << 30, (1 << 30) + 1,
+                                                      (1 << 31) - 1, 1 << 31])
+def test_fast_divmod(d):
+    rng = np.random.default_rng(d)
+    ns = list(range(0, 2000)) + [(1 << 31) - 1, (1 << 31) - 2, d - 1, d, d + 1, 2 * d - 1, 2 * d]
+    ns += [int(x) for x in rng.integers(0, 1 << 31, 300)]
+    for n in ns:
+        if n < 0 or n >= (1 << 31):
+            continue
+        assert g.fast_divmod(n, d) == divmod(n, d), (n, d)
+
+
+def test_fast_divmod_rejects_out_of_range():
+    with pytest.raises(g.GemmError):
+        g.fast_divmod(5, 0)
+    with pytest.raises(g.GemmError):
+        g.fast_divmod(1 << 31, 3)
+
+
+@pytest.mark.parametrize("sw", [1, 2, 3, 4, 5, 8, 16, 64])
+def test_raster_is_bijection(sw):
+    for mt in range(1, 21):
+        for nt in range(1, 21):
+            seen = set()
+            for t in range(mt * nt):
+                m, n = g.tile_coord(t, mt, nt, sw)
+                assert 0 <= m < mt and 0 <= n < nt
+                seen.add((m, n))
+            assert len(seen) == mt * nt, (mt, nt, sw)
+
+
+def test_raster_groups_are_row_major_with_narrow_last_group():
+    # 5 x 7 grid, groups of 3 columns: groups {0,1,2}, {3,4,5}, {6} (narrower)
+    order = [g.tile_coord(t, 5, 7, 3) for t in range(35)]
+    assert order[:6] == [(0, 0), (0, 1), (0, 2), (1, 0), (1, 1), (1, 2)]
+    assert order[15:18] == [(0, 3), (0, 4), (0, 5)]
+    assert order[30:] == [(0, 6), (1, 6), (2, 6), (3, 6), (4, 6)]
+
+
+def test_raster_reproduces_the_pages_wave_example():
+    path = os.path.join(ROOT, "tests", "golden", "raster_wave_8x8.txt")
+    rows = [l.split() for l in open(path) if l.strip() and not l.startswith("#")]
+    assert len(rows) == 2
+    for r in rows:
+        mt, nt, wave, sw, a_rows, b_cols, strips = map(int, r)
+        tiles = [g.tile_coord(t, mt, nt, sw) for t in range(wave)]
+        am = {m for m, _ in tiles}
+        bn = {n for _, n in tiles}
+        assert (len(am), len(bn), len(am) + len(bn)) == (a_rows, b_cols, strips)
+
+
+def test_plan_headline_shape():
+    p = g.plan(8192, 8192, 8192, num_sms=152)
+    assert (p["cta_group"], p["tile_m"], p["tile_n"], p["block_k"]) == (2, 256, 256, 64)
+    assert (p["m_tiles"], p["n_tiles"], p["k_blocks"], p["num_tiles"]) == (32, 32, 128, 1024)
+    assert (p["clusters"], p["grid_ctas"]) == (76, 152)
+    assert p["smem_bytes"] <= 232448 and p["tmem_cols"] == 512
+    # 1024 tiles over 76 pairs: 13.47 rounds, the last one 47% full
+    assert abs(p["num_tiles"] / p["clusters"] - 13.47) < 0.01
+
+
+def test_plan_edges_and_options():
+    p = g.plan(4000, 3000, 5000)
+    assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (16, 12, 79)
+    p = g.plan(100, 100, 8)                        # one pair tile, rank-1 rows all out of range
+    assert (p["num_tiles"], p["clusters"], p["grid_ctas"]) == (1, 1, 2)
+    p1 = g.plan(4000, 3000, 5000, options=g.Options(cta_group=1))
+    assert (p1["tile_m"], p1["m_tiles"], p1["grid_ctas"]) == (128, 32, 152)
+    p = g.plan(8192, 8192, 8192, options=g.Options(max_clusters=3, swizzle=4))
+    assert (p["clusters"], p["swizzle"]) == (3, 4)
+    p = g.plan(8192, 300, 64, options=g.Options(swizzle=16))
+    assert p["swizzle"] == 2                         # clipped to the 2 N tiles
+    for bad in (g.Options(cta_group=3), g.Options(swizzle=65), g.Options(max_clusters=-1)):
+        with pytest.raises(g.GemmError):
+            g.plan(256, 256, 256, options=bad)
+    with pytest.raises(g.GemmError):
+        g.plan(-1, 5, 5)
+    with pytest.raises(g.GemmError):
+        g.plan(1 << 31, 5, 5)
+
+
+# ---------------------------------------------------------------------------
+# argument validation (returns before any CUDA call)
+# ---------------------------------------------------------------------------
+
+def call(M, N, K, a=0x10000, lda=None, b=0x20000, ldb=None, c=0x30000, ldc=None, opts=None):
+    lib = g.library()
+    lda = K if lda is None else lda
+    ldb = K if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    if opts is None:
+        return lib.gemm_f16_nt(M, N, K, a, lda, b, ldb, c, ldc, None)
+    return lib.gemm_f16_nt_ex(M, N, K, a, lda, b, ldb, c, ldc, None, opts)
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(M=-1, N=8, K=8), 1),
+    (dict(M=8, N=8, K=1 << 31), 1),
+    (dict(M=8, N=8, K=16, lda=8), 1),               # lda < K
+    (dict(M=8, N=8, K=16, ldb=8), 1),               # ldb < K
+    (dict(M=8, N=16, K=16, ldc=8), 1),              # ldc < N
+    (dict(M=8, N=8, K=16, a=0), 1),                 # NULL A
+    (dict(M=8, N=8, K=16, c=0), 1),                 # NULL C
+    (dict(M=8, N=8, K=16, a=0x10008), 2),           # A not 16-byte aligned
+    (dict(M=8, N=8, K=16, b=0x20002), 2),
+    (dict(M=8, N=8, K=16, c=0x30004), 2),
+    (dict(M=8, N=8, K=12, lda=12, ldb=16), 2),      # lda not a multiple of 8
+    (dict(M=8, N=12, K=16, ldc=12), 2),             # ldc not a multiple of 8
+    (dict(M=0, N=8, K=16, a=0, b=0, c=0), 0),       # empty output: no-op
+    (dict(M=8, N=0, K=16), 0),
+])
+def test_argument_validation(args, code):
+    assert call(**args) == code
+
+
+def test_bad_options_rejected():
+    assert call(8, 8, 16, opts=g.Options(cta_group=4)) == 1
+    assert call(8, 8, 16, opts=g.Options(swizzle=-1)) == 1
+
+
+def test_without_a_gpu_valid_calls_report_no_device():
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this case is for GPU-less hosts")
+    assert call(128, 128, 64) == 3
+    assert g.library().gemm_f16_nt_device_status(None, None) == 3

@@ -33,7 +33,8 @@ def _finite_grid():
     """All finite fp16 values as sorted (float64 value, bit pattern) arrays,
     one entry per value (-0 dropped)."""
     h = _ALL.view(np.float16)
-    v = h.astype(np.float64)
+    with np.errstate(invalid="ignore"):
+        v = h.astype(np.float64)
     ok = np.isfinite(v) & ~((_ALL == 0x8000))
     vals, bits = v[ok], _ALL[ok]
     order = np.argsort(vals, kind="stable")
