@@ -139,56 +139,113 @@ def recorded_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+    """Samples the SM clock, its maximum, board power and the clock-event
+    (throttle) reasons while the timed region runs.  Reads only: it queries
+    NVML through ctypes (libnvidia-ml ships with the driver) every few ms from a
+    background thread, and falls back to `nvidia-smi -lms` if NVML cannot be
+    loaded.  Each sample carries a host timestamp so that only samples taken
+    inside a timed window are summarised."""
 
-    def __init__(self, gpu_index: int, period_ms: int = 100):
-        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
-        self.proc = None
+    # clock-event reason bits of the NVML API
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, gpu_index: int, period_s: float = 0.005):
+        import threading
+        self.samples = []          # (t, sm_mhz, max_mhz, power_w, reason_bits)
+        self.windows = []
+        self._stop = threading.Event()
+        self._smi = None
+        self._nvml = self._open_nvml(gpu_index)
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._poll, args=(period_s,), daemon=True)
+            self._thread.start()
+        else:
+            self._thread = None
+            self._start_smi(gpu_index)
+
+    def _open_nvml(self, idx):
+        import ctypes
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={SMI_FIELDS}", "--format=csv,noheader,nounits",
-                 "-i", str(gpu_index), "-lms", str(period_ms)],
-                stdout=self.f, stderr=subprocess.DEVNULL)
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return None
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(h)) != 0:
+                return None
+            return lib, h
         except OSError:
-            self.proc = None
+            return None
+
+    def _poll(self, period):
+        import ctypes
+        lib, h = self._nvml
+        mhz, mx, mw = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint()
+        bits = ctypes.c_ulonglong()
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        while not self._stop.is_set():
+            t = time.time()
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0 and \
+                    lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                pw = mw.value / 1e3 if lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) == 0 else 0.0
+                rb = bits.value if get_reasons(h, ctypes.byref(bits)) == 0 else 0
+                self.samples.append((t, float(mhz.value), float(mx.value), pw, int(rb)))
+            time.sleep(period)
+
+    def _start_smi(self, idx):
+        self._f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self._smi = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu=timestamp,{SMI_FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(idx), "-lms", "50"], stdout=self._f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self._smi = None
+
+    def window(self, t0: float, t1: float):
+        self.windows.append((t0, t1))
 
     def stop(self):
-        if self.proc is not None:
-            self.proc.terminate()
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
+        if self._smi is not None:
+            import datetime
+            self._smi.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self._smi.wait(timeout=5)
             except subprocess.TimeoutExpired:
-                self.proc.kill()
-        self.f.flush()
-        self.f.seek(0)
-        rows = [l.strip().split(",") for l in self.f.read().splitlines() if l.strip()]
-        self.f.close()
-        os.unlink(self.f.name)
-        return rows
+                self._smi.kill()
+            self._f.flush()
+            self._f.seek(0)
+            names = {5: 0x8, 6: 0x40, 7: 0x20, 8: 0x4}
+            for line in self._f.read().splitlines():
+                r = [x.strip() for x in line.split(",")]
+                if len(r) < 10:
+                    continue
+                try:
+                    t = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rb = sum(bit for col, bit in names.items() if r[col + 1].lower() == "active")
+                    self.samples.append((t, float(r[2]), float(r[3]), float(r[4]), rb))
+                except ValueError:
+                    continue
+            self._f.close()
+            os.unlink(self._f.name)
+        return self.summary()
 
-
-def summarize_clocks(rows):
-    sm, smax, power, reasons = [], [], [], set()
-    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-    for r in rows:
-        r = [x.strip() for x in r]
-        if len(r) < 9:
-            continue
-        try:
-            sm.append(float(r[1]))
-            smax.append(float(r[2]))
-            power.append(float(r[3]))
-        except ValueError:
-            continue
-        for name, v in zip(names, r[5:9]):
-            if v.lower() == "active":
-                reasons.add(name)
-    if not sm:
-        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-    loaded = [s for s, p in zip(sm, power) if p > 0.5 * max(power)] or sm
-    return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
-            "reasons": sorted(reasons), "samples": len(sm),
-            "power_w_max": max(power)}
+    def summary(self):
+        inside = [s for s in self.samples if any(a <= s[0] <= b for a, b in self.windows)]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "source": "nvml" if self._nvml else "nvidia-smi"}
+        reasons = set()
+        for s in inside:
+            reasons |= {name for bit, name in self.REASONS.items() if s[4] & bit}
+        return {"sm_mhz": statistics.median(s[1] for s in inside),
+                "sm_mhz_min": min(s[1] for s in inside),
+                "sm_max_mhz": max(s[2] for s in inside), "reasons": sorted(reasons),
+                "samples": len(inside), "power_w_median": statistics.median(s[3] for s in inside),
+                "source": "nvml" if self._nvml else "nvidia-smi"}
 
 
 # ---------------------------------------------------------------------------
@@ -224,6 +281,28 @@ def workload_config(w):
             "accumulate": "f32", "inputs": f"A {w.dist_a}, B {w.dist_b}, seeds {w.seed_a},{w.seed_b}",
             "l2": f"operands larger than L2: A+B+C = {w.compulsory_bytes / 2**20:.0f} MiB > 129 MB",
             "parallelism": "replicas"}
+
+
+def cublas_context(A_d, B_d, steps: int, stream):
+    """torch.matmul on the same operands and stream, fp32 accumulation kept
+    (reduced-precision reductions off), timed the same way: context only."""
+    import torch
+    prev = torch.backends.cuda.matmul.allow_fp16_reduced_precision_reduction
+    torch.backends.cuda.matmul.allow_fp16_reduced_precision_reduction = False
+    try:
+        out = torch.empty((A_d.shape[0], B_d.shape[0]), dtype=torch.float16, device=A_d.device)
+        for _ in range(3):
+            torch.matmul(A_d, B_d.t(), out=out)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            torch.matmul(A_d, B_d.t(), out=out)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / steps
+    finally:
+        torch.backends.cuda.matmul.allow_fp16_reduced_precision_reduction = prev
 
 
 def run_ours(args, w):
@@ -271,6 +350,7 @@ def run_ours(args, w):
         t_end = torch.cuda.Event(enable_timing=True)
         barrier(dist, device)
         torch.cuda.synchronize(device)
+        w0 = time.time()
         t_start.record(stream)
         for i in range(args.steps):
             evs[i][0].record(stream)
@@ -278,10 +358,13 @@ def run_ours(args, w):
             evs[i][1].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize(device)
+        w1 = time.time()
         barrier(dist, device)
+        if sampler:
+            sampler.window(w0, w1)
         times.append(t_start.elapsed_time(t_end) / 1e3)
         launch_ms.extend(a.elapsed_time(b) for a, b in evs)
-    clocks = summarize_clocks(sampler.stop()) if sampler else None
+    clocks = sampler.stop() if sampler else None
     if g.device_status(stream) != 0:
         raise SystemExit("bench.py: watchdog word set during the timed region")
 
@@ -321,6 +404,14 @@ def run_ours(args, w):
     if torch.isnan(Ch).any().item():
         raise SystemExit("bench.py: end-to-end result has unwritten elements")
 
+    context = None
+    if rank == 0 and not args.no_cublas:
+        time.sleep(args.cooldown)
+        t_cublas = cublas_context(Ad, Bd, max(args.steps, 10), stream)
+        context = {"torch_matmul_cublas_tflops": round(w.flops / t_cublas / 1e12, 2),
+                   "note": "same operands, same stream, fp32 accumulation; run as a library, "
+                           "context only (not the target, not part of the value)"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle_sample(w, A, B, args.cpu_seconds)
@@ -346,6 +437,7 @@ def run_ours(args, w):
             "timing": {"repeats": args.repeat, "cooldown_s": args.cooldown,
                        "per_repeat_ms_per_step": [round(t / args.steps * 1e3, 4) for t in times]},
             "cpu_baseline": cpu,
+            "context": context,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -391,7 +483,7 @@ def run_reference(args, w):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gemm_8192", choices=sorted(inputs.WORKLOADS))
@@ -399,6 +491,8 @@ def main(argv=None):
     ap.add_argument("--cooldown", type=float, default=1.0, help="seconds of idle before each repeat")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cublas", action="store_true",
+                    help="skip the torch.matmul (cuBLAS) context measurement")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

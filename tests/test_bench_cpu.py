@@ -1,0 +1,79 @@
+"""bench.py on the CPU: the replica aggregation across ranks (two gloo
+processes) and the CPU-oracle reference arm."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    dist = bench.init_dist(world, "gloo")
+    bench.barrier(dist)
+    # rank r "took" 1 + r seconds for 10·(r+1) units of work
+    t, w = bench.reduce_time_and_work(dist, 1.0 + rank, 10.0 * (rank + 1))
+    q.put((rank, t, w))
+    bench.barrier(dist)
+    dist.destroy_process_group()
+
+
+def test_replica_timing_is_max_over_ranks_and_work_sums():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, t, w in out:
+        assert t == 2.0 and w == 30.0, (rank, t, w)
+
+
+def _bench(args, env=None):
+    e = dict(os.environ)
+    e.update(env or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args],
+                          capture_output=True, text=True, env=e, timeout=600, cwd=ROOT)
+
+
+def test_reference_arm_prints_one_line():
+    r = _bench(["--impl", "reference", "--workload", "gemm_256", "--steps", "3", "--warmup", "3",
+                "--cpu-seconds", "1"])
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "TFLOP/s"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"] == "gemm_256" and d["higher_is_better"] is True
+
+
+def test_reference_arm_non_zero_rank_is_silent():
+    r = _bench(["--impl", "reference", "--workload", "gemm_256", "--steps", "3", "--warmup", "3",
+                "--gpus", "2"], env={"WORLD_SIZE": "2", "RANK": "1", "LOCAL_RANK": "1"})
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
+
+
+def test_warmup_floor_enforced():
+    r = _bench(["--impl", "reference", "--workload", "gemm_256", "--steps", "3", "--warmup", "2"])
+    assert r.returncode != 0
