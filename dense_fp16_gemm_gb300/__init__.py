@@ -18,7 +18,7 @@ import os
 
 from . import _build_ext
 
-__all__ = ["gemm_f16_nt", "gemm_f16_nt_ptr", "device_status", "plan", "tile_coord",
+__all__ = ["gemm_f16_nt", "gemm_f16_nt_ptr", "device_status", "device_limits", "plan", "tile_coord",
            "fast_divmod", "GemmError", "Options", "Plan", "library", "STATUS"]
 
 STATUS = {
@@ -43,7 +43,8 @@ class Options(ctypes.Structure):
     """gemm_f16_nt_options_t (zero = default in every field)."""
     _fields_ = [("cta_group", ctypes.c_int32), ("swizzle", ctypes.c_int32),
                 ("max_clusters", ctypes.c_int32), ("inject_stall", ctypes.c_int32),
-                ("timeout_ns", ctypes.c_uint64)]
+                ("timeout_ns", ctypes.c_uint64), ("schedule", ctypes.c_int32),
+                ("trace_items", ctypes.c_int32), ("trace", ctypes.c_void_p)]
 
 
 class Plan(ctypes.Structure):
@@ -54,10 +55,12 @@ class Plan(ctypes.Structure):
                 ("n_tiles", ctypes.c_int32), ("k_blocks", ctypes.c_int32),
                 ("num_tiles", ctypes.c_int64), ("clusters", ctypes.c_int32),
                 ("grid_ctas", ctypes.c_int32), ("swizzle", ctypes.c_int32),
-                ("smem_bytes", ctypes.c_int32), ("tmem_cols", ctypes.c_int32)]
+                ("smem_bytes", ctypes.c_int32), ("tmem_cols", ctypes.c_int32),
+                ("sk_tiles", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_int64)]
 
     def as_dict(self):
-        return {f: getattr(self, f) for f, _ in self._fields_}
+        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
 
 
 _lib = None
@@ -93,6 +96,8 @@ def library(path: str | None = None):
         lib.gemm_f16_nt_fast_divmod.argtypes = [_u32, _u32, ctypes.POINTER(_u32),
                                                 ctypes.POINTER(_u32)]
         lib.gemm_f16_nt_fast_divmod.restype = ctypes.c_int
+        lib.gemm_f16_nt_device_limits.argtypes = [ctypes.POINTER(_i32)] * 3
+        lib.gemm_f16_nt_device_limits.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -170,6 +175,14 @@ def device_status(stream=None) -> int:
     if st not in (0, 5):
         raise GemmError(st, "gemm_f16_nt_device_status")
     return int(flags.value)
+
+
+def device_limits() -> dict:
+    """SM count and resident CTA pairs / CTAs of the current device."""
+    a, b, c = _i32(0), _i32(0), _i32(0)
+    _check(library().gemm_f16_nt_device_limits(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
+           "gemm_f16_nt_device_limits")
+    return {"sms": a.value, "resident_pairs": b.value, "resident_ctas": c.value}
 
 
 def plan(M: int, N: int, K: int, num_sms: int = 152, max_clusters: int = 0,

@@ -35,6 +35,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "gemm_f16_nt.h"
@@ -64,7 +65,11 @@ enum : uint32_t {
     kSiteEpiAccFull = 4,
     kSiteProducerDrain = 5,
     kSiteMmaDrain = 6,
+    kSiteStreamK = 7,
 };
+
+// Work items (see work_next)
+enum : uint32_t { kItemWhole = 0, kItemPartialOut = 1, kItemOwner = 2 };
 
 __device__ uint32_t g_watchdog_word;
 
@@ -122,6 +127,14 @@ struct Params {
     uint64_t timeout_ns;
     uint32_t* watchdog;
     int32_t inject_stall;
+    // stream-K part of the schedule (0 tiles = purely data-parallel)
+    uint32_t sk_tiles;     // tiles [0, sk_tiles) are cut into k-block units
+    uint64_t sk_units;     // sk_tiles * num_kb
+    float* partials;       // [cluster][cta rank][BN/4][128 rows] float4 partial tiles
+    uint64_t* flags;       // [cluster][cta rank][epilogue warp]: launch_id once written
+    uint64_t launch_id;    // unique per launch, so stale flags never match
+    uint64_t* trace;       // optional per-item timestamps (debugging)
+    uint32_t trace_items;
 };
 
 // ---------------------------------------------------------------------------
@@ -186,6 +199,88 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
     return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
            (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+// ---------------------------------------------------------------------------
+// work schedule
+// ---------------------------------------------------------------------------
+//
+// The tiles [0, sk_tiles) form the stream-K part: their sk_tiles * num_kb
+// k-block units are split into G equal contiguous ranges, one per cluster, so
+// the last, partly filled wave of a purely tile-parallel schedule is spread
+// over every cluster.  The rest of the tiles go round-robin, whole.  A range
+// may start or end inside a tile:
+//   - a piece that does not start at k-block 0 (only ever a cluster's first
+//     item) is written as an fp32 partial tile to the cluster's workspace slot
+//     and published with a release flag;
+//   - the piece that starts at k-block 0 but stops early is the tile's owner:
+//     it waits for the partials of the clusters that took the rest of the tile
+//     (the next ones in order), adds them in that order and stores C.
+// Owner pieces come at the end of a cluster's range and partial pieces at the
+// start, so an owner seldom waits.
+
+struct Item {
+    uint32_t tile;
+    uint32_t kb0, kb1;   // k-block range [kb0, kb1)
+    uint32_t kind;
+};
+
+struct Work {
+    uint64_t u, u_end;   // this cluster's stream-K units still to do
+    uint32_t t;          // next whole tile
+    uint32_t G;          // clusters
+};
+
+__device__ __forceinline__ uint64_t sk_begin(const Params& p, uint32_t c, uint32_t G) {
+    return p.sk_units * c / G;
+}
+
+__device__ __forceinline__ void work_init(Work& s, const Params& p, uint32_t c, uint32_t G) {
+    s.u = sk_begin(p, c, G);
+    s.u_end = sk_begin(p, c + 1, G);
+    s.t = p.sk_tiles + c;
+    s.G = G;
+}
+
+__device__ __forceinline__ bool work_next(Work& s, const Params& p, Item& it) {
+    if (s.u < s.u_end) {
+        const uint32_t t = uint32_t(s.u / p.num_kb);
+        const uint32_t kb0 = uint32_t(s.u - uint64_t(t) * p.num_kb);
+        const uint64_t left = s.u_end - s.u;
+        const uint32_t kb1 = left >= uint64_t(p.num_kb - kb0) ? p.num_kb : kb0 + uint32_t(left);
+        it.tile = t;
+        it.kb0 = kb0;
+        it.kb1 = kb1;
+        it.kind = kb0 > 0 ? kItemPartialOut : (kb1 < p.num_kb ? kItemOwner : kItemWhole);
+        s.u += kb1 - kb0;
+        return true;
+    }
+    if (s.t < p.num_tiles) {
+        it.tile = s.t;
+        it.kb0 = 0;
+        it.kb1 = p.num_kb;
+        it.kind = kItemWhole;
+        s.t += s.G;
+        return true;
+    }
+    return false;
+}
+
+// Wait until *flag == want (the partner's release store); false on watchdog.
+__device__ __noinline__ bool wait_flag(const uint64_t* flag, uint64_t want, const Watch w,
+                                       uint32_t site) {
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (ptx::ld_acquire_u64(flag) == want) return true;
+        if ((i & 15u) == 0) {
+            if (*w.abort_flag) return false;
+            if (ptx::globaltimer() - t0 > w.limit_ns) {
+                raise_abort(w, site);
+                return false;
+            }
+        }
+        __nanosleep(64);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -258,12 +353,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
             const uint32_t full_tgt = CG == 2 ? ptx::mapa(full0, 0) : full0;
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
-            for (uint32_t t = cluster; ok && t < p.num_tiles; t += nclusters) {
+            Work work;
+            Item it;
+            work_init(work, p, cluster, nclusters);
+            while (ok && work_next(work, p, it)) {
                 uint32_t mt, nt;
-                raster_coord(p.raster, t, mt, nt);
+                raster_coord(p.raster, it.tile, mt, nt);
                 const int32_t m0 = int32_t(mt * Cfg::kTileM + rank * kBlockM);
                 const int32_t n0 = int32_t(nt * BN + rank * Cfg::kBRows);
-                for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+                for (uint32_t kb = it.kb0; kb < it.kb1; ++kb) {
                     if (!wait(empty0 + 8 * stage, phase ^ 1u, w, kSiteProducerEmpty)) {
                         ok = false;
                         break;
@@ -311,11 +409,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
         if (lane == 0 && rank == 0) {
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
-            for (uint32_t t = cluster; ok && t < p.num_tiles; t += nclusters) {
+            Work work;
+            Item it;
+            work_init(work, p, cluster, nclusters);
+            uint32_t item_no = 0;
+            while (ok && work_next(work, p, it)) {
                 if (!wait(acce0 + 8 * acc, acc_phase ^ 1u, w, kSiteMmaAccFree)) break;
                 ptx::tc_fence_after();
+                uint64_t* tr = (p.trace && item_no < p.trace_items)
+                                   ? p.trace + (size_t(cluster) * p.trace_items + item_no) * 8 : nullptr;
+                if (tr) {
+                    tr[0] = uint64_t(it.tile) | (uint64_t(it.kind) << 32);
+                    tr[1] = uint64_t(it.kb0) | (uint64_t(it.kb1) << 32);
+                    tr[2] = ptx::globaltimer();
+                }
+                ++item_no;
                 const uint32_t d = tmem_base + acc * uint32_t(BN);
-                for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+                for (uint32_t kb = it.kb0; kb < it.kb1; ++kb) {
                     if (!wait(full0 + 8 * stage, phase, w, kSiteMmaFull)) {
                         ok = false;
                         break;
@@ -326,7 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
 #pragma unroll
                     for (int k = 0; k < kBlockK / kUmmaK; ++k) {
                         const uint64_t koff = uint64_t((k * kUmmaK * 2) >> 4);
-                        ptx::mma_f16<CG>(d, ad + koff, bd + koff, Cfg::kIdesc, (kb | uint32_t(k)) != 0u);
+                        ptx::mma_f16<CG>(d, ad + koff, bd + koff, Cfg::kIdesc,
+                                         (kb != it.kb0 || k != 0) ? 1u : 0u);
                     }
                     // Free this ring slot in every CTA of the pair once these MMAs retire.
                     if constexpr (CG == 2) ptx::mma_commit_pair(empty0 + 8 * stage, 0x3);
@@ -339,6 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                 if (!ok) break;
                 if constexpr (CG == 2) ptx::mma_commit_pair(accf0 + 8 * acc, 0x3);
                 else ptx::mma_commit(accf0 + 8 * acc);
+                if (tr) tr[3] = ptx::globaltimer();
                 acc ^= 1u;
                 if (acc == 0) acc_phase ^= 1u;
             }
@@ -354,17 +466,48 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
         const uint32_t lane_off = (q * 32u) << 16;
         const uint32_t out0 = sOut + (warp - 2u) * kOutBufs * kOutBufBytes;
         const uint32_t acce_tgt = CG == 2 ? ptx::mapa(acce0, 0) : acce0;
+        // A partial tile in workspace slot `slot` is stored as float4 groups of
+        // columns, row innermost: [col/4][128 rows], so that the 32 lanes of a
+        // warp (32 consecutive rows) touch 512 contiguous bytes per access.
+        auto partial_f4 = [&](uint32_t slot, uint32_t col4) {
+            return reinterpret_cast<float4*>(p.partials) +
+                   ((size_t(slot) * CG + rank) * (BN / 4) + col4) * kBlockM + q * 32u + lane;
+        };
         uint32_t acc = 0, acc_phase = 0, ob = 0;
-        for (uint32_t t = cluster; t < p.num_tiles; t += nclusters) {
+        Work work;
+        Item it;
+        work_init(work, p, cluster, nclusters);
+        uint32_t item_no = 0;
+        while (work_next(work, p, it)) {
             uint32_t mt, nt;
-            raster_coord(p.raster, t, mt, nt);
+            raster_coord(p.raster, it.tile, mt, nt);
             const int32_t row0 = int32_t(mt * Cfg::kTileM + rank * kBlockM + q * 32u);
             const int32_t col0 = int32_t(nt * BN);
+            uint64_t* tr = (p.trace && item_no < p.trace_items && rank == 0 && warp == 2 && lane == 0)
+                               ? p.trace + (size_t(cluster) * p.trace_items + item_no) * 8 : nullptr;
+            ++item_no;
             uint32_t ok = 0;
             if (lane == 0) ok = wait(accf0 + 8 * acc, acc_phase, w, kSiteEpiAccFull) ? 1u : 0u;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             ptx::tc_fence_after();
+            if (tr) tr[4] = ptx::globaltimer();
+            // An owner adds the partials of the clusters that took the rest of its tile.
+            uint32_t npart = 0;
+            if (it.kind == kItemOwner) {
+                const uint64_t tile_end = uint64_t(it.tile + 1) * p.num_kb;
+                while (cluster + 1 + npart < nclusters && sk_begin(p, cluster + 1 + npart, nclusters) < tile_end)
+                    ++npart;
+                uint32_t okf = 1;
+                if (lane == 0)
+                    for (uint32_t i = 0; i < npart && okf; ++i)
+                        okf = wait_flag(p.flags + (size_t(cluster + 1 + i) * CG + rank) * kEpiWarps + q,
+                                        p.launch_id, w, kSiteStreamK) ? 1u : 0u;
+                okf = __shfl_sync(0xffffffffu, okf, 0);
+                if (!okf) break;
+                __threadfence();
+            }
+            if (tr) tr[5] = ptx::globaltimer();
             const uint32_t tacc = tmem_base + lane_off + acc * uint32_t(BN);
 #pragma unroll 1
             for (int c = 0; c < BN / kEpiCols; ++c) {
@@ -379,6 +522,40 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                     if (lane == 0) {
                         if constexpr (CG == 2) ptx::mbar_arrive_cluster(acce_tgt + 8 * acc);
                         else ptx::mbar_arrive(acce0 + 8 * acc);
+                    }
+                }
+                if (it.kind == kItemPartialOut) {
+                    // fp32 partial: 16 float4 groups of this lane's row, 64 columns
+                    float4* dst = partial_f4(cluster, uint32_t(c * kEpiCols / 4));
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        __stcg(dst + size_t(j) * kBlockM,
+                               make_float4(__uint_as_float(lo[4 * j]), __uint_as_float(lo[4 * j + 1]),
+                                           __uint_as_float(lo[4 * j + 2]), __uint_as_float(lo[4 * j + 3])));
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        __stcg(dst + size_t(8 + j) * kBlockM,
+                               make_float4(__uint_as_float(hi[4 * j]), __uint_as_float(hi[4 * j + 1]),
+                                           __uint_as_float(hi[4 * j + 2]), __uint_as_float(hi[4 * j + 3])));
+                    continue;
+                }
+                for (uint32_t i = 0; i < npart; ++i) {   // k order: this piece, then each partner
+                    const float4* src = partial_f4(cluster + 1 + i, uint32_t(c * kEpiCols / 4));
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 v = __ldcg(src + size_t(j) * kBlockM);
+                        lo[4 * j] = __float_as_uint(__uint_as_float(lo[4 * j]) + v.x);
+                        lo[4 * j + 1] = __float_as_uint(__uint_as_float(lo[4 * j + 1]) + v.y);
+                        lo[4 * j + 2] = __float_as_uint(__uint_as_float(lo[4 * j + 2]) + v.z);
+                        lo[4 * j + 3] = __float_as_uint(__uint_as_float(lo[4 * j + 3]) + v.w);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 v = __ldcg(src + size_t(8 + j) * kBlockM);
+                        hi[4 * j] = __float_as_uint(__uint_as_float(hi[4 * j]) + v.x);
+                        hi[4 * j + 1] = __float_as_uint(__uint_as_float(hi[4 * j + 1]) + v.y);
+                        hi[4 * j + 2] = __float_as_uint(__uint_as_float(hi[4 * j + 2]) + v.z);
+                        hi[4 * j + 3] = __float_as_uint(__uint_as_float(hi[4 * j + 3]) + v.w);
                     }
                 }
                 uint32_t h[32];
@@ -420,6 +597,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                 }
                 ob ^= 1u;
             }
+            if (it.kind == kItemPartialOut) {
+                // publish: every lane's partial stores before the flag
+                __threadfence();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::st_release_u64(p.flags + (size_t(cluster) * CG + rank) * kEpiWarps + q, p.launch_id);
+            }
+            if (tr) tr[6] = ptx::globaltimer();
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
@@ -462,12 +647,16 @@ struct DeviceState {
     int max_clusters2 = 0;   // resident CTA pairs for Cfg2
     int max_ctas1 = 0;       // resident CTAs for Cfg1
     uint32_t* watchdog = nullptr;
+    cudaMemPool_t pool = nullptr;   // private stream-ordered pool for stream-K workspaces
 };
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 EncodeTiledFn g_encode = nullptr;
+std::atomic<uint64_t> g_launch_seq{0};
+
+constexpr int kMinSplitKb = 8;   // smallest stream-K share worth its fix-up, in k-blocks
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -536,6 +725,19 @@ gemm_status_t setup_device(int dev, DeviceState& st) {
     }
     st.watchdog = static_cast<uint32_t*>(wd);
     st.sms = sms;
+    // Workspaces come from a pool of this library's own, on the caller's stream,
+    // and stay cached in it between calls.
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    if (cudaMemPoolCreate(&st.pool, &props) != cudaSuccess) {
+        cudaGetLastError();
+        st.pool = nullptr;
+    } else {
+        uint64_t keep = UINT64_MAX;
+        cudaMemPoolSetAttribute(st.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    }
     return GEMM_OK;
 }
 
@@ -573,6 +775,15 @@ gemm_status_t check_args(int64_t M, int64_t N, int64_t K, const uint16_t* A, int
     return GEMM_OK;
 }
 
+// Stream-K workspace: flags first ([cluster][rank][warp] uint64, 256-byte
+// aligned), then the fp32 partial tiles ([cluster][rank][tile_n/4][128] float4).
+int64_t flags_bytes(int cg, int64_t clusters) {
+    return (clusters * cg * kEpiWarps * 8 + 255) / 256 * 256;
+}
+int64_t workspace_bytes(int cg, int tile_n, int64_t clusters) {
+    return flags_bytes(cg, clusters) + clusters * cg * int64_t(kBlockM) * tile_n * 4;
+}
+
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t max_resident,
                         const gemm_f16_nt_options_t* o, gemm_f16_nt_plan_t* pl) {
     const int64_t lim = int64_t(1) << 31;
@@ -580,7 +791,9 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
         return GEMM_ERR_INVALID_VALUE;
     const int cg = (o && o->cta_group) ? o->cta_group : 2;
     const int sw = (o && o->swizzle) ? o->swizzle : kDefaultSwizzle;
-    if ((cg != 1 && cg != 2) || sw < 1 || sw > 64 || (o && o->max_clusters < 0))
+    const int sched = o ? o->schedule : 0;
+    if ((cg != 1 && cg != 2) || sw < 1 || sw > 64 || (o && o->max_clusters < 0) || sched < 0 ||
+        sched > 2)
         return GEMM_ERR_INVALID_VALUE;
     memset(pl, 0, sizeof(*pl));
     pl->cta_group = cg;
@@ -601,9 +814,36 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
     int64_t resident = max_resident > 0 ? max_resident : (cg == 2 ? num_sms / 2 : num_sms);
     if (resident < 1) resident = 1;
     if (o && o->max_clusters > 0 && o->max_clusters < resident) resident = o->max_clusters;
-    const int64_t clusters = tiles < resident ? tiles : resident;
+
+    // Schedule.  Whole tiles round-robin over the clusters leave the last wave
+    // partly empty when tiles % clusters != 0.  The stream-K part spreads the
+    // k-block units of (the partial wave + one full wave) evenly instead; with
+    // fewer tiles than clusters it spreads all of them.  Auto mode (0) uses it
+    // when the last wave is at most 90 % full and every share keeps at least
+    // kMinSplitKb k-blocks; 1 = whole tiles only; 2 = stream-K whenever it can.
+    const int64_t kb = pl->k_blocks;
+    int64_t clusters = tiles < resident ? tiles : resident;
+    int64_t sk_tiles = 0;
+    if (tiles > 0 && kb > 0 && sched != 1) {
+        if (tiles >= resident) {
+            const int64_t rem = tiles % resident;
+            const bool worth = rem != 0 && rem * 10 <= resident * 9 && kb >= kMinSplitKb;
+            if (sched == 2 || worth) sk_tiles = rem + resident;
+            if (sk_tiles > tiles) sk_tiles = tiles;
+        } else {
+            int64_t g = tiles * kb / kMinSplitKb;      // clusters that still get kMinSplitKb each
+            if (sched == 2) g = tiles * kb;            // forced: up to one k-block each
+            if (g > resident) g = resident;
+            if (g > tiles) {
+                clusters = g;
+                sk_tiles = tiles;
+            }
+        }
+    }
     pl->clusters = int32_t(clusters);
     pl->grid_ctas = int32_t(clusters * cg);
+    pl->sk_tiles = int32_t(sk_tiles);
+    pl->workspace_bytes = sk_tiles > 0 ? workspace_bytes(cg, pl->tile_n, clusters) : 0;
     return GEMM_OK;
 }
 
@@ -622,7 +862,8 @@ gemm_status_t encode_2d(CUtensorMap* tm, const void* ptr, uint64_t inner, uint64
 template <class Cfg>
 gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t K, const uint16_t* A,
                      int64_t lda, const uint16_t* B, int64_t ldb, uint16_t* C, int64_t ldc,
-                     cudaStream_t stream, const gemm_f16_nt_options_t* o, uint32_t* watchdog) {
+                     cudaStream_t stream, const gemm_f16_nt_options_t* o, uint32_t* watchdog,
+                     void* workspace) {
     Params p;
     memset(&p, 0, sizeof(p));
     gemm_status_t s;
@@ -645,6 +886,18 @@ gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t
     p.timeout_ns = (o && o->timeout_ns) ? o->timeout_ns : kDefaultTimeoutNs;
     p.watchdog = watchdog;
     p.inject_stall = o ? o->inject_stall : 0;
+    p.sk_tiles = uint32_t(pl.sk_tiles);
+    p.sk_units = uint64_t(pl.sk_tiles) * uint64_t(pl.k_blocks);
+    if (pl.sk_tiles > 0) {
+        uint8_t* ws = static_cast<uint8_t*>(workspace);
+        p.flags = reinterpret_cast<uint64_t*>(ws);
+        p.partials = reinterpret_cast<float*>(ws + flags_bytes(Cfg::kCG, pl.clusters));
+    }
+    p.launch_id = ++g_launch_seq;
+    if (o && o->trace && o->trace_items > 0) {
+        p.trace = o->trace;
+        p.trace_items = uint32_t(o->trace_items);
+    }
 
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -672,7 +925,8 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t ld
     gemm_status_t s = check_args(M, N, K, A, lda, B, ldb, C, ldc);
     if (s != GEMM_OK) return s;
     if (o && ((o->cta_group != 0 && o->cta_group != 1 && o->cta_group != 2) || o->swizzle < 0 ||
-              o->swizzle > 64 || o->max_clusters < 0))
+              o->swizzle > 64 || o->max_clusters < 0 || o->schedule < 0 || o->schedule > 2 ||
+              o->trace_items < 0 || (o->trace && (reinterpret_cast<uintptr_t>(o->trace) & 7))))
         return GEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return GEMM_OK;
     DeviceState* st = nullptr;
@@ -688,10 +942,27 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t ld
     }
     const int cg = (o && o->cta_group) ? o->cta_group : 2;
     gemm_f16_nt_plan_t pl;
-    if ((s = make_plan(M, N, K, st->sms, cg == 2 ? st->max_clusters2 : st->max_ctas1, o, &pl)) != GEMM_OK)
-        return s;
-    if (cg == 2) return launch<Cfg2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, o, st->watchdog);
-    return launch<Cfg1>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, o, st->watchdog);
+    const int resident = cg == 2 ? st->max_clusters2 : st->max_ctas1;
+    if ((s = make_plan(M, N, K, st->sms, resident, o, &pl)) != GEMM_OK) return s;
+    void* ws = nullptr;
+    if (pl.sk_tiles > 0) {
+        // The workspace is taken from the library's pool on the caller's stream
+        // and handed back on it right after the launch (stream-ordered reuse).
+        if (!st->pool || cudaMallocFromPoolAsync(&ws, size_t(pl.workspace_bytes), st->pool, stream) != cudaSuccess) {
+            cudaGetLastError();
+            ws = nullptr;
+            gemm_f16_nt_options_t dp = o ? *o : gemm_f16_nt_options_t{};
+            dp.schedule = 1;   // no workspace: whole tiles only
+            if ((s = make_plan(M, N, K, st->sms, resident, &dp, &pl)) != GEMM_OK) return s;
+        }
+    }
+    s = cg == 2 ? launch<Cfg2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, o, st->watchdog, ws)
+                : launch<Cfg1>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, o, st->watchdog, ws);
+    if (ws && cudaFreeAsync(ws, stream) != cudaSuccess) {
+        cudaGetLastError();
+        if (s == GEMM_OK) s = GEMM_ERR_LAUNCH;
+    }
+    return s;
 }
 
 }  // namespace g16
@@ -728,6 +999,17 @@ G16_EXPORT gemm_status_t gemm_f16_nt_device_status(void* stream, uint32_t* flags
     }
     if (flags) *flags = v;
     return v ? GEMM_ERR_TIMEOUT : GEMM_OK;
+}
+
+G16_EXPORT gemm_status_t gemm_f16_nt_device_limits(int32_t* sms, int32_t* resident_pairs,
+                                                   int32_t* resident_ctas) {
+    g16::DeviceState* st = nullptr;
+    gemm_status_t s = g16::current_device(&st);
+    if (s != GEMM_OK) return s;
+    if (sms) *sms = st->sms;
+    if (resident_pairs) *resident_pairs = st->max_clusters2;
+    if (resident_ctas) *resident_ctas = st->max_ctas1;
+    return GEMM_OK;
 }
 
 G16_EXPORT const char* gemm_f16_nt_status_string(int32_t status) {

@@ -64,7 +64,10 @@ typedef enum {
  * Ownership: the caller owns A, B and C and keeps them alive until the work on
  * `stream` completes.  The library keeps no pointer after the call returns.
  * The first call on a device performs one-time set-up on that device (device
- * query, kernel attributes, the watchdog word's address); later calls do none.
+ * query, kernel attributes, the watchdog word's address, a private memory
+ * pool); later calls do none.  Shapes whose last wave of output tiles would
+ * run mostly empty use a stream-K schedule (see `schedule` below) whose
+ * workspace is taken from that pool on `stream` and handed back on it.
  *
  * Errors: invalid arguments are reported before anything is enqueued, and C is
  * left unchanged.  The call returns after enqueueing; a fault during execution
@@ -79,8 +82,8 @@ gemm_status_t gemm_f16_nt(int64_t M, int64_t N, int64_t K,
                           void *stream);
 
 /*
- * Tuning and test options for gemm_f16_nt_ex.  Zero in any field selects the
- * default that gemm_f16_nt uses.
+ * Tuning and test options for gemm_f16_nt_ex.  Zero (or NULL) in any field
+ * selects the default that gemm_f16_nt uses.
  *
  *   cta_group     2: a CTA pair computes one 256×256 tile with 2-SM MMAs and
  *                 each CTA loads half of the shared B tile (default);
@@ -98,6 +101,29 @@ gemm_status_t gemm_f16_nt(int64_t M, int64_t N, int64_t K,
  *                 every consumer wait runs into the watchdog; the kernel then
  *                 sets the watchdog word, releases its tensor memory and
  *                 exits without writing C.
+ *   schedule      0 (default): whole tiles round-robin over the persistent
+ *                 clusters, except that when the last wave of tiles would be
+ *                 at most 90 % full the k-block work of that wave plus one
+ *                 full wave is split evenly across all clusters (stream-K),
+ *                 with fp32 partial tiles summed by each tile's first piece in
+ *                 a fixed order (results are reproducible run to run);
+ *                 1: whole tiles only; 2: stream-K whenever possible (tests).
+ *                 A stream-K launch needs a workspace (gemm_f16_nt_plan's
+ *                 workspace_bytes); the call takes it from a memory pool
+ *                 private to this library on `stream` (cudaMallocFromPoolAsync)
+ *                 and returns it on the same stream after the launch.  If the
+ *                 pool cannot supply it the call runs whole tiles only.
+ *   trace, trace_items
+ *                 debugging aid: if `trace` is a device pointer to
+ *                 clusters × trace_items × 8 uint64 (zeroed by the caller), the
+ *                 kernel records for each work item i < trace_items of each
+ *                 cluster c, at trace[(c·trace_items + i)·8 + j]:
+ *                 j=0 tile | kind << 32 (0 whole, 1 partial piece, 2 owner),
+ *                 j=1 kb0 | kb1 << 32, and %globaltimer stamps (ns) j=2 MMA
+ *                 issue start, j=3 MMA issue end, j=4 accumulator ready at the
+ *                 epilogue, j=5 partner partials ready, j=6 epilogue done
+ *                 (stamps from the leader CTA's MMA thread and one of its
+ *                 epilogue warps).
  */
 typedef struct {
     int32_t cta_group;
@@ -105,6 +131,9 @@ typedef struct {
     int32_t max_clusters;
     int32_t inject_stall;
     uint64_t timeout_ns;
+    int32_t schedule;
+    int32_t trace_items;
+    uint64_t *trace;
 } gemm_f16_nt_options_t;
 
 /* gemm_f16_nt with options (opts may be NULL).  Same arguments, layout,
@@ -132,6 +161,15 @@ gemm_status_t gemm_f16_nt_ex(int64_t M, int64_t N, int64_t K,
  */
 gemm_status_t gemm_f16_nt_device_status(void *stream, uint32_t *flags);
 
+/*
+ * What the one-time set-up found on the current device: its SM count and how
+ * many CTA pairs (cta_group 2) and single CTAs (cta_group 1) of the GEMM
+ * kernel can be resident at once (the persistent grid sizes).  Any pointer may
+ * be NULL.  GEMM_ERR_UNSUPPORTED_DEVICE without a usable device.
+ */
+gemm_status_t gemm_f16_nt_device_limits(int32_t *sms, int32_t *resident_pairs,
+                                        int32_t *resident_ctas);
+
 /* A static, human-readable name for a gemm_status_t value. */
 const char *gemm_f16_nt_status_string(int32_t status);
 
@@ -158,6 +196,9 @@ typedef struct {
     int32_t swizzle;       /* raster group width actually used */
     int32_t smem_bytes;    /* dynamic shared memory per CTA */
     int32_t tmem_cols;     /* tensor-memory columns allocated per CTA */
+    int32_t sk_tiles;      /* tiles [0, sk_tiles) are split in k across all clusters (stream-K) */
+    int32_t reserved;
+    int64_t workspace_bytes; /* device workspace a stream-K launch needs (0 if none) */
 } gemm_f16_nt_plan_t;
 
 gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms,

@@ -72,6 +72,38 @@ def test_persistent_loop_many_tiles_per_cta(cg, max_clusters, swizzle):
     check_close(C, oracle.gemm_f16_nt(A, B), K, f"persistent cg{cg} mc{max_clusters} sw{swizzle}")
 
 
+@pytest.mark.parametrize("cg,max_clusters,shape", [
+    (2, 7, (1100, 2100, 520)),     # 45 tiles on 7 pairs: 3 left over + 7 split in k
+    (2, 5, (1100, 2100, 520)),     # 45 % 5 == 0: forced split of one full wave
+    (2, 0, (256, 256, 4096)),      # one tile split over 64 pairs: 63 partials per owner
+    (2, 0, (700, 900, 1500)),      # 12 tiles over many pairs, ragged edges
+    (1, 9, (1000, 1100, 700)),     # single-CTA tiles
+    (1, 0, (130, 300, 2048)),
+])
+def test_stream_k_split_tiles(cg, max_clusters, shape):
+    M, N, K = shape
+    A = inputs.draw((M, K), inputs.U, 91 + M)
+    B = inputs.draw((N, K), inputs.U, 92 + N)
+    o = opts(cg, max_clusters=max_clusters, schedule=2)
+    pl = g.plan(M, N, K, options=o)
+    assert pl["sk_tiles"] > 0
+    C1 = run(A, B, options=o)
+    check_close(C1, oracle.gemm_f16_nt(A, B), K, f"stream-K {shape} cg{cg}")
+    C2 = run(A, B, options=o)                      # partials are summed in a fixed order
+    assert np.array_equal(C1.view(np.uint16), C2.view(np.uint16))
+
+
+def test_stream_k_integers_bit_exact_and_matches_whole_tiles():
+    M, N, K = 1200, 1000, 2200
+    A = inputs.draw((M, K), inputs.I2, 93)
+    B = inputs.draw((N, K), inputs.I2, 94)
+    ref = oracle.gemm_f16_nt(A, B)
+    sk = run(A, B, options=opts(2, max_clusters=6, schedule=2))
+    dp = run(A, B, options=opts(2, max_clusters=6, schedule=1))
+    check_bitexact(sk, ref, "stream-K int")
+    check_bitexact(dp, ref, "whole tiles int")
+
+
 @pytest.mark.parametrize("cg", [2, 1])
 def test_leading_dimensions_and_margins(cg):
     # N % 8 != 0: the last columns are not a whole 16-byte unit of C's rows

@@ -108,6 +108,30 @@ def test_plan_headline_shape():
     assert abs(p["num_tiles"] / p["clusters"] - 13.47) < 0.01
 
 
+def test_plan_stream_k_schedule():
+    # 8192^3: 1024 tiles over 76 pairs leaves a last wave of 36 (47 % full):
+    # that wave plus one full wave (112 tiles) is split in k over all pairs
+    p = g.plan(8192, 8192, 8192, num_sms=152)
+    assert p["sk_tiles"] == 36 + 76
+    assert p["workspace_bytes"] == 76 * 2 * 4 * 8 + 76 * 2 * 128 * 256 * 4
+    # whole tiles only on request, or when the last wave is nearly full
+    assert g.plan(8192, 8192, 8192, options=g.Options(schedule=1))["sk_tiles"] == 0
+    assert g.plan(8192, 8192, 8192, options=g.Options(schedule=1))["workspace_bytes"] == 0
+    p = g.plan(256 * 19, 256 * 8, 4096, num_sms=152)      # 152 tiles = 2 full waves
+    assert p["sk_tiles"] == 0
+    p = g.plan(256 * 15, 256 * 10, 4096, num_sms=152)     # 150 tiles: last wave 74/76 full
+    assert p["sk_tiles"] == 0
+    # fewer tiles than pairs: spread when each share keeps >= 8 k-blocks
+    p = g.plan(1000, 700, 1000)                           # 12 tiles x 16 k-blocks
+    assert (p["sk_tiles"], p["clusters"]) == (12, 24)
+    p = g.plan(256, 256, 256)                             # 1 tile x 4 k-blocks: not worth it
+    assert (p["sk_tiles"], p["clusters"]) == (0, 1)
+    p = g.plan(256, 256, 4096, options=g.Options(schedule=2))   # forced: one k-block per pair
+    assert (p["sk_tiles"], p["clusters"]) == (1, 64)
+    with pytest.raises(g.GemmError):
+        g.plan(256, 256, 256, options=g.Options(schedule=3))
+
+
 def test_plan_edges_and_options():
     p = g.plan(4000, 3000, 5000)
     assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (16, 12, 79)
@@ -165,6 +189,7 @@ def test_argument_validation(args, code):
 def test_bad_options_rejected():
     assert call(8, 8, 16, opts=g.Options(cta_group=4)) == 1
     assert call(8, 8, 16, opts=g.Options(swizzle=-1)) == 1
+    assert call(8, 8, 16, opts=g.Options(schedule=7)) == 1
 
 
 def test_without_a_gpu_valid_calls_report_no_device():
