@@ -28,6 +28,7 @@ STATUS = {
     3: "GEMM_ERR_UNSUPPORTED_DEVICE",
     4: "GEMM_ERR_LAUNCH",
     5: "GEMM_ERR_TIMEOUT",
+    6: "GEMM_ERR_SCRATCH_LIMIT",
 }
 
 
@@ -83,6 +84,8 @@ def library(path: str | None = None):
         lib.gemm_f16_nt.restype = ctypes.c_int
         lib.gemm_f16_nt_ex.argtypes = sig + [ctypes.POINTER(Options)]
         lib.gemm_f16_nt_ex.restype = ctypes.c_int
+        lib.gemm_f16_nt_noalloc.argtypes = sig
+        lib.gemm_f16_nt_noalloc.restype = ctypes.c_int
         lib.gemm_f16_nt_device_status.argtypes = [_p, ctypes.POINTER(_u32)]
         lib.gemm_f16_nt_device_status.restype = ctypes.c_int
         lib.gemm_f16_nt_status_string.argtypes = [_i32]

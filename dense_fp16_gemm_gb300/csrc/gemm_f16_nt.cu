@@ -647,6 +647,7 @@ struct DeviceState {
     int max_clusters2 = 0;   // resident CTA pairs for Cfg2
     int max_ctas1 = 0;       // resident CTAs for Cfg1
     uint32_t* watchdog = nullptr;
+    bool pool_ready = false;
     cudaMemPool_t pool = nullptr;   // private stream-ordered pool for stream-K workspaces
 };
 
@@ -725,8 +726,12 @@ gemm_status_t setup_device(int dev, DeviceState& st) {
     }
     st.watchdog = static_cast<uint32_t*>(wd);
     st.sms = sms;
-    // Workspaces come from a pool of this library's own, on the caller's stream,
-    // and stay cached in it between calls.
+    return GEMM_OK;
+}
+
+// Workspaces come from a pool of this library's own, on the caller's stream,
+// and stay cached in it between calls.
+void setup_pool(int dev, DeviceState& st) {
     cudaMemPoolProps props = {};
     props.allocType = cudaMemAllocationTypePinned;
     props.location.type = cudaMemLocationTypeDevice;
@@ -738,10 +743,11 @@ gemm_status_t setup_device(int dev, DeviceState& st) {
         uint64_t keep = UINT64_MAX;
         cudaMemPoolSetAttribute(st.pool, cudaMemPoolAttrReleaseThreshold, &keep);
     }
-    return GEMM_OK;
 }
 
-gemm_status_t current_device(DeviceState** out) {
+// The current device's state after its one-time set-up; `with_pool` also
+// creates the workspace pool (the static-scratch entry point never needs it).
+gemm_status_t device_state(DeviceState** out, int* dev_out, bool with_pool) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         cudaGetLastError();
@@ -754,9 +760,16 @@ gemm_status_t current_device(DeviceState** out) {
         st.ready = true;
     }
     if (st.status != GEMM_OK) return st.status;
+    if (with_pool && !st.pool_ready) {
+        setup_pool(dev, st);
+        st.pool_ready = true;
+    }
     *out = &st;
+    if (dev_out) *dev_out = dev;
     return GEMM_OK;
 }
+
+gemm_status_t current_device(DeviceState** out) { return device_state(out, nullptr, true); }
 
 gemm_status_t check_args(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
                          const uint16_t* B, int64_t ldb, const uint16_t* C, int64_t ldc) {
@@ -965,6 +978,73 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t ld
     return s;
 }
 
+// ---------------------------------------------------------------------------
+// the entry point that allocates nothing: stream-K scratch in a static array
+// ---------------------------------------------------------------------------
+
+// 20 MiB holds the stream-K workspace of the largest persistent grid on a
+// 152-SM GB300 (76 pairs × 2 CTAs × 128 KiB of fp32 partials + flags).  Like
+// every __device__ variable it is placed on each GPU that loads this library
+// and kept there until the process exits.
+constexpr size_t kStaticScratchBytes = size_t(20) << 20;
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+struct StaticScratch {
+    bool ready = false;
+    bool ok = false;
+    void* ptr = nullptr;   // device address of g_static_scratch on this device
+};
+StaticScratch g_static_scratch_addr[kMaxDevices];
+
+// In host code `g_static_scratch` names a host-side stand-in, not device
+// memory: the kernel must be given the address the runtime reports, looked up
+// once per device with that device current.
+gemm_status_t static_scratch(int dev, void** out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    StaticScratch& sc = g_static_scratch_addr[dev];
+    if (!sc.ready) {
+        void* ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+        if (e != cudaSuccess) cudaGetLastError();
+        sc.ok = e == cudaSuccess && ptr != nullptr;
+        sc.ptr = ptr;
+        sc.ready = true;
+    }
+    if (!sc.ok) return GEMM_ERR_LAUNCH;
+    *out = sc.ptr;
+    return GEMM_OK;
+}
+
+gemm_status_t run_noalloc(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
+                          const uint16_t* B, int64_t ldb, uint16_t* C, int64_t ldc, void* stream_v) {
+    gemm_status_t s = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+    if (s != GEMM_OK) return s;
+    if (M == 0 || N == 0) return GEMM_OK;
+    DeviceState* st = nullptr;
+    int dev = -1;
+    if ((s = device_state(&st, &dev, false)) != GEMM_OK) return s;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    if (K == 0) {
+        const int64_t total = M * N;
+        int64_t blocks = cdiv(total, 256);
+        if (blocks > int64_t(st->sms) * 8) blocks = int64_t(st->sms) * 8;
+        zero_fill_kernel<<<dim3(uint32_t(blocks)), dim3(256), 0, stream>>>(C, M, N, ldc);
+        if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+        return GEMM_OK;
+    }
+    gemm_f16_nt_plan_t pl;
+    if ((s = make_plan(M, N, K, st->sms, st->max_clusters2, nullptr, &pl)) != GEMM_OK) return s;
+    void* ws = nullptr;
+    if (pl.sk_tiles > 0) {
+        if (uint64_t(pl.workspace_bytes) > kStaticScratchBytes) return GEMM_ERR_SCRATCH_LIMIT;
+        if ((s = static_scratch(dev, &ws)) != GEMM_OK) return s;
+    }
+    // Nothing in the scratch has to start at zero: each launch's completion
+    // flags carry that launch's own 64-bit id, so values left by an earlier
+    // call never match, and every partial tile is written before it is read.
+    return launch<Cfg2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr, st->watchdog, ws);
+}
+
 }  // namespace g16
 
 // ---------------------------------------------------------------------------
@@ -975,6 +1055,12 @@ G16_EXPORT gemm_status_t gemm_f16_nt(int64_t M, int64_t N, int64_t K, const uint
                                      const uint16_t* B, int64_t ldb, uint16_t* C, int64_t ldc,
                                      void* stream) {
     return g16::run(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr);
+}
+
+G16_EXPORT gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K, const uint16_t* A,
+                                             int64_t lda, const uint16_t* B, int64_t ldb, uint16_t* C,
+                                             int64_t ldc, void* stream) {
+    return g16::run_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream);
 }
 
 G16_EXPORT gemm_status_t gemm_f16_nt_ex(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
@@ -1020,6 +1106,9 @@ G16_EXPORT const char* gemm_f16_nt_status_string(int32_t status) {
         case GEMM_ERR_UNSUPPORTED_DEVICE: return "GEMM_ERR_UNSUPPORTED_DEVICE: needs a compute capability 10.3 GPU";
         case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH: a CUDA runtime or driver call failed";
         case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: a pipeline wait ran into the device watchdog";
+        case GEMM_ERR_SCRATCH_LIMIT:
+            return "GEMM_ERR_SCRATCH_LIMIT: the problem's stream-K scratch exceeds the 20 MiB static array "
+                   "of gemm_f16_nt_noalloc; use gemm_f16_nt";
         default: return "unknown gemm_status_t";
     }
 }

@@ -36,7 +36,8 @@ typedef enum {
     GEMM_ERR_MISALIGNED = 2,         /* a pointer or row pitch breaks the 16-byte rule below */
     GEMM_ERR_UNSUPPORTED_DEVICE = 3, /* no CUDA device, or the current device is not compute capability 10.3 */
     GEMM_ERR_LAUNCH = 4,             /* the CUDA runtime or driver refused a call (set-up or launch) */
-    GEMM_ERR_TIMEOUT = 5             /* the device watchdog word is set (see gemm_f16_nt_device_status) */
+    GEMM_ERR_TIMEOUT = 5,            /* the device watchdog word is set (see gemm_f16_nt_device_status) */
+    GEMM_ERR_SCRATCH_LIMIT = 6       /* gemm_f16_nt_noalloc: the scratch needed exceeds its static array */
 } gemm_status_t;
 
 /*
@@ -80,6 +81,44 @@ gemm_status_t gemm_f16_nt(int64_t M, int64_t N, int64_t K,
                           const uint16_t *B, int64_t ldb,
                           uint16_t *C, int64_t ldc,
                           void *stream);
+
+/*
+ * gemm_f16_nt_noalloc — gemm_f16_nt for callers that cannot allocate device
+ * memory during the call.
+ *
+ * No counterpart in the tutorial pages: this is an interface choice of the
+ * library, not part of the method.
+ *
+ * Who needs it: gemm_f16_nt takes the stream-K workspace (up to about 20 MB)
+ * from a memory pool of its own.  Some callers cannot let a library allocate:
+ * processes whose device memory is reserved up front by their own allocator,
+ * so that an extra allocation can fail or fragment it, and latency-critical
+ * loops that cannot afford an allocation's cost or implicit synchronisation.
+ * This entry point computes the same product with the same kernel and the same
+ * schedule, and takes no memory at all during the call: its scratch is a
+ * fixed array of 20 MiB (20,971,520 bytes) compiled into the library, which
+ * every GPU that loads the library holds until the process exits.
+ *
+ * Arguments, layout, alignment, ownership and errors are those of gemm_f16_nt.
+ * Extra rules:
+ *   - It calls no cudaMalloc, cudaFree, pool or other allocating routine.
+ *   - Its first call on a device also looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); later calls reuse it.
+ *   - Every call on a device shares the one array, which keeps what the last
+ *     call left in it.  Calls that can overlap on the GPU (for example on two
+ *     streams with no ordering between them) race on it and may return wrong
+ *     results: order them, e.g. keep them on one stream.  Nothing in the array
+ *     has to start at zero (each launch tags its completion flags with its own
+ *     id, and writes every partial tile before reading it).
+ *   - A problem whose stream-K scratch would exceed the array (possible only
+ *     on GPUs with more than 152 SMs) is rejected with GEMM_ERR_SCRATCH_LIMIT
+ *     before anything is enqueued.
+ */
+gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
+                                  const uint16_t *A, int64_t lda,
+                                  const uint16_t *B, int64_t ldb,
+                                  uint16_t *C, int64_t ldc,
+                                  void *stream);
 
 /*
  * Tuning and test options for gemm_f16_nt_ex.  Zero (or NULL) in any field
