@@ -154,16 +154,19 @@ __device__ __noinline__ void raise_abort(const Watch w, uint32_t site) {
     atomicOr(w.word, 1u | (1u << (7u + site)));
 }
 
+// Between checks of the watchdog, a waiting thread sleeps in the barrier
+// (woken when the phase completes) rather than polling shared memory, which
+// would take issue slots and shared-memory bandwidth from the tensor cores.
+constexpr uint32_t kWaitSleepNs = 20000;
+
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Watch w, uint32_t site) {
     const uint64_t t0 = ptx::globaltimer();
-    for (uint32_t i = 1;; ++i) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-        if ((i & 7u) == 0) {
-            if (*w.abort_flag) return false;
-            if (ptx::globaltimer() - t0 > w.limit_ns) {
-                raise_abort(w, site);
-                return false;
-            }
+    for (;;) {
+        if (ptx::mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+        if (*w.abort_flag) return false;
+        if (ptx::globaltimer() - t0 > w.limit_ns) {
+            raise_abort(w, site);
+            return false;
         }
     }
 }
@@ -178,9 +181,9 @@ __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, const Watch&
 // Teardown wait after an abort: ignores the abort flag, bounded by the limit.
 __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = ptx::globaltimer();
-    for (uint32_t i = 1;; ++i) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-        if ((i & 7u) == 0 && ptx::globaltimer() - t0 > limit_ns) return false;
+    for (;;) {
+        if (ptx::mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+        if (ptx::globaltimer() - t0 > limit_ns) return false;
     }
 }
 
@@ -425,11 +428,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                 }
                 ++item_no;
                 const uint32_t d = tmem_base + acc * uint32_t(BN);
+                uint64_t starved_ns = 0;   // traced: time spent waiting for filled stages
                 for (uint32_t kb = it.kb0; kb < it.kb1; ++kb) {
-                    if (!wait(full0 + 8 * stage, phase, w, kSiteMmaFull)) {
-                        ok = false;
-                        break;
+                    if (tr && !ptx::mbar_try_wait(full0 + 8 * stage, phase)) {
+                        const uint64_t ts = ptx::globaltimer();
+                        ok = wait(full0 + 8 * stage, phase, w, kSiteMmaFull);
+                        starved_ns += ptx::globaltimer() - ts;
+                    } else if (!tr) {
+                        ok = wait(full0 + 8 * stage, phase, w, kSiteMmaFull);
                     }
+                    if (!ok) break;
                     ptx::tc_fence_after();
                     const uint64_t ad = sdesc_sw128(sA + stage * Cfg::kABytes);
                     const uint64_t bd = sdesc_sw128(sB + stage * Cfg::kBBytes);
@@ -450,7 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                 if (!ok) break;
                 if constexpr (CG == 2) ptx::mma_commit_pair(accf0 + 8 * acc, 0x3);
                 else ptx::mma_commit(accf0 + 8 * acc);
-                if (tr) tr[3] = ptx::globaltimer();
+                if (tr) {
+                    tr[3] = ptx::globaltimer();
+                    tr[7] = starved_ns;
+                }
                 acc ^= 1u;
                 if (acc == 0) acc_phase ^= 1u;
             }

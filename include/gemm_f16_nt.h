@@ -162,7 +162,8 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  *                 issue start, j=3 MMA issue end, j=4 accumulator ready at the
  *                 epilogue, j=5 partner partials ready, j=6 epilogue done
  *                 (stamps from the leader CTA's MMA thread and one of its
- *                 epilogue warps).
+ *                 epilogue warps), j=7 total ns the MMA thread waited for
+ *                 filled pipeline stages during the item.
  */
 typedef struct {
     int32_t cta_group;
