@@ -441,6 +441,14 @@ def run_ours(args, w):
 
     if rank == 0:
         traffic = recorded_traffic(w.name)
+        lim = g.device_limits()
+        pl = g.plan(w.M, w.N, w.K, num_sms=lim["sms"])
+        pl = g.plan(w.M, w.N, w.K, num_sms=lim["sms"],
+                    max_clusters=lim["resident_pair_pairs"] if pl["cluster_pairs"] == 2 else lim["resident_pairs"])
+        kernel_desc = (f"gemm_f16_nt_kernel<KCfg<{pl['cta_group']},256,{pl['stages']},{pl['cluster_pairs']}>>: "
+                       f"{pl['clusters']} clusters x {pl['grid_ctas'] // pl['clusters']} CTAs, "
+                       f"{pl['tile_m']}x{pl['tile_n']} cluster tiles, {pl['sk_tiles']} of {pl['num_tiles']} "
+                       f"split in k")
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
@@ -452,7 +460,7 @@ def run_ours(args, w):
                          "unit": UNIT, "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_source": f"{peak_src} bf16 dense burst (fp16 runs at the bf16 rate)",
                          "frac_of_sustained": round(achieved / peak_sustained, 4) if peak_sustained else None,
-                         "kernel": "gemm_f16_nt_kernel<KCfg<2,256,6>>"},
+                         "kernel": kernel_desc},
             "e2e": {"value": round(e2e_work / e2e_t / 1e12, 2), "unit": UNIT,
                     "h2d_bytes_per_step": int(A.nbytes + B.nbytes), "d2h_bytes_per_step": int(Ch.numel() * 2)},
             "gpu_launches": args.steps * args.repeat,

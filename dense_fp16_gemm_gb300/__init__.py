@@ -45,7 +45,8 @@ class Options(ctypes.Structure):
     _fields_ = [("cta_group", ctypes.c_int32), ("swizzle", ctypes.c_int32),
                 ("max_clusters", ctypes.c_int32), ("inject_stall", ctypes.c_int32),
                 ("timeout_ns", ctypes.c_uint64), ("schedule", ctypes.c_int32),
-                ("trace_items", ctypes.c_int32), ("trace", ctypes.c_void_p)]
+                ("trace_items", ctypes.c_int32), ("trace", ctypes.c_void_p),
+                ("cluster_pairs", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class Plan(ctypes.Structure):
@@ -57,11 +58,11 @@ class Plan(ctypes.Structure):
                 ("num_tiles", ctypes.c_int64), ("clusters", ctypes.c_int32),
                 ("grid_ctas", ctypes.c_int32), ("swizzle", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("tmem_cols", ctypes.c_int32),
-                ("sk_tiles", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("sk_tiles", ctypes.c_int32), ("cluster_pairs", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64)]
 
     def as_dict(self):
-        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
+        return {f: getattr(self, f) for f, _ in self._fields_}
 
 
 _lib = None
@@ -99,7 +100,7 @@ def library(path: str | None = None):
         lib.gemm_f16_nt_fast_divmod.argtypes = [_u32, _u32, ctypes.POINTER(_u32),
                                                 ctypes.POINTER(_u32)]
         lib.gemm_f16_nt_fast_divmod.restype = ctypes.c_int
-        lib.gemm_f16_nt_device_limits.argtypes = [ctypes.POINTER(_i32)] * 3
+        lib.gemm_f16_nt_device_limits.argtypes = [ctypes.POINTER(_i32)] * 4
         lib.gemm_f16_nt_device_limits.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -182,10 +183,11 @@ def device_status(stream=None) -> int:
 
 def device_limits() -> dict:
     """SM count and resident CTA pairs / CTAs of the current device."""
-    a, b, c = _i32(0), _i32(0), _i32(0)
-    _check(library().gemm_f16_nt_device_limits(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
-           "gemm_f16_nt_device_limits")
-    return {"sms": a.value, "resident_pairs": b.value, "resident_ctas": c.value}
+    a, b, c, d = _i32(0), _i32(0), _i32(0), _i32(0)
+    _check(library().gemm_f16_nt_device_limits(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c),
+                                               ctypes.byref(d)), "gemm_f16_nt_device_limits")
+    return {"sms": a.value, "resident_pairs": b.value, "resident_ctas": c.value,
+            "resident_pair_pairs": d.value}
 
 
 def plan(M: int, N: int, K: int, num_sms: int = 152, max_clusters: int = 0,

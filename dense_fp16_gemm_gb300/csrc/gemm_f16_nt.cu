@@ -73,9 +73,11 @@ enum : uint32_t { kItemWhole = 0, kItemPartialOut = 1, kItemOwner = 2 };
 
 __device__ uint32_t g_watchdog_word;
 
-template <int CG, int BN, int STAGES>
+template <int CG, int BN, int STAGES, int CP = 1>
 struct KCfg {
     static constexpr int kCG = CG;
+    static constexpr int kCP = CP;                   // CTA pairs per cluster (A shared by multicast)
+    static constexpr int kCtas = CG * CP;            // CTAs per cluster
     static constexpr int kBN = BN;                   // columns of C per tile
     static constexpr int kStages = STAGES;
     static constexpr int kTileM = kBlockM * CG;      // rows of C per tile
@@ -99,6 +101,7 @@ struct KCfg {
     static_assert(BN % kEpiCols == 0, "epilogue works in 64-column chunks");
     static_assert(kBRows <= 256, "a TMA box is at most 256 rows");
     static_assert(kSmemBytes <= 232448, "dynamic shared memory limit per CTA");
+    static_assert(CP == 1 || (CG == 2 && CP == 2), "two pairs per cluster only with CTA pairs");
 };
 
 template <int STAGES>
@@ -144,13 +147,17 @@ struct Params {
 struct Watch {
     uint64_t limit_ns;
     volatile uint32_t* abort_flag;   // this CTA's flag
-    uint32_t peer_abort;             // shared::cluster address of the peer's flag, 0 if none
+    uint32_t abort_addr;             // its shared-memory address (same offset in every CTA)
+    uint32_t ctas;                   // CTAs in the cluster
+    uint32_t rank;                   // this CTA's rank in the cluster
     uint32_t* word;
 };
 
+// Stop this CTA and every other CTA of the cluster (they wait on each other).
 __device__ __noinline__ void raise_abort(const Watch w, uint32_t site) {
     *w.abort_flag = 1u;
-    if (w.peer_abort) ptx::st_cluster_u32(w.peer_abort, 1u);
+    for (uint32_t r = 0; r < w.ctas; ++r)
+        if (r != w.rank) ptx::st_cluster_u32(ptx::mapa(w.abort_addr, r), 1u);
     atomicOr(w.word, 1u | (1u << (7u + site)));
 }
 
@@ -293,6 +300,8 @@ __device__ __noinline__ bool wait_flag(const uint64_t* flag, uint64_t want, cons
 template <class Cfg>
 __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_constant__ Params p) {
     constexpr int CG = Cfg::kCG;
+    constexpr int CP = Cfg::kCP;
+    constexpr int NCTA = Cfg::kCtas;
     constexpr int BN = Cfg::kBN;
     constexpr int S = Cfg::kStages;
 
@@ -306,9 +315,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
 
     const uint32_t warp = __shfl_sync(0xffffffffu, threadIdx.x >> 5, 0);
     const uint32_t lane = threadIdx.x & 31u;
-    const uint32_t rank = CG == 2 ? ptx::cluster_ctarank() : 0u;
-    const uint32_t cluster = CG == 2 ? ptx::cluster_id_x() : blockIdx.x;
-    const uint32_t nclusters = CG == 2 ? ptx::nclusters_x() : gridDim.x;
+    const uint32_t rank = NCTA > 1 ? ptx::cluster_ctarank() : 0u;   // rank in the cluster
+    const uint32_t pair = CG == 2 ? rank >> 1 : 0u;                  // CTA pair in the cluster
+    const uint32_t prank = CG == 2 ? rank & 1u : 0u;                 // rank in the pair
+    const uint32_t lead = pair * 2u;                                 // the pair's leader CTA
+    const uint32_t cluster = NCTA > 1 ? ptx::cluster_id_x() : blockIdx.x;
+    const uint32_t nclusters = NCTA > 1 ? ptx::nclusters_x() : gridDim.x;
 
     const uint32_t full0 = ptx::smem_u32(&ctl->full[0]);
     const uint32_t empty0 = ptx::smem_u32(&ctl->empty[0]);
@@ -319,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(full0 + 8 * s, 1);     // the leader's expect-tx arrive
-            ptx::mbar_init(empty0 + 8 * s, 1);    // one tcgen05.commit
+            ptx::mbar_init(empty0 + 8 * s, CP);   // one tcgen05.commit from each pair's leader
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(accf0 + 8 * b, 1);                  // one tcgen05.commit
@@ -339,45 +351,57 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
         ptx::tmem_relinquish<CG>();
     }
     ptx::tc_fence_before();
-    if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
+    if constexpr (NCTA > 1) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(&ctl->tmem_base);
 
     Watch w;
     w.limit_ns = p.timeout_ns;
     w.abort_flag = &ctl->abort_flag;
-    w.peer_abort = CG == 2 ? ptx::mapa(ptx::smem_u32(&ctl->abort_flag), rank ^ 1u) : 0u;
+    w.abort_addr = ptx::smem_u32(&ctl->abort_flag);
+    w.ctas = NCTA;
+    w.rank = rank;
     w.word = p.watchdog;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && !p.inject_stall) {
-            // Completion bytes of both CTAs' loads go to the leader's full barrier.
-            const uint32_t full_tgt = CG == 2 ? ptx::mapa(full0, 0) : full0;
+            // Completion bytes of both CTAs' loads go to the pair leader's full barrier.
+            const uint32_t full_tgt = CG == 2 ? ptx::mapa(full0, lead) : full0;
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
+            // Tiles of one raster group share B column strips across successive
+            // waves: keep B in L2 in preference to the streamed A rows.
+            const uint64_t keep_b = ptx::policy_evict_last();
             Work work;
             Item it;
             work_init(work, p, cluster, nclusters);
             while (ok && work_next(work, p, it)) {
                 uint32_t mt, nt;
                 raster_coord(p.raster, it.tile, mt, nt);
-                const int32_t m0 = int32_t(mt * Cfg::kTileM + rank * kBlockM);
-                const int32_t n0 = int32_t(nt * BN + rank * Cfg::kBRows);
+                const int32_t m0 = int32_t(mt * Cfg::kTileM + prank * kBlockM);
+                const int32_t n0 = int32_t((nt * CP + pair) * BN + prank * Cfg::kBRows);
                 for (uint32_t kb = it.kb0; kb < it.kb1; ++kb) {
                     if (!wait(empty0 + 8 * stage, phase ^ 1u, w, kSiteProducerEmpty)) {
                         ok = false;
                         break;
                     }
-                    if (rank == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * stage, Cfg::kTxBytes);
+                    if (prank == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * stage, Cfg::kTxBytes);
                     const int32_t k0 = int32_t(kb * kBlockK);
                     const uint32_t bar = full_tgt + 8 * stage;
-                    if constexpr (CG == 2) {
+                    if constexpr (CP == 2) {
+                        // Both pairs need the same A rows: this CTA loads half of them
+                        // into the same-rank CTA of both pairs (TMA multicast).
+                        ptx::tma_load_2d_pair_mcast(sA + stage * Cfg::kABytes + pair * (Cfg::kABytes / 2),
+                                                    &p.tmA, k0, m0 + int32_t(pair * (kBlockM / 2)), bar,
+                                                    uint16_t((1u << prank) | (1u << (prank + 2u))));
+                        ptx::tma_load_2d_pair_hint(sB + stage * Cfg::kBBytes, &p.tmB, k0, n0, bar, keep_b);
+                    } else if constexpr (CG == 2) {
                         ptx::tma_load_2d_pair(sA + stage * Cfg::kABytes, &p.tmA, k0, m0, bar);
-                        ptx::tma_load_2d_pair(sB + stage * Cfg::kBBytes, &p.tmB, k0, n0, bar);
+                        ptx::tma_load_2d_pair_hint(sB + stage * Cfg::kBBytes, &p.tmB, k0, n0, bar, keep_b);
                     } else {
                         ptx::tma_load_2d(sA + stage * Cfg::kABytes, &p.tmA, k0, m0, bar);
-                        ptx::tma_load_2d(sB + stage * Cfg::kBBytes, &p.tmB, k0, n0, bar);
+                        ptx::tma_load_2d_hint(sB + stage * Cfg::kBBytes, &p.tmB, k0, n0, bar, keep_b);
                     }
                     ++issued;
                     if (++stage == uint32_t(S)) {
@@ -388,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
             }
             if (!ok && issued) {
                 // Let the copies already issued land before the CTA can exit.
-                if (rank == 0) {
+                if (prank == 0) {
                     uint32_t s = stage, ph = phase;
                     const uint32_t n = issued < uint32_t(S) ? issued : uint32_t(S);
                     for (uint32_t i = 0; i < n; ++i) {
@@ -409,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && rank == 0) {
+        if (lane == 0 && prank == 0) {
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             Work work;
@@ -448,7 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                                          (kb != it.kb0 || k != 0) ? 1u : 0u);
                     }
                     // Free this ring slot in every CTA of the pair once these MMAs retire.
-                    if constexpr (CG == 2) ptx::mma_commit_pair(empty0 + 8 * stage, 0x3);
+                    // (with two pairs, the stage is free only once both pairs' MMAs are done)
+                    if constexpr (CG == 2) ptx::mma_commit_pair(empty0 + 8 * stage, CP == 2 ? 0xF : 0x3);
                     else ptx::mma_commit(empty0 + 8 * stage);
                     if (++stage == uint32_t(S)) {
                         stage = 0;
@@ -456,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                     }
                 }
                 if (!ok) break;
-                if constexpr (CG == 2) ptx::mma_commit_pair(accf0 + 8 * acc, 0x3);
+                if constexpr (CG == 2) ptx::mma_commit_pair(accf0 + 8 * acc, uint16_t(0x3u << lead));
                 else ptx::mma_commit(accf0 + 8 * acc);
                 if (tr) {
                     tr[3] = ptx::globaltimer();
@@ -466,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                 if (acc == 0) acc_phase ^= 1u;
             }
             // Every MMA must have retired before the tensor memory is released.
-            if constexpr (CG == 2) ptx::mma_commit_pair(mma_done, 0x1);
+            if constexpr (CG == 2) ptx::mma_commit_pair(mma_done, uint16_t(1u << lead));
             else ptx::mma_commit(mma_done);
             if (!wait_drain(mma_done, 0, p.timeout_ns)) atomicOr(p.watchdog, 1u | (1u << (7u + kSiteMmaDrain)));
         }
@@ -476,13 +501,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
         const uint32_t q = warp & 3u;                      // TMEM lane quarter this warp may read
         const uint32_t lane_off = (q * 32u) << 16;
         const uint32_t out0 = sOut + (warp - 2u) * kOutBufs * kOutBufBytes;
-        const uint32_t acce_tgt = CG == 2 ? ptx::mapa(acce0, 0) : acce0;
+        const uint32_t acce_tgt = CG == 2 ? ptx::mapa(acce0, lead) : acce0;
         // A partial tile in workspace slot `slot` is stored as float4 groups of
         // columns, row innermost: [col/4][128 rows], so that the 32 lanes of a
         // warp (32 consecutive rows) touch 512 contiguous bytes per access.
         auto partial_f4 = [&](uint32_t slot, uint32_t col4) {
             return reinterpret_cast<float4*>(p.partials) +
-                   ((size_t(slot) * CG + rank) * (BN / 4) + col4) * kBlockM + q * 32u + lane;
+                   ((size_t(slot) * NCTA + rank) * (BN / 4) + col4) * kBlockM + q * 32u + lane;
         };
         uint32_t acc = 0, acc_phase = 0, ob = 0;
         Work work;
@@ -492,8 +517,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
         while (work_next(work, p, it)) {
             uint32_t mt, nt;
             raster_coord(p.raster, it.tile, mt, nt);
-            const int32_t row0 = int32_t(mt * Cfg::kTileM + rank * kBlockM + q * 32u);
-            const int32_t col0 = int32_t(nt * BN);
+            const int32_t row0 = int32_t(mt * Cfg::kTileM + prank * kBlockM + q * 32u);
+            const int32_t col0 = int32_t((nt * CP + pair) * BN);
             uint64_t* tr = (p.trace && item_no < p.trace_items && rank == 0 && warp == 2 && lane == 0)
                                ? p.trace + (size_t(cluster) * p.trace_items + item_no) * 8 : nullptr;
             ++item_no;
@@ -512,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                 uint32_t okf = 1;
                 if (lane == 0)
                     for (uint32_t i = 0; i < npart && okf; ++i)
-                        okf = wait_flag(p.flags + (size_t(cluster + 1 + i) * CG + rank) * kEpiWarps + q,
+                        okf = wait_flag(p.flags + (size_t(cluster + 1 + i) * NCTA + rank) * kEpiWarps + q,
                                         p.launch_id, w, kSiteStreamK) ? 1u : 0u;
                 okf = __shfl_sync(0xffffffffu, okf, 0);
                 if (!okf) break;
@@ -613,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                 __threadfence();
                 __syncwarp();
                 if (lane == 0)
-                    ptx::st_release_u64(p.flags + (size_t(cluster) * CG + rank) * kEpiWarps + q, p.launch_id);
+                    ptx::st_release_u64(p.flags + (size_t(cluster) * NCTA + rank) * kEpiWarps + q, p.launch_id);
             }
             if (tr) tr[6] = ptx::globaltimer();
             acc ^= 1u;
@@ -624,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
     }
 
     ptx::tc_fence_before();
-    if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
+    if constexpr (NCTA > 1) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after();
     if (warp == 1) ptx::tmem_dealloc<CG>(tmem_base, Cfg::kTmemCols);
 }
@@ -643,8 +668,9 @@ __global__ void zero_fill_kernel(uint16_t* C, int64_t M, int64_t N, int64_t ldc)
 // host side
 // ---------------------------------------------------------------------------
 
-using Cfg2 = KCfg<2, 256, 6>;   // CTA pair, 256×256 tile, 6-stage ring
-using Cfg1 = KCfg<1, 256, 4>;   // single CTA, 128×256 tile, 4-stage ring
+using Cfg2 = KCfg<2, 256, 6>;      // CTA pair, 256×256 tile, 6-stage ring
+using Cfg2x2 = KCfg<2, 256, 6, 2>; // two CTA pairs per cluster sharing A: 256×512 cluster tile
+using Cfg1 = KCfg<1, 256, 4>;      // single CTA, 128×256 tile, 4-stage ring
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -656,6 +682,7 @@ struct DeviceState {
     gemm_status_t status = GEMM_OK;
     int sms = 0;
     int max_clusters2 = 0;   // resident CTA pairs for Cfg2
+    int max_clusters4 = 0;   // resident clusters of two pairs for Cfg2x2
     int max_ctas1 = 0;       // resident CTAs for Cfg1
     uint32_t* watchdog = nullptr;
     bool pool_ready = false;
@@ -694,32 +721,37 @@ gemm_status_t setup_device(int dev, DeviceState& st) {
     }
     if (cudaFuncSetAttribute(gemm_f16_nt_kernel<Cfg2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg2::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_f16_nt_kernel<Cfg2x2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg2x2::kSmemBytes) != cudaSuccess ||
         cudaFuncSetAttribute(gemm_f16_nt_kernel<Cfg1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg1::kSmemBytes) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
-    // How many CTA pairs can be resident at once (cluster placement may leave
-    // some SMs unpaired).
-    {
+    // How many clusters can be resident at once (cluster placement within the
+    // GPCs may leave some SMs out: on a 152-SM GB300, 76 pairs but only 36
+    // clusters of four).
+    auto resident_clusters = [&](auto kernel, int ctas, int smem) {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.x = ctas;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+        cfg.gridDim = dim3(ctas * (sms / ctas), 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = Cfg2::kSmemBytes;
+        cfg.dynamicSmemBytes = smem;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, gemm_f16_nt_kernel<Cfg2>, &cfg) != cudaSuccess || n < 1) {
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n < 1) {
             cudaGetLastError();
-            n = sms / 2;
+            n = sms / ctas;
         }
-        st.max_clusters2 = n < sms / 2 ? n : sms / 2;
-    }
+        return n < sms / ctas ? n : sms / ctas;
+    };
+    st.max_clusters2 = resident_clusters(gemm_f16_nt_kernel<Cfg2>, 2, Cfg2::kSmemBytes);
+    st.max_clusters4 = resident_clusters(gemm_f16_nt_kernel<Cfg2x2>, 4, Cfg2x2::kSmemBytes);
     {
         int per_sm = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_f16_nt_kernel<Cfg1>, kThreads,
@@ -800,12 +832,36 @@ gemm_status_t check_args(int64_t M, int64_t N, int64_t K, const uint16_t* A, int
 }
 
 // Stream-K workspace: flags first ([cluster][rank][warp] uint64, 256-byte
-// aligned), then the fp32 partial tiles ([cluster][rank][tile_n/4][128] float4).
-int64_t flags_bytes(int cg, int64_t clusters) {
-    return (clusters * cg * kEpiWarps * 8 + 255) / 256 * 256;
+// aligned), then the fp32 partial tiles ([cluster][rank][256/4][128] float4),
+// one 128×256 partial per CTA of the cluster.
+constexpr int kCtaTileN = 256;
+int64_t flags_bytes(int ctas, int64_t clusters) {
+    return (clusters * ctas * kEpiWarps * 8 + 255) / 256 * 256;
 }
-int64_t workspace_bytes(int cg, int tile_n, int64_t clusters) {
-    return flags_bytes(cg, clusters) + clusters * cg * int64_t(kBlockM) * tile_n * 4;
+int64_t workspace_bytes(int ctas, int64_t clusters) {
+    return flags_bytes(ctas, clusters) + clusters * ctas * int64_t(kBlockM) * kCtaTileN * 4;
+}
+
+// Default CTA pairs per cluster.  Two pairs that share A through multicast pay
+// off when a row pitch of A or B is not a multiple of 128 bytes: every 128-byte
+// row slice of a tile then spans two L2 lines, L2 traffic becomes the limit,
+// and halving A's share outweighs the SMs that clusters of four leave idle.
+// They need N wide enough for both pairs' tiles.
+int auto_cluster_pairs(int cg, int64_t N, int64_t lda, int64_t ldb) {
+    if (cg != 2 || N <= kCtaTileN) return 1;
+    return (lda % 64 != 0 || ldb % 64 != 0) ? 2 : 1;
+}
+
+// The options with every "auto" (zero) CTA-group and cluster choice resolved.
+gemm_f16_nt_options_t resolve_options(const gemm_f16_nt_options_t* o, int64_t N, int64_t lda, int64_t ldb) {
+    gemm_f16_nt_options_t r = o ? *o : gemm_f16_nt_options_t{};
+    if (r.cta_group == 0) r.cta_group = 2;
+    if (r.cluster_pairs == 0) r.cluster_pairs = auto_cluster_pairs(r.cta_group, N, lda, ldb);
+    return r;
+}
+
+int resident_clusters_for(const DeviceState& st, const gemm_f16_nt_options_t& r) {
+    return r.cta_group == 1 ? st.max_ctas1 : (r.cluster_pairs == 2 ? st.max_clusters4 : st.max_clusters2);
 }
 
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t max_resident,
@@ -816,13 +872,15 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
     const int cg = (o && o->cta_group) ? o->cta_group : 2;
     const int sw = (o && o->swizzle) ? o->swizzle : kDefaultSwizzle;
     const int sched = o ? o->schedule : 0;
+    const int cp = (o && o->cluster_pairs) ? o->cluster_pairs : 1;
     if ((cg != 1 && cg != 2) || sw < 1 || sw > 64 || (o && o->max_clusters < 0) || sched < 0 ||
-        sched > 2)
+        sched > 2 || cp < 1 || cp > 2 || (cp == 2 && cg != 2))
         return GEMM_ERR_INVALID_VALUE;
     memset(pl, 0, sizeof(*pl));
     pl->cta_group = cg;
+    pl->cluster_pairs = cp;
     pl->tile_m = kBlockM * cg;
-    pl->tile_n = cg == 2 ? Cfg2::kBN : Cfg1::kBN;
+    pl->tile_n = kCtaTileN * cp;
     pl->block_k = kBlockK;
     pl->stages = cg == 2 ? Cfg2::kStages : Cfg1::kStages;
     pl->smem_bytes = cg == 2 ? Cfg2::kSmemBytes : Cfg1::kSmemBytes;
@@ -835,7 +893,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
     pl->k_blocks = int32_t(cdiv(K, kBlockK));
     pl->num_tiles = tiles;
     pl->swizzle = int32_t(nt > 0 && sw > nt ? nt : sw);
-    int64_t resident = max_resident > 0 ? max_resident : (cg == 2 ? num_sms / 2 : num_sms);
+    int64_t resident = max_resident > 0 ? max_resident : num_sms / (cg * cp);
     if (resident < 1) resident = 1;
     if (o && o->max_clusters > 0 && o->max_clusters < resident) resident = o->max_clusters;
 
@@ -865,9 +923,9 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
         }
     }
     pl->clusters = int32_t(clusters);
-    pl->grid_ctas = int32_t(clusters * cg);
+    pl->grid_ctas = int32_t(clusters * cg * cp);
     pl->sk_tiles = int32_t(sk_tiles);
-    pl->workspace_bytes = sk_tiles > 0 ? workspace_bytes(cg, pl->tile_n, clusters) : 0;
+    pl->workspace_bytes = sk_tiles > 0 ? workspace_bytes(cg * cp, clusters) : 0;
     return GEMM_OK;
 }
 
@@ -895,7 +953,7 @@ gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t
     // C covers only the first N8 = N - N % 8 columns; the kernel writes the rest
     // with plain stores and no byte past column N-1 is ever written.
     const int64_t N8 = N & ~int64_t(7);
-    if ((s = encode_2d(&p.tmA, A, uint64_t(K), uint64_t(M), uint64_t(lda), kBlockK, kBlockM)) != GEMM_OK ||
+    if ((s = encode_2d(&p.tmA, A, uint64_t(K), uint64_t(M), uint64_t(lda), kBlockK, kBlockM / Cfg::kCP)) != GEMM_OK ||
         (s = encode_2d(&p.tmB, B, uint64_t(K), uint64_t(N), uint64_t(ldb), kBlockK, Cfg::kBRows)) != GEMM_OK ||
         (N8 > 0 && (s = encode_2d(&p.tmC, C, uint64_t(N8), uint64_t(M), uint64_t(ldc), kEpiCols, 32)) != GEMM_OK))
         return s;
@@ -915,7 +973,7 @@ gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t
     if (pl.sk_tiles > 0) {
         uint8_t* ws = static_cast<uint8_t*>(workspace);
         p.flags = reinterpret_cast<uint64_t*>(ws);
-        p.partials = reinterpret_cast<float*>(ws + flags_bytes(Cfg::kCG, pl.clusters));
+        p.partials = reinterpret_cast<float*>(ws + flags_bytes(Cfg::kCtas, pl.clusters));
     }
     p.launch_id = ++g_launch_seq;
     if (o && o->trace && o->trace_items > 0) {
@@ -929,9 +987,9 @@ gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cfg.stream = stream;
-    if (Cfg::kCG == 2) {
+    if (Cfg::kCtas > 1) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.x = Cfg::kCtas;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
@@ -950,6 +1008,7 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t ld
     if (s != GEMM_OK) return s;
     if (o && ((o->cta_group != 0 && o->cta_group != 1 && o->cta_group != 2) || o->swizzle < 0 ||
               o->swizzle > 64 || o->max_clusters < 0 || o->schedule < 0 || o->schedule > 2 ||
+              o->cluster_pairs < 0 || o->cluster_pairs > 2 || (o->cluster_pairs == 2 && o->cta_group == 1) ||
               o->trace_items < 0 || (o->trace && (reinterpret_cast<uintptr_t>(o->trace) & 7))))
         return GEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return GEMM_OK;
@@ -964,10 +1023,11 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t ld
         if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
         return GEMM_OK;
     }
-    const int cg = (o && o->cta_group) ? o->cta_group : 2;
+    const gemm_f16_nt_options_t ro = resolve_options(o, N, lda, ldb);
+    const int cg = ro.cta_group, cp = ro.cluster_pairs;
     gemm_f16_nt_plan_t pl;
-    const int resident = cg == 2 ? st->max_clusters2 : st->max_ctas1;
-    if ((s = make_plan(M, N, K, st->sms, resident, o, &pl)) != GEMM_OK) return s;
+    const int resident = resident_clusters_for(*st, ro);
+    if ((s = make_plan(M, N, K, st->sms, resident, &ro, &pl)) != GEMM_OK) return s;
     void* ws = nullptr;
     if (pl.sk_tiles > 0) {
         // The workspace is taken from the library's pool on the caller's stream
@@ -975,13 +1035,14 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t ld
         if (!st->pool || cudaMallocFromPoolAsync(&ws, size_t(pl.workspace_bytes), st->pool, stream) != cudaSuccess) {
             cudaGetLastError();
             ws = nullptr;
-            gemm_f16_nt_options_t dp = o ? *o : gemm_f16_nt_options_t{};
+            gemm_f16_nt_options_t dp = ro;
             dp.schedule = 1;   // no workspace: whole tiles only
             if ((s = make_plan(M, N, K, st->sms, resident, &dp, &pl)) != GEMM_OK) return s;
         }
     }
-    s = cg == 2 ? launch<Cfg2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, o, st->watchdog, ws)
-                : launch<Cfg1>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, o, st->watchdog, ws);
+    if (cg == 1) s = launch<Cfg1>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
+    else if (cp == 2) s = launch<Cfg2x2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
+    else s = launch<Cfg2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
     if (ws && cudaFreeAsync(ws, stream) != cudaSuccess) {
         cudaGetLastError();
         if (s == GEMM_OK) s = GEMM_ERR_LAUNCH;
@@ -1043,8 +1104,9 @@ gemm_status_t run_noalloc(int64_t M, int64_t N, int64_t K, const uint16_t* A, in
         if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
         return GEMM_OK;
     }
+    const gemm_f16_nt_options_t ro = resolve_options(nullptr, N, lda, ldb);
     gemm_f16_nt_plan_t pl;
-    if ((s = make_plan(M, N, K, st->sms, st->max_clusters2, nullptr, &pl)) != GEMM_OK) return s;
+    if ((s = make_plan(M, N, K, st->sms, resident_clusters_for(*st, ro), &ro, &pl)) != GEMM_OK) return s;
     void* ws = nullptr;
     if (pl.sk_tiles > 0) {
         if (uint64_t(pl.workspace_bytes) > kStaticScratchBytes) return GEMM_ERR_SCRATCH_LIMIT;
@@ -1053,7 +1115,9 @@ gemm_status_t run_noalloc(int64_t M, int64_t N, int64_t K, const uint16_t* A, in
     // Nothing in the scratch has to start at zero: each launch's completion
     // flags carry that launch's own 64-bit id, so values left by an earlier
     // call never match, and every partial tile is written before it is read.
-    return launch<Cfg2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr, st->watchdog, ws);
+    if (ro.cluster_pairs == 2)
+        return launch<Cfg2x2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
+    return launch<Cfg2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
 }
 
 }  // namespace g16
@@ -1099,13 +1163,14 @@ G16_EXPORT gemm_status_t gemm_f16_nt_device_status(void* stream, uint32_t* flags
 }
 
 G16_EXPORT gemm_status_t gemm_f16_nt_device_limits(int32_t* sms, int32_t* resident_pairs,
-                                                   int32_t* resident_ctas) {
+                                                   int32_t* resident_ctas, int32_t* resident_pair_pairs) {
     g16::DeviceState* st = nullptr;
     gemm_status_t s = g16::current_device(&st);
     if (s != GEMM_OK) return s;
     if (sms) *sms = st->sms;
     if (resident_pairs) *resident_pairs = st->max_clusters2;
     if (resident_ctas) *resident_ctas = st->max_ctas1;
+    if (resident_pair_pairs) *resident_pair_pairs = st->max_clusters4;
     return GEMM_OK;
 }
 
@@ -1127,7 +1192,9 @@ G16_EXPORT const char* gemm_f16_nt_status_string(int32_t status) {
 G16_EXPORT gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms,
                                           int32_t max_clusters, const gemm_f16_nt_options_t* opts,
                                           gemm_f16_nt_plan_t* plan) {
-    return g16::make_plan(M, N, K, num_sms, max_clusters, opts, plan);
+    // the automatic choices as for contiguous operands (lda = ldb = K)
+    const gemm_f16_nt_options_t ro = g16::resolve_options(opts, N, K, K);
+    return g16::make_plan(M, N, K, num_sms, max_clusters, &ro, plan);
 }
 
 G16_EXPORT gemm_status_t gemm_f16_nt_tile_coord(int64_t linear, int32_t m_tiles, int32_t n_tiles,

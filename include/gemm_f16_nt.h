@@ -164,6 +164,15 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  *                 (stamps from the leader CTA's MMA thread and one of its
  *                 epilogue warps), j=7 total ns the MMA thread waited for
  *                 filled pipeline stages during the item.
+ *   cluster_pairs 1: a cluster is one CTA pair; 2: a cluster is two CTA
+ *                 pairs side by side in N (a 256×512 tile) that share their A
+ *                 rows: each CTA loads half of its A tile and TMA multicasts it
+ *                 to the same-rank CTA of the other pair, which halves A's
+ *                 L2 → SM traffic.  Clusters of four CTAs fit on fewer SMs (144
+ *                 of 152 on a GB300).  Needs cta_group 2.  Default (0): 2 when
+ *                 lda or ldb is not a multiple of 64 elements (128 bytes: each
+ *                 128-byte row slice of a tile then spans two L2 lines and L2
+ *                 traffic is the limit) and N > 256, else 1.
  */
 typedef struct {
     int32_t cta_group;
@@ -174,6 +183,8 @@ typedef struct {
     int32_t schedule;
     int32_t trace_items;
     uint64_t *trace;
+    int32_t cluster_pairs;
+    int32_t reserved;     /* must be 0 */
 } gemm_f16_nt_options_t;
 
 /* gemm_f16_nt with options (opts may be NULL).  Same arguments, layout,
@@ -203,12 +214,13 @@ gemm_status_t gemm_f16_nt_device_status(void *stream, uint32_t *flags);
 
 /*
  * What the one-time set-up found on the current device: its SM count and how
- * many CTA pairs (cta_group 2) and single CTAs (cta_group 1) of the GEMM
- * kernel can be resident at once (the persistent grid sizes).  Any pointer may
- * be NULL.  GEMM_ERR_UNSUPPORTED_DEVICE without a usable device.
+ * many clusters of the GEMM kernel can be resident at once (the persistent
+ * grid sizes): CTA pairs (cta_group 2), single CTAs (cta_group 1), and
+ * clusters of two pairs (cluster_pairs 2).  Any pointer may be NULL.
+ * GEMM_ERR_UNSUPPORTED_DEVICE without a usable device.
  */
 gemm_status_t gemm_f16_nt_device_limits(int32_t *sms, int32_t *resident_pairs,
-                                        int32_t *resident_ctas);
+                                        int32_t *resident_ctas, int32_t *resident_pair_pairs);
 
 /* A static, human-readable name for a gemm_status_t value. */
 const char *gemm_f16_nt_status_string(int32_t status);
@@ -216,15 +228,16 @@ const char *gemm_f16_nt_status_string(int32_t status);
 /* ---- host-only helpers (no CUDA call; used by the scheduler and its tests) ---- */
 
 /*
- * The launch plan gemm_f16_nt would use for a problem on a device with
- * `num_sms` SMs and room for `max_clusters` resident clusters (0 = num_sms/2
- * pairs, or num_sms CTAs for cta_group 1).  Returns GEMM_ERR_INVALID_VALUE for
- * sizes out of range.
+ * The launch plan gemm_f16_nt would use for a problem with contiguous operands
+ * (lda = ldb = K; the automatic cluster choice depends on them) on a device
+ * with `num_sms` SMs and room for `max_clusters` resident clusters of the
+ * chosen kind (0 = num_sms divided by the CTAs per cluster).  Returns
+ * GEMM_ERR_INVALID_VALUE for sizes or options out of range.
  */
 typedef struct {
     int32_t cta_group;     /* 1 or 2 */
-    int32_t tile_m;        /* rows of C per tile (128 · cta_group) */
-    int32_t tile_n;        /* columns of C per tile */
+    int32_t tile_m;        /* rows of C per cluster tile (128 · cta_group) */
+    int32_t tile_n;        /* columns of C per cluster tile */
     int32_t block_k;       /* k per pipeline stage */
     int32_t stages;        /* shared-memory ring depth */
     int32_t m_tiles;       /* cdiv(M, tile_m) */
@@ -237,7 +250,7 @@ typedef struct {
     int32_t smem_bytes;    /* dynamic shared memory per CTA */
     int32_t tmem_cols;     /* tensor-memory columns allocated per CTA */
     int32_t sk_tiles;      /* tiles [0, sk_tiles) are split in k across all clusters (stream-K) */
-    int32_t reserved;
+    int32_t cluster_pairs; /* CTA pairs per cluster (tile_n = 256 · cluster_pairs) */
     int64_t workspace_bytes; /* device workspace a stream-K launch needs (0 if none) */
 } gemm_f16_nt_plan_t;
 

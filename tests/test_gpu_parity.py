@@ -93,6 +93,30 @@ def test_stream_k_split_tiles(cg, max_clusters, shape):
     assert np.array_equal(C1.view(np.uint16), C2.view(np.uint16))
 
 
+@pytest.mark.parametrize("shape,max_clusters,schedule", [
+    ((1100, 2100, 520), 0, 0),      # 5 x 5 cluster tiles of 256 x 512
+    ((1100, 2100, 520), 2, 1),      # persistent: 12-13 cluster tiles per cluster
+    ((513, 1300, 200), 0, 2),       # odd number of 256-wide N tiles: pair 1 out of range
+    ((256, 300, 4096), 0, 2),       # one cluster tile split in k over many clusters
+    ((4000, 3000, 5000), 0, 0),     # the ragged workload shape
+    ((7, 9, 3), 0, 0),
+])
+def test_two_pairs_per_cluster_a_multicast(shape, max_clusters, schedule):
+    M, N, K = shape
+    A = inputs.draw((M, K), inputs.U, 71 + M)
+    B = inputs.draw((N, K), inputs.U, 72 + N)
+    o = g.Options(cluster_pairs=2, max_clusters=max_clusters, schedule=schedule)
+    C = run(A, B, options=o)
+    check_close(C, oracle.gemm_f16_nt(A, B), K, f"two pairs {shape}")
+
+
+def test_two_pairs_integers_bit_exact():
+    M, N, K = 1000, 1500, 2000
+    A = inputs.draw((M, K), inputs.I2, 73)
+    B = inputs.draw((N, K), inputs.I2, 74)
+    check_bitexact(run(A, B, options=g.Options(cluster_pairs=2)), oracle.gemm_f16_nt(A, B), "two pairs int")
+
+
 def test_stream_k_integers_bit_exact_and_matches_whole_tiles():
     M, N, K = 1200, 1000, 2200
     A = inputs.draw((M, K), inputs.I2, 93)

@@ -20,8 +20,8 @@ pytestmark = pytest.mark.gpu
 import dense_fp16_gemm_gb300 as g  # noqa: E402
 
 
-@pytest.mark.parametrize("cg", [2, 1])
-def test_stalled_pipeline_reports_timeout_then_recovers(cg):
+@pytest.mark.parametrize("cg,cp", [(2, 1), (1, 1), (2, 2)])
+def test_stalled_pipeline_reports_timeout_then_recovers(cg, cp):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     assert g.device_status() == 0
@@ -30,7 +30,7 @@ def test_stalled_pipeline_reports_timeout_then_recovers(cg):
     B = inputs.draw((N, K), inputs.U, 82)
     Ad, Bd = to_device(A), to_device(B)
     Cd, _ = empty_out(M, N)
-    g.gemm_f16_nt(Ad, Bd, Cd, options=g.Options(cta_group=cg, inject_stall=1,
+    g.gemm_f16_nt(Ad, Bd, Cd, options=g.Options(cta_group=cg, cluster_pairs=cp, inject_stall=1,
                                                 timeout_ns=20_000_000))
     word = g.device_status()
     assert word & 1, f"watchdog word {word:#x}"
@@ -39,7 +39,7 @@ def test_stalled_pipeline_reports_timeout_then_recovers(cg):
     assert sites and sites <= {2, 4}, f"unexpected wait sites in {word:#x}"
     assert np.isnan(to_host(Cd).astype(np.float32)).all(), "C was written by a stalled kernel"
     # the context is intact: a normal call right after is correct
-    g.gemm_f16_nt(Ad, Bd, Cd, options=g.Options(cta_group=cg))
+    g.gemm_f16_nt(Ad, Bd, Cd, options=g.Options(cta_group=cg, cluster_pairs=cp))
     torch.cuda.synchronize()
     assert g.device_status() == 0
     check_close(to_host(Cd), oracle.gemm_f16_nt(A, B), K, "after watchdog")

@@ -122,7 +122,8 @@ def test_plan_stream_k_schedule():
     p = g.plan(256 * 15, 256 * 10, 4096, num_sms=152)     # 150 tiles: last wave 74/76 full
     assert p["sk_tiles"] == 0
     # fewer tiles than pairs: spread when each share keeps >= 8 k-blocks
-    p = g.plan(1000, 700, 1000)                           # 12 tiles x 16 k-blocks
+    one = g.Options(cluster_pairs=1)
+    p = g.plan(1000, 700, 1000, options=one)              # 12 tiles x 16 k-blocks
     assert (p["sk_tiles"], p["clusters"]) == (12, 24)
     p = g.plan(256, 256, 256)                             # 1 tile x 4 k-blocks: not worth it
     assert (p["sk_tiles"], p["clusters"]) == (0, 1)
@@ -132,9 +133,31 @@ def test_plan_stream_k_schedule():
         g.plan(256, 256, 256, options=g.Options(schedule=3))
 
 
+def test_plan_two_pairs_per_cluster():
+    o = g.Options(cluster_pairs=2)
+    p = g.plan(8192, 8192, 8192, num_sms=152, max_clusters=36, options=o)
+    assert (p["cluster_pairs"], p["tile_m"], p["tile_n"]) == (2, 256, 512)
+    assert (p["m_tiles"], p["n_tiles"], p["num_tiles"]) == (32, 16, 512)
+    assert (p["clusters"], p["grid_ctas"]) == (36, 144)
+    assert p["sk_tiles"] == 512 % 36 + 36               # last wave 8/36 full
+    assert p["workspace_bytes"] == 36 * 4 * 4 * 8 + 36 * 4 * 128 * 256 * 4
+    p = g.plan(4000, 3000, 5000, num_sms=152, max_clusters=36, options=o)
+    assert (p["m_tiles"], p["n_tiles"]) == (16, 6)
+    with pytest.raises(g.GemmError):
+        g.plan(256, 256, 256, options=g.Options(cluster_pairs=2, cta_group=1))
+    with pytest.raises(g.GemmError):
+        g.plan(256, 256, 256, options=g.Options(cluster_pairs=3))
+
+
 def test_plan_edges_and_options():
-    p = g.plan(4000, 3000, 5000)
+    p = g.plan(4000, 3000, 5000, options=g.Options(cluster_pairs=1))
     assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (16, 12, 79)
+    # K = 5000: 10,000-byte rows are not 128-byte multiples, so by default two
+    # pairs share A through multicast (256 x 512 cluster tiles)
+    p = g.plan(4000, 3000, 5000)
+    assert (p["cluster_pairs"], p["m_tiles"], p["n_tiles"]) == (2, 16, 6)
+    assert g.plan(8192, 8192, 8192)["cluster_pairs"] == 1
+    assert g.plan(4000, 256, 5000)["cluster_pairs"] == 1      # too narrow for two pairs
     p = g.plan(100, 100, 8)                        # one pair tile, rank-1 rows all out of range
     assert (p["num_tiles"], p["clusters"], p["grid_ctas"]) == (1, 1, 2)
     p1 = g.plan(4000, 3000, 5000, options=g.Options(cta_group=1))

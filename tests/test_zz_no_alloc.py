@@ -39,7 +39,9 @@ def test_noalloc_matches_gemm_f16_nt_on_two_calls(M, N, K, uses_scratch):
         pytest.skip("no CUDA device")
     lib = g.library()
     lim = g.device_limits()
-    pl = g.plan(M, N, K, num_sms=lim["sms"], max_clusters=lim["resident_pairs"])
+    pl = g.plan(M, N, K, num_sms=lim["sms"])
+    resident = lim["resident_pair_pairs"] if pl["cluster_pairs"] == 2 else lim["resident_pairs"]
+    pl = g.plan(M, N, K, num_sms=lim["sms"], max_clusters=resident)
     assert (pl["sk_tiles"] > 0) == uses_scratch
     A = inputs.draw((M, K), inputs.U, 301 + M)
     B = inputs.draw((N, K), inputs.U, 302 + N)
