@@ -900,16 +900,21 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
     // Schedule.  Whole tiles round-robin over the clusters leave the last wave
     // partly empty when tiles % clusters != 0.  The stream-K part spreads the
     // k-block units of (the partial wave + one full wave) evenly instead; with
-    // fewer tiles than clusters it spreads all of them.  Auto mode (0) uses it
-    // when the last wave is at most 90 % full and every share keeps at least
-    // kMinSplitKb k-blocks; 1 = whole tiles only; 2 = stream-K whenever it can.
+    // fewer tiles than clusters it spreads all of them.  Splitting costs fp32
+    // partial tiles through L2 (and DRAM), so auto mode (0) splits only when at
+    // least 10 % of the whole-tile schedule's tile slots would sit idle, with one
+    // pair per cluster (two-pair clusters are picked when L2 traffic already
+    // limits), and every share keeps at least kMinSplitKb k-blocks.  Measured on
+    // GB300: 4096^3 (16 % idle) gains 5.6 %; 8192^3 (3.8 % idle, power-capped)
+    // loses 1.4 % when split.  1 = whole tiles only; 2 = stream-K whenever it can.
     const int64_t kb = pl->k_blocks;
     int64_t clusters = tiles < resident ? tiles : resident;
     int64_t sk_tiles = 0;
     if (tiles > 0 && kb > 0 && sched != 1) {
         if (tiles >= resident) {
             const int64_t rem = tiles % resident;
-            const bool worth = rem != 0 && rem * 10 <= resident * 9 && kb >= kMinSplitKb;
+            const int64_t slots = (tiles + resident - 1) / resident * resident;
+            const bool worth = rem != 0 && cp == 1 && (slots - tiles) * 10 >= slots && kb >= kMinSplitKb;
             if (sched == 2 || worth) sk_tiles = rem + resident;
             if (sk_tiles > tiles) sk_tiles = tiles;
         } else {

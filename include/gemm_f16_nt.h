@@ -141,9 +141,11 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  *                 sets the watchdog word, releases its tensor memory and
  *                 exits without writing C.
  *   schedule      0 (default): whole tiles round-robin over the persistent
- *                 clusters, except that when the last wave of tiles would be
- *                 at most 90 % full the k-block work of that wave plus one
- *                 full wave is split evenly across all clusters (stream-K),
+ *                 clusters, except that when at least 10 % of that schedule's
+ *                 tile slots would sit idle in its last wave (one pair per
+ *                 cluster), or when there are fewer tiles than clusters, the
+ *                 k-block work of the last wave plus one full wave (or of all
+ *                 tiles) is split evenly across all clusters (stream-K),
  *                 with fp32 partial tiles summed by each tile's first piece in
  *                 a fixed order (results are reproducible run to run);
  *                 1: whole tiles only; 2: stream-K whenever possible (tests).

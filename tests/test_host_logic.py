@@ -109,14 +109,17 @@ def test_plan_headline_shape():
 
 
 def test_plan_stream_k_schedule():
-    # 8192^3: 1024 tiles over 76 pairs leaves a last wave of 36 (47 % full):
-    # that wave plus one full wave (112 tiles) is split in k over all pairs
-    p = g.plan(8192, 8192, 8192, num_sms=152)
-    assert p["sk_tiles"] == 36 + 76
+    # 4096^3: 256 tiles over 76 pairs leave 48 of 304 slots (16 %) idle: the
+    # last wave (28 tiles) plus one full wave is split in k over all pairs
+    p = g.plan(4096, 4096, 4096, num_sms=152)
+    assert p["sk_tiles"] == 28 + 76
     assert p["workspace_bytes"] == 76 * 2 * 4 * 8 + 76 * 2 * 128 * 256 * 4
+    # 8192^3: 40 of 1064 slots (3.8 %) idle: whole tiles, unless forced
+    assert g.plan(8192, 8192, 8192, num_sms=152)["sk_tiles"] == 0
+    assert g.plan(8192, 8192, 8192, options=g.Options(schedule=2))["sk_tiles"] == 36 + 76
     # whole tiles only on request, or when the last wave is nearly full
-    assert g.plan(8192, 8192, 8192, options=g.Options(schedule=1))["sk_tiles"] == 0
-    assert g.plan(8192, 8192, 8192, options=g.Options(schedule=1))["workspace_bytes"] == 0
+    assert g.plan(4096, 4096, 4096, options=g.Options(schedule=1))["sk_tiles"] == 0
+    assert g.plan(4096, 4096, 4096, options=g.Options(schedule=1))["workspace_bytes"] == 0
     p = g.plan(256 * 19, 256 * 8, 4096, num_sms=152)      # 152 tiles = 2 full waves
     assert p["sk_tiles"] == 0
     p = g.plan(256 * 15, 256 * 10, 4096, num_sms=152)     # 150 tiles: last wave 74/76 full
@@ -139,7 +142,10 @@ def test_plan_two_pairs_per_cluster():
     assert (p["cluster_pairs"], p["tile_m"], p["tile_n"]) == (2, 256, 512)
     assert (p["m_tiles"], p["n_tiles"], p["num_tiles"]) == (32, 16, 512)
     assert (p["clusters"], p["grid_ctas"]) == (36, 144)
-    assert p["sk_tiles"] == 512 % 36 + 36               # last wave 8/36 full
+    assert p["sk_tiles"] == 0                           # auto: two pairs keep whole tiles
+    o = g.Options(cluster_pairs=2, schedule=2)
+    p = g.plan(8192, 8192, 8192, num_sms=152, max_clusters=36, options=o)
+    assert p["sk_tiles"] == 512 % 36 + 36               # forced: last wave 8/36 + one wave
     assert p["workspace_bytes"] == 36 * 4 * 4 * 8 + 36 * 4 * 128 * 256 * 4
     p = g.plan(4000, 3000, 5000, num_sms=152, max_clusters=36, options=o)
     assert (p["m_tiles"], p["n_tiles"]) == (16, 6)
