@@ -518,7 +518,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gemm_8192", choices=sorted(inputs.WORKLOADS))
-    ap.add_argument("--repeat", type=int, default=3, help="timed regions per process (median)")
+    ap.add_argument("--repeat", type=int, default=1,
+                    help="timed regions of K steps per process (the median is reported)")
     ap.add_argument("--cooldown", type=float, default=1.0, help="seconds of idle before each repeat")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -89,6 +89,36 @@ def draw(shape, dist: tuple, seed: int, ld: int | None = None) -> np.ndarray:
     return buf[:, :cols]
 
 
+def draw_bf16(shape, dist: tuple, seed: int, ld: int | None = None) -> np.ndarray:
+    """Like `draw`, but rounded to bfloat16: the result holds bf16 bit
+    patterns as uint16 (numpy has no bfloat16 type).  The float32 values are
+    rounded to nearest, ties to even, on their bit pattern; padding columns
+    (ld > cols) hold a bf16 NaN (0x7fc0)."""
+    rows, cols = shape
+    rng = np.random.Generator(np.random.PCG64(seed))
+    kind = dist[0]
+    if kind == "uniform":
+        x = rng.random(size=(rows, cols), dtype=np.float32)
+        x *= np.float32(dist[2] - dist[1])
+        x += np.float32(dist[1])
+    elif kind == "normal":
+        x = rng.standard_normal(size=(rows, cols), dtype=np.float32)
+        x = (x * np.float32(dist[2]) + np.float32(dist[1])).astype(np.float32)
+    elif kind == "int":
+        x = rng.integers(dist[1], dist[2] + 1, size=(rows, cols), dtype=np.int8).astype(np.float32)
+    else:
+        raise ValueError(f"unknown distribution {kind!r}")
+    u = x.view(np.uint32).astype(np.uint64)
+    h = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)   # finite inputs only
+    if ld is None or ld == cols:
+        return h
+    if ld < cols:
+        raise ValueError("ld < cols")
+    buf = np.full((rows, ld), 0x7FC0, dtype=np.uint16)
+    buf[:, :cols] = h
+    return buf[:, :cols]
+
+
 def operands(w: Workload):
     """(A [M,K], B [N,K]) for a workload, contiguous float16."""
     return draw((w.M, w.K), w.dist_a, w.seed_a), draw((w.N, w.K), w.dist_b, w.seed_b)

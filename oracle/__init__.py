@@ -63,10 +63,10 @@ def default_threads() -> int:
         return max(1, os.cpu_count() or 1)
 
 
-def _rows(x: np.ndarray, name: str):
-    """(pointer, leading dimension) of a 2-D fp16 array with unit column stride."""
-    if x.dtype != np.float16 or x.ndim != 2:
-        raise TypeError(f"{name} must be a 2-D float16 array")
+def _rows(x: np.ndarray, name: str, dtype=np.float16):
+    """(pointer, leading dimension) of a 2-D 16-bit array with unit column stride."""
+    if x.dtype != dtype or x.ndim != 2:
+        raise TypeError(f"{name} must be a 2-D {np.dtype(dtype).name} array")
     if x.shape[1] > 1 and x.strides[1] != 2:
         raise ValueError(f"{name} must have unit stride along its last axis")
     ld = x.strides[0] // 2 if x.shape[0] > 1 else max(x.shape[1], 1)
@@ -91,6 +91,15 @@ class Oracle:
         lib.oracle_f64_to_f16_array.restype = None
         lib.oracle_f16_to_f64_array.argtypes = [_i64, _p, _p]
         lib.oracle_f16_to_f64_array.restype = None
+        lib.oracle_gemm_bf16_nt.argtypes = [_i64, _i64, _i64, _p, _i64, _p, _i64, _p, _i64,
+                                            ctypes.c_int]
+        lib.oracle_gemm_bf16_nt.restype = None
+        lib.oracle_gemm_bf16_nt_points.argtypes = [_i64, _p, _i64, _p, _i64, _i64, _p, _p, _p]
+        lib.oracle_gemm_bf16_nt_points.restype = None
+        lib.oracle_f64_to_bf16_array.argtypes = [_i64, _p, _p]
+        lib.oracle_f64_to_bf16_array.restype = None
+        lib.oracle_bf16_to_f64_array.argtypes = [_i64, _p, _p]
+        lib.oracle_bf16_to_f64_array.restype = None
         self.lib = lib
         self.path = lib_path
 
@@ -151,6 +160,56 @@ class Oracle:
                                            out.ctypes.data, out64.ctypes.data)
         return out, out64
 
+    # ---- bfloat16: arrays hold bf16 bit patterns as numpy.uint16 ----------
+
+    def gemm_bf16_nt(self, A: np.ndarray, B: np.ndarray, C: np.ndarray | None = None,
+                     threads: int | None = None) -> np.ndarray:
+        """C = RNE_bf16(A · Bᵀ), fp64 sequential sum per element; A [M, K] and
+        B [N, K] are bf16 bit patterns (uint16), and so is the result."""
+        M, K = A.shape
+        N, K2 = B.shape
+        if K2 != K:
+            raise ValueError("A and B disagree on K")
+        if C is None:
+            C = np.empty((M, N), dtype=np.uint16)
+        if C.shape != (M, N):
+            raise ValueError("C has the wrong shape")
+        pa, lda = _rows(A, "A", np.uint16)
+        pb, ldb = _rows(B, "B", np.uint16)
+        pc, ldc = _rows(C, "C", np.uint16)
+        self.lib.oracle_gemm_bf16_nt(M, N, K, pa, lda, pb, ldb, pc, ldc,
+                                     threads or default_threads())
+        return C
+
+    def gemm_bf16_nt_points(self, A: np.ndarray, B: np.ndarray, rows, cols) -> np.ndarray:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        cols = np.ascontiguousarray(cols, dtype=np.int64)
+        M, K = A.shape
+        N, _ = B.shape
+        if rows.size and (rows.min() < 0 or rows.max() >= M
+                          or cols.min() < 0 or cols.max() >= N):
+            raise IndexError("sample position out of range")
+        out = np.empty(rows.shape, dtype=np.uint16)
+        pa, lda = _rows(A, "A", np.uint16)
+        pb, ldb = _rows(B, "B", np.uint16)
+        self.lib.oracle_gemm_bf16_nt_points(K, pa, lda, pb, ldb, rows.size, rows.ctypes.data,
+                                            cols.ctypes.data, out.ctypes.data)
+        return out
+
+    def round_f64_to_bf16(self, x) -> np.ndarray:
+        """The oracle's own fp64 -> bf16 round-to-nearest-even (uint16 bits)."""
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        out = np.empty(x.shape, dtype=np.uint16)
+        self.lib.oracle_f64_to_bf16_array(x.size, x.ctypes.data, out.ctypes.data)
+        return out
+
+    def widen_bf16_to_f64(self, h) -> np.ndarray:
+        """The oracle's own bf16 -> fp64 decoding."""
+        h = np.ascontiguousarray(np.asarray(h, dtype=np.uint16))
+        out = np.empty(h.shape, dtype=np.float64)
+        self.lib.oracle_bf16_to_f64_array(h.size, h.ctypes.data, out.ctypes.data)
+        return out
+
     def round_f64_to_f16(self, x) -> np.ndarray:
         """The oracle's own fp64 -> fp16 round-to-nearest-even."""
         x = np.ascontiguousarray(x, dtype=np.float64)
@@ -192,3 +251,19 @@ def round_f64_to_f16(x):
 
 def widen_f16_to_f64(h):
     return default().widen_f16_to_f64(h)
+
+
+def gemm_bf16_nt(A, B, C=None, threads=None):
+    return default().gemm_bf16_nt(A, B, C, threads)
+
+
+def gemm_bf16_nt_points(A, B, rows, cols):
+    return default().gemm_bf16_nt_points(A, B, rows, cols)
+
+
+def round_f64_to_bf16(x):
+    return default().round_f64_to_bf16(x)
+
+
+def widen_bf16_to_f64(h):
+    return default().widen_bf16_to_f64(h)

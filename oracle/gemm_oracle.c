@@ -29,6 +29,10 @@
  *
  * Threads split the output by row blocks; each element's summation order is
  * the same whatever the thread count.
+ *
+ * The same product with bfloat16 operands and result (oracle_gemm_bf16_nt and
+ * its helpers, at the end of this file) serves the bf16 variant of the
+ * method: the sum is again a sequential fp64 sum, rounded once, to bf16.
  */
 #include <math.h>
 #include <pthread.h>
@@ -214,4 +218,157 @@ void oracle_f64_to_f16_array(int64_t n, const double *x, uint16_t *out)
 void oracle_f16_to_f64_array(int64_t n, const uint16_t *h, double *out)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_f16_to_f64(h[i]);
+}
+
+/* ---- bfloat16 (the same product with bf16 operands and result) ------------
+ *
+ * bfloat16: 1 sign bit, 8 exponent bits with bias 127, 7 fraction bits,
+ * subnormals below 2^-126 (spacing 2^-133), largest finite (2 - 2^-7)·2^127.
+ * The sum is the same sequential fp64 sum; the one final rounding is to the
+ * nearest bf16, ties to the even significand, overflowing to ±inf.
+ */
+
+double oracle_bf16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int efield = (h >> 7) & 0xff;
+    int frac = h & 0x7f;
+    double v;
+    if (efield == 0) {
+        v = ldexp((double)frac, -133);                 /* subnormal: frac * 2^-133 */
+    } else if (efield == 255) {
+        v = frac ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(frac | 0x80), efield - 134); /* 1.frac * 2^(e-127) */
+    }
+    return sign ? -v : v;
+}
+
+/* For |x| in [2^E, 2^(E+1)) with E >= -126 the bf16 grid spacing is 2^(E-7);
+ * below 2^-126 it is 2^-133.  q = |x| / spacing is exact, r = RNE(q) lies in
+ * [0, 256], and the result is r * spacing. */
+uint16_t oracle_f64_to_bf16(double x)
+{
+    if (isnan(x)) return 0x7fc0;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (isinf(a)) return sign | 0x7f80;
+    if (a == 0.0) return sign;
+
+    int e2;
+    (void)frexp(a, &e2);
+    int E = e2 - 1;
+    if (E > 127) return sign | 0x7f80;
+    if (E < -126) E = -126;
+
+    double q = ldexp(a, 7 - E);   /* in [0, 256) */
+    double fl = floor(q);
+    double rem = q - fl;
+    double r;
+    if (rem > 0.5) {
+        r = fl + 1.0;
+    } else if (rem < 0.5) {
+        r = fl;
+    } else {
+        r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+    }
+    long ri = (long)r;
+
+    if (ri < 128) {
+        /* only possible when E == -126: a subnormal (or zero) result */
+        return sign | (uint16_t)ri;
+    }
+    if (ri == 256) {
+        ri = 128;
+        E += 1;
+        if (E > 127) return sign | 0x7f80;
+    }
+    return sign | (uint16_t)(((E + 127) << 7) | (int)(ri - 128));
+}
+
+static double g_bf16_table[65536];
+static pthread_once_t g_bf16_once = PTHREAD_ONCE_INIT;
+
+static void build_bf16_table(void)
+{
+    for (uint32_t h = 0; h < 65536u; ++h) g_bf16_table[h] = oracle_bf16_to_f64((uint16_t)h);
+}
+
+static double dot_bf16(int64_t K, const uint16_t *a, const uint16_t *b)
+{
+    double s = 0.0;
+    for (int64_t k = 0; k < K; ++k) s += g_bf16_table[a[k]] * g_bf16_table[b[k]];
+    return s;
+}
+
+typedef struct {
+    int64_t m0, m1, N, K;
+    const uint16_t *A; int64_t lda;
+    const uint16_t *B; int64_t ldb;
+    uint16_t *C; int64_t ldc;
+} bf16_job;
+
+static void *bf16_worker(void *p)
+{
+    bf16_job *j = (bf16_job *)p;
+    for (int64_t m = j->m0; m < j->m1; ++m)
+        for (int64_t n = 0; n < j->N; ++n)
+            j->C[m * j->ldc + n] = oracle_f64_to_bf16(dot_bf16(j->K, j->A + m * j->lda, j->B + n * j->ldb));
+    return NULL;
+}
+
+/* C[m*ldc+n] = RNE_bf16(sum_k A[m,k]·B[n,k]) for all m < M, n < N (bf16 bit
+ * patterns in and out). */
+void oracle_gemm_bf16_nt(int64_t M, int64_t N, int64_t K,
+                         const uint16_t *A, int64_t lda,
+                         const uint16_t *B, int64_t ldb,
+                         uint16_t *C, int64_t ldc, int nthreads)
+{
+    pthread_once(&g_bf16_once, build_bf16_table);
+    if (M <= 0 || N <= 0) return;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > M) nthreads = (int)M;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t tid[256];
+    int created[256];
+    bf16_job job[256];
+    int64_t per = (M + nthreads - 1) / nthreads;
+    int njobs = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        int64_t m0 = t * per, m1 = m0 + per;
+        if (m0 >= M) break;
+        if (m1 > M) m1 = M;
+        job[t] = (bf16_job){m0, m1, N, K, A, lda, B, ldb, C, ldc};
+        created[t] = 0;
+        njobs = t + 1;
+    }
+    for (int t = 1; t < njobs; ++t)
+        created[t] = (pthread_create(&tid[t], NULL, bf16_worker, &job[t]) == 0);
+    bf16_worker(&job[0]);
+    for (int t = 1; t < njobs; ++t) {
+        if (created[t]) pthread_join(tid[t], NULL);
+        else bf16_worker(&job[t]);
+    }
+}
+
+/* Selected elements, one by one (bf16). */
+void oracle_gemm_bf16_nt_points(int64_t K,
+                                const uint16_t *A, int64_t lda,
+                                const uint16_t *B, int64_t ldb,
+                                int64_t npts, const int64_t *rows, const int64_t *cols,
+                                uint16_t *out)
+{
+    pthread_once(&g_bf16_once, build_bf16_table);
+    for (int64_t i = 0; i < npts; ++i)
+        out[i] = oracle_f64_to_bf16(dot_bf16(K, A + rows[i] * lda, B + cols[i] * ldb));
+}
+
+void oracle_f64_to_bf16_array(int64_t n, const double *x, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f64_to_bf16(x[i]);
+}
+
+void oracle_bf16_to_f64_array(int64_t n, const uint16_t *h, double *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_to_f64(h[i]);
 }

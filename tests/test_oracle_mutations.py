@@ -2,7 +2,7 @@
 
 Each case below plants one mistake in a copy of the oracle's C source (on the
 CPU, in a temporary directory), compiles it, and runs every pin of
-test_oracle_pins.py against the planted copy: at least one pin has to fail.
+test_oracle_pins.py and test_oracle_pins_bf16.py against the planted copy: at least one pin has to fail.
 The committed oracle is never modified.
 """
 import inspect
@@ -12,6 +12,7 @@ import pytest
 
 import oracle
 import tests.test_oracle_pins as pins
+import tests.test_oracle_pins_bf16 as pins_bf16
 
 _SRC = os.path.join(os.path.dirname(oracle.__file__), "gemm_oracle.c")
 
@@ -33,13 +34,25 @@ MUTATIONS = {
     "overflow_saturates": ("if (E > 15) return sign | 0x7c00;\n    if (E < -14)",
                            "if (E > 15) return sign | 0x7bff;\n    if (E < -14)"),
     "B_row_stride_ignored": ("j->B + n * j->ldb", "j->B + n * j->K"),
+    "bf16_fp32_accumulator": (
+        "    double s = 0.0;\n    for (int64_t k = 0; k < K; ++k) s += g_bf16_table[a[k]] * g_bf16_table[b[k]];",
+        "    float s = 0.0f;\n    for (int64_t k = 0; k < K; ++k) s += (float)(g_bf16_table[a[k]] * g_bf16_table[b[k]]);"),
+    "bf16_subnormal_scale": ("v = ldexp((double)frac, -133);", "v = ldexp((double)frac, -132);"),
+    "bf16_exponent_bias": ("v = ldexp((double)(frac | 0x80), efield - 134);",
+                           "v = ldexp((double)(frac | 0x80), efield - 133);"),
+    "bf16_round_bias": ("double q = ldexp(a, 7 - E);", "double q = ldexp(a, 7 - E) + 0.25;"),
+    "bf16_overflow_saturates": ("if (E > 127) return sign | 0x7f80;\n    if (E < -126)",
+                                "if (E > 127) return sign | 0x7f7f;\n    if (E < -126)"),
+    "bf16_reversed_k_index": ("g_bf16_table[a[k]] * g_bf16_table[b[k]]",
+                              "g_bf16_table[a[k]] * g_bf16_table[b[K - 1 - k]]"),
 }
 
 
 def _pin_calls():
-    """Every (name, function, kwargs) of the pin module, parametrizations expanded."""
+    """Every (name, function, kwargs) of the pin modules, parametrizations expanded."""
     calls = []
-    for name, fn in inspect.getmembers(pins, inspect.isfunction):
+    for name, fn in (inspect.getmembers(pins, inspect.isfunction)
+                     + inspect.getmembers(pins_bf16, inspect.isfunction)):
         if not name.startswith("test_"):
             continue
         marks = [m for m in getattr(fn, "pytestmark", []) if m.name == "parametrize"]
