@@ -291,10 +291,12 @@ def cublas_context(A_d, B_d, steps: int, stream, flush=None):
     (reduced-precision reductions off), timed the same way as the GEMM (the same
     L2 flush between steps when one is used): context only."""
     import torch
-    prev = torch.backends.cuda.matmul.allow_fp16_reduced_precision_reduction
-    torch.backends.cuda.matmul.allow_fp16_reduced_precision_reduction = False
+    m = torch.backends.cuda.matmul
+    prev = (m.allow_fp16_reduced_precision_reduction, m.allow_bf16_reduced_precision_reduction)
+    m.allow_fp16_reduced_precision_reduction = False
+    m.allow_bf16_reduced_precision_reduction = False
     try:
-        out = torch.empty((A_d.shape[0], B_d.shape[0]), dtype=torch.float16, device=A_d.device)
+        out = torch.empty((A_d.shape[0], B_d.shape[0]), dtype=A_d.dtype, device=A_d.device)
         for _ in range(3):
             torch.matmul(A_d, B_d.t(), out=out)
         torch.cuda.synchronize()
@@ -314,7 +316,7 @@ def cublas_context(A_d, B_d, steps: int, stream, flush=None):
             return sum(a.elapsed_time(b) for a, b in evs) / 1e3 / steps
         return t0.elapsed_time(t1) / 1e3 / steps
     finally:
-        torch.backends.cuda.matmul.allow_fp16_reduced_precision_reduction = prev
+        m.allow_fp16_reduced_precision_reduction, m.allow_bf16_reduced_precision_reduction = prev
 
 
 def run_ours(args, w):
@@ -329,19 +331,27 @@ def run_ours(args, w):
     torch.cuda.set_device(device)
     dist = init_dist(world, "nccl")
 
-    A, B = inputs.operands(w)
-    Ad = torch.from_numpy(A).to(device)
-    Bd = torch.from_numpy(B).to(device)
-    Cd = torch.full((w.M, w.N), float("nan"), dtype=torch.float16, device=device)
+    bf16 = args.dtype == "bf16"
+    tdt = torch.bfloat16 if bf16 else torch.float16
+    if bf16:   # bf16 bit patterns, same distributions and seeds
+        A = inputs.draw_bf16((w.M, w.K), w.dist_a, w.seed_a)
+        B = inputs.draw_bf16((w.N, w.K), w.dist_b, w.seed_b)
+        Ad = torch.from_numpy(A.view(np.int16)).to(device).view(tdt)
+        Bd = torch.from_numpy(B.view(np.int16)).to(device).view(tdt)
+    else:
+        A, B = inputs.operands(w)
+        Ad = torch.from_numpy(A).to(device)
+        Bd = torch.from_numpy(B).to(device)
+    Cd = torch.full((w.M, w.N), float("nan"), dtype=tdt, device=device)
     stream = torch.cuda.current_stream(device)
     handle = stream.cuda_stream
     lib = g.library()
+    entry = lib.gemm_bf16_nt if bf16 else lib.gemm_f16_nt
 
     def step():
-        st = lib.gemm_f16_nt(w.M, w.N, w.K, Ad.data_ptr(), w.K, Bd.data_ptr(), w.K,
-                             Cd.data_ptr(), w.N, handle)
+        st = entry(w.M, w.N, w.K, Ad.data_ptr(), w.K, Bd.data_ptr(), w.K, Cd.data_ptr(), w.N, handle)
         if st != 0:
-            raise g.GemmError(st, "gemm_f16_nt")
+            raise g.GemmError(st, "gemm_bf16_nt" if bf16 else "gemm_f16_nt")
 
     for _ in range(args.warmup):
         step()
@@ -402,9 +412,9 @@ def run_ours(args, w):
 
     # end to end through the same C ABI from pinned host memory
     e2e_steps = max(1, min(args.steps, 10))
-    Ah = torch.from_numpy(A).pin_memory()
-    Bh = torch.from_numpy(B).pin_memory()
-    Ch = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
+    Ah = Ad.cpu().pin_memory()
+    Bh = Bd.cpu().pin_memory()
+    Ch = torch.empty((w.M, w.N), dtype=tdt).pin_memory()
 
     def e2e_step():
         Ad.copy_(Ah, non_blocking=True)
@@ -436,7 +446,7 @@ def run_ours(args, w):
                            "context only (not the target, not part of the value)"}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not bf16:
         cpu = cpu_oracle_sample(w, A, B, args.cpu_seconds)
 
     if rank == 0:
@@ -453,7 +463,8 @@ def run_ours(args, w):
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(t_max / args.steps * 1e3, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if bf16 else "f16",
             "data": "synthetic", "config": workload_config(w, flush is not None),
             "pct_of_peak": round(100.0 * achieved / peak, 2),
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
@@ -517,6 +528,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--dtype", choices=["f16", "bf16"], default="f16",
+                    help="operand/result type: f16 (the method's) or the bf16 variant")
     ap.add_argument("--workload", default="gemm_8192", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--repeat", type=int, default=1,
                     help="timed regions of K steps per process (the median is reported)")

@@ -18,7 +18,7 @@ import os
 
 from . import _build_ext
 
-__all__ = ["gemm_f16_nt", "gemm_f16_nt_ptr", "device_status", "device_limits", "plan", "tile_coord",
+__all__ = ["gemm_f16_nt", "gemm_bf16_nt", "gemm_f16_nt_ptr", "device_status", "device_limits", "plan", "tile_coord",
            "fast_divmod", "GemmError", "Options", "Plan", "library", "STATUS"]
 
 STATUS = {
@@ -87,6 +87,10 @@ def library(path: str | None = None):
         lib.gemm_f16_nt_ex.restype = ctypes.c_int
         lib.gemm_f16_nt_noalloc.argtypes = sig
         lib.gemm_f16_nt_noalloc.restype = ctypes.c_int
+        lib.gemm_bf16_nt.argtypes = sig
+        lib.gemm_bf16_nt.restype = ctypes.c_int
+        lib.gemm_bf16_nt_ex.argtypes = sig + [ctypes.POINTER(Options)]
+        lib.gemm_bf16_nt_ex.restype = ctypes.c_int
         lib.gemm_f16_nt_device_status.argtypes = [_p, ctypes.POINTER(_u32)]
         lib.gemm_f16_nt_device_status.restype = ctypes.c_int
         lib.gemm_f16_nt_status_string.argtypes = [_i32]
@@ -112,24 +116,28 @@ def _check(status: int, what: str):
 
 
 def gemm_f16_nt_ptr(M: int, N: int, K: int, a_ptr: int, lda: int, b_ptr: int, ldb: int,
-                    c_ptr: int, ldc: int, stream: int = 0, options: Options | None = None) -> None:
+                    c_ptr: int, ldc: int, stream: int = 0, options: Options | None = None,
+                    bf16: bool = False) -> None:
     """Raw call: device pointers (ints), leading dimensions in elements, a
-    cudaStream_t handle (int).  Raises GemmError on a non-OK status."""
+    cudaStream_t handle (int); bf16=True calls the bfloat16 entry points.
+    Raises GemmError on a non-OK status."""
     lib = library()
+    name = "gemm_bf16_nt" if bf16 else "gemm_f16_nt"
     if options is None:
-        st = lib.gemm_f16_nt(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, stream)
+        st = getattr(lib, name)(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, stream)
     else:
-        st = lib.gemm_f16_nt_ex(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, stream,
-                                ctypes.byref(options))
-    _check(st, "gemm_f16_nt")
+        st = getattr(lib, name + "_ex")(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, stream,
+                                        ctypes.byref(options))
+    _check(st, name)
 
 
-def _rows(t, name):
+def _rows(t, name, dtype=None):
     import torch
+    dtype = dtype or torch.float16
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.dtype != torch.float16 or t.dim() != 2:
-        raise TypeError(f"{name} must be a 2-D float16 tensor")
+    if t.dtype != dtype or t.dim() != 2:
+        raise TypeError(f"{name} must be a 2-D {dtype} tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be on a CUDA device")
     if t.shape[1] > 1 and t.stride(1) != 1:
@@ -165,6 +173,29 @@ def gemm_f16_nt(A, B, C=None, *, stream=None, options: Options | None = None):
     pc, ldc = _rows(C, "C")
     with torch.cuda.device(A.device):
         gemm_f16_nt_ptr(M, N, K, pa, lda, pb, ldb, pc, ldc, handle, options)
+    return C
+
+
+def gemm_bf16_nt(A, B, C=None, *, stream=None, options: Options | None = None):
+    """C = A @ B.T for CUDA bfloat16 tensors A [M, K] and B [N, K] (fp32
+    accumulation, bf16 result); otherwise as gemm_f16_nt."""
+    import torch
+    M, K = A.shape
+    N, K2 = B.shape
+    if K2 != K:
+        raise ValueError(f"A is [{M}, {K}] but B is [{N}, {K2}]")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    if tuple(C.shape) != (M, N):
+        raise ValueError(f"C must be [{M}, {N}]")
+    if stream is None:
+        stream = torch.cuda.current_stream(A.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    pa, lda = _rows(A, "A", torch.bfloat16)
+    pb, ldb = _rows(B, "B", torch.bfloat16)
+    pc, ldc = _rows(C, "C", torch.bfloat16)
+    with torch.cuda.device(A.device):
+        gemm_f16_nt_ptr(M, N, K, pa, lda, pb, ldb, pc, ldc, handle, options, bf16=True)
     return C
 
 

@@ -73,9 +73,10 @@ enum : uint32_t { kItemWhole = 0, kItemPartialOut = 1, kItemOwner = 2 };
 
 __device__ uint32_t g_watchdog_word;
 
-template <int CG, int BN, int STAGES, int CP = 1>
+template <int CG, int BN, int STAGES, int CP = 1, bool BF = false>
 struct KCfg {
     static constexpr int kCG = CG;
+    static constexpr bool kBF = BF;                  // bf16 operands and result instead of fp16
     static constexpr int kCP = CP;                   // CTA pairs per cluster (A shared by multicast)
     static constexpr int kCtas = CG * CP;            // CTAs per cluster
     static constexpr int kBN = BN;                   // columns of C per tile
@@ -92,10 +93,10 @@ struct KCfg {
     static constexpr int kCtlBytes = 256;
     static constexpr int kSmemBytes = 1024 + kRingBytes + kOutBytes + kCtlBytes;
     // tcgen05 instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B
-    // fp16 (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N>>3 at bit 17,
-    // M>>4 at bit 24.
-    static constexpr uint32_t kIdesc =
-        (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t(kTileM >> 4) << 24);
+    // fp16 (bits 7-9, 10-12 = 0) or bf16 (= 1), both K-major (bits 15, 16 = 0),
+    // N>>3 at bit 17, M>>4 at bit 24.
+    static constexpr uint32_t kIdesc = (1u << 4) | (uint32_t(BF) << 7) | (uint32_t(BF) << 10) |
+                                       (uint32_t(BN >> 3) << 17) | (uint32_t(kTileM >> 4) << 24);
 
     static_assert(2 * BN <= 512, "two accumulator buffers must fit in the 512 TMEM columns");
     static_assert(BN % kEpiCols == 0, "epilogue works in 64-column chunks");
@@ -596,9 +597,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                 }
                 uint32_t h[32];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) h[j] = ptx::pack_f16x2_rn(lo[2 * j], lo[2 * j + 1]);
+                for (int j = 0; j < 16; ++j)
+                    h[j] = Cfg::kBF ? ptx::pack_bf16x2_rn(lo[2 * j], lo[2 * j + 1])
+                                    : ptx::pack_f16x2_rn(lo[2 * j], lo[2 * j + 1]);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) h[16 + j] = ptx::pack_f16x2_rn(hi[2 * j], hi[2 * j + 1]);
+                for (int j = 0; j < 16; ++j)
+                    h[16 + j] = Cfg::kBF ? ptx::pack_bf16x2_rn(hi[2 * j], hi[2 * j + 1])
+                                         : ptx::pack_f16x2_rn(hi[2 * j], hi[2 * j + 1]);
 
                 // The staging buffer about to be written was last read by the
                 // store issued two chunks ago.
@@ -671,6 +676,15 @@ __global__ void zero_fill_kernel(uint16_t* C, int64_t M, int64_t N, int64_t ldc)
 using Cfg2 = KCfg<2, 256, 6>;      // CTA pair, 256×256 tile, 6-stage ring
 using Cfg2x2 = KCfg<2, 256, 6, 2>; // two CTA pairs per cluster sharing A: 256×512 cluster tile
 using Cfg1 = KCfg<1, 256, 4>;      // single CTA, 128×256 tile, 4-stage ring
+using Cfg2Bf = KCfg<2, 256, 6, 1, true>;    // the same three with bf16 operands and result
+using Cfg2x2Bf = KCfg<2, 256, 6, 2, true>;
+using Cfg1Bf = KCfg<1, 256, 4, 1, true>;
+
+template <class Cfg>
+bool allow_smem() {
+    return cudaFuncSetAttribute(gemm_f16_nt_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg::kSmemBytes) == cudaSuccess;
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -719,12 +733,8 @@ gemm_status_t setup_device(int dev, DeviceState& st) {
         }
         g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
-    if (cudaFuncSetAttribute(gemm_f16_nt_kernel<Cfg2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg2::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(gemm_f16_nt_kernel<Cfg2x2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg2x2::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(gemm_f16_nt_kernel<Cfg1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg1::kSmemBytes) != cudaSuccess) {
+    if (!allow_smem<Cfg2>() || !allow_smem<Cfg2x2>() || !allow_smem<Cfg1>() ||
+        !allow_smem<Cfg2Bf>() || !allow_smem<Cfg2x2Bf>() || !allow_smem<Cfg1Bf>()) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
@@ -934,13 +944,13 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
     return GEMM_OK;
 }
 
-gemm_status_t encode_2d(CUtensorMap* tm, const void* ptr, uint64_t inner, uint64_t outer,
-                        uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer) {
+gemm_status_t encode_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* ptr, uint64_t inner,
+                        uint64_t outer, uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer) {
     const cuuint64_t dims[2] = {inner, outer};
     const cuuint64_t strides[1] = {pitch_elems * 2};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+    CUresult r = g_encode(tm, dtype, 2, const_cast<void*>(ptr), dims, strides,
                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_LAUNCH;
@@ -958,9 +968,10 @@ gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t
     // C covers only the first N8 = N - N % 8 columns; the kernel writes the rest
     // with plain stores and no byte past column N-1 is ever written.
     const int64_t N8 = N & ~int64_t(7);
-    if ((s = encode_2d(&p.tmA, A, uint64_t(K), uint64_t(M), uint64_t(lda), kBlockK, kBlockM / Cfg::kCP)) != GEMM_OK ||
-        (s = encode_2d(&p.tmB, B, uint64_t(K), uint64_t(N), uint64_t(ldb), kBlockK, Cfg::kBRows)) != GEMM_OK ||
-        (N8 > 0 && (s = encode_2d(&p.tmC, C, uint64_t(N8), uint64_t(M), uint64_t(ldc), kEpiCols, 32)) != GEMM_OK))
+    const CUtensorMapDataType dt = Cfg::kBF ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if ((s = encode_2d(&p.tmA, dt, A, uint64_t(K), uint64_t(M), uint64_t(lda), kBlockK, kBlockM / Cfg::kCP)) != GEMM_OK ||
+        (s = encode_2d(&p.tmB, dt, B, uint64_t(K), uint64_t(N), uint64_t(ldb), kBlockK, Cfg::kBRows)) != GEMM_OK ||
+        (N8 > 0 && (s = encode_2d(&p.tmC, dt, C, uint64_t(N8), uint64_t(M), uint64_t(ldc), kEpiCols, 32)) != GEMM_OK))
         return s;
     p.N8 = int32_t(N8);
     p.C = C;
@@ -1008,7 +1019,8 @@ gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t
 }
 
 gemm_status_t run(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B,
-                  int64_t ldb, uint16_t* C, int64_t ldc, void* stream_v, const gemm_f16_nt_options_t* o) {
+                  int64_t ldb, uint16_t* C, int64_t ldc, void* stream_v, const gemm_f16_nt_options_t* o,
+                  bool bf16 = false) {
     gemm_status_t s = check_args(M, N, K, A, lda, B, ldb, C, ldc);
     if (s != GEMM_OK) return s;
     if (o && ((o->cta_group != 0 && o->cta_group != 1 && o->cta_group != 2) || o->swizzle < 0 ||
@@ -1045,9 +1057,15 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t ld
             if ((s = make_plan(M, N, K, st->sms, resident, &dp, &pl)) != GEMM_OK) return s;
         }
     }
-    if (cg == 1) s = launch<Cfg1>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
-    else if (cp == 2) s = launch<Cfg2x2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
-    else s = launch<Cfg2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
+    if (bf16) {
+        if (cg == 1) s = launch<Cfg1Bf>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
+        else if (cp == 2) s = launch<Cfg2x2Bf>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
+        else s = launch<Cfg2Bf>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
+    } else {
+        if (cg == 1) s = launch<Cfg1>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
+        else if (cp == 2) s = launch<Cfg2x2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
+        else s = launch<Cfg2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
+    }
     if (ws && cudaFreeAsync(ws, stream) != cudaSuccess) {
         cudaGetLastError();
         if (s == GEMM_OK) s = GEMM_ERR_LAUNCH;
@@ -1147,6 +1165,18 @@ G16_EXPORT gemm_status_t gemm_f16_nt_ex(int64_t M, int64_t N, int64_t K, const u
                                         const uint16_t* B, int64_t ldb, uint16_t* C, int64_t ldc,
                                         void* stream, const gemm_f16_nt_options_t* opts) {
     return g16::run(M, N, K, A, lda, B, ldb, C, ldc, stream, opts);
+}
+
+G16_EXPORT gemm_status_t gemm_bf16_nt(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
+                                      const uint16_t* B, int64_t ldb, uint16_t* C, int64_t ldc,
+                                      void* stream) {
+    return g16::run(M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr, true);
+}
+
+G16_EXPORT gemm_status_t gemm_bf16_nt_ex(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
+                                         const uint16_t* B, int64_t ldb, uint16_t* C, int64_t ldc,
+                                         void* stream, const gemm_f16_nt_options_t* opts) {
+    return g16::run(M, N, K, A, lda, B, ldb, C, ldc, stream, opts, true);
 }
 
 G16_EXPORT gemm_status_t gemm_f16_nt_device_status(void* stream, uint32_t* flags) {

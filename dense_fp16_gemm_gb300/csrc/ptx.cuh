@@ -272,6 +272,13 @@ __device__ __forceinline__ uint32_t pack_f16x2_rn(uint32_t lo_f32, uint32_t hi_f
         "f"(__uint_as_float(lo_f32)));
     return d;
 }
+// Two fp32 -> packed bf16x2, round to nearest even; `lo` lands in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(uint32_t lo_f32, uint32_t hi_f32) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(__uint_as_float(hi_f32)),
+        "f"(__uint_as_float(lo_f32)));
+    return d;
+}
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"

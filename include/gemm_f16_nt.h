@@ -199,6 +199,30 @@ gemm_status_t gemm_f16_nt_ex(int64_t M, int64_t N, int64_t K,
                              void *stream, const gemm_f16_nt_options_t *opts);
 
 /*
+ * gemm_bf16_nt, gemm_bf16_nt_ex — the same product with bfloat16 operands and
+ * result: C[M,N] = A[M,K] · B[N,K]ᵀ, bf16 in, fp32 accumulation, bf16 out.
+ *
+ * The tutorial pages compute in fp16 only; bf16 is this library's variant of
+ * the same method (same kernel, schedule and options; the tensor cores read
+ * bf16 operands and the epilogue rounds the fp32 accumulator to the nearest
+ * bf16, ties to even).  A, B and C hold bf16 bit patterns (1 sign, 8 exponent,
+ * 7 fraction bits).  Arguments, layout, alignment, ownership, options and
+ * errors are those of gemm_f16_nt / gemm_f16_nt_ex.  Results agree with an
+ * fp64 reference rounded once to bf16 within 2 bf16 ulps + 1e-4·sqrt(K), and
+ * exactly when every partial sum is an fp32-exact integer.
+ */
+gemm_status_t gemm_bf16_nt(int64_t M, int64_t N, int64_t K,
+                           const uint16_t *A, int64_t lda,
+                           const uint16_t *B, int64_t ldb,
+                           uint16_t *C, int64_t ldc,
+                           void *stream);
+gemm_status_t gemm_bf16_nt_ex(int64_t M, int64_t N, int64_t K,
+                              const uint16_t *A, int64_t lda,
+                              const uint16_t *B, int64_t ldb,
+                              uint16_t *C, int64_t ldc,
+                              void *stream, const gemm_f16_nt_options_t *opts);
+
+/*
  * gemm_f16_nt_device_status — read and clear the current device's watchdog word.
  *
  * Synchronises `stream`, copies the word into *flags (may be NULL) and resets

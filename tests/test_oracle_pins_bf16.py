@@ -21,7 +21,8 @@ _ALL = np.arange(65536, dtype=np.uint32)
 
 def _grid():
     """All finite bf16 values (from numpy's float32 view), sorted, -0 dropped."""
-    v = (_ALL << 16).astype(np.uint32).view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):
+        v = (_ALL << 16).astype(np.uint32).view(np.float32).astype(np.float64)
     ok = np.isfinite(v) & (_ALL != 0x8000)
     vals, bits = v[ok], _ALL[ok].astype(np.uint16)
     order = np.argsort(vals, kind="stable")

@@ -19,8 +19,25 @@ def ulp16(x) -> np.ndarray:
     return np.ldexp(1.0, e - 10)
 
 
-def check_close(c_gpu, c_ref, K: int, where: str = ""):
-    """Assert the per-element tolerance; returns the worst ratio err/bound."""
+def ulp_bf16(x) -> np.ndarray:
+    """Spacing of the bfloat16 grid at |x| (7 fraction bits, normal from 2^-126)."""
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    _, e2 = np.frexp(a)
+    e = np.where(a > 0, np.maximum(e2.astype(np.int64) - 1, -126), -126)
+    return np.ldexp(1.0, e - 7)
+
+
+def bf16_to_f64(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float64, through numpy's float32 view."""
+    b = np.asarray(bits).view(np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def check_close(c_gpu, c_ref, K: int, where: str = "", ulp=None):
+    """Assert the per-element tolerance (2 ulps of the output format + 1e-4
+    sqrt(K)); returns the worst ratio err/bound.  Arrays may be fp16 values or
+    float64 values of another format with its `ulp` function."""
+    ulp = ulp or ulp16
     g = np.asarray(c_gpu).astype(np.float64)
     r = np.asarray(c_ref).astype(np.float64)
     assert g.shape == r.shape, (g.shape, r.shape)
@@ -30,7 +47,7 @@ def check_close(c_gpu, c_ref, K: int, where: str = ""):
         assert np.array_equal(g[inf_ref], r[inf_ref]), f"{where}: inf mismatch"
     fin = ~inf_ref
     assert not np.isinf(g[fin]).any(), f"{where}: GPU inf where the reference is finite"
-    bound = 2.0 * ulp16(r[fin]) + 1e-4 * np.sqrt(max(K, 1))
+    bound = 2.0 * ulp(r[fin]) + 1e-4 * np.sqrt(max(K, 1))
     err = np.abs(g[fin] - r[fin])
     ratio = err / bound
     if ratio.size and ratio.max() > 1.0:
