@@ -46,7 +46,8 @@ class Options(ctypes.Structure):
                 ("max_clusters", ctypes.c_int32), ("inject_stall", ctypes.c_int32),
                 ("timeout_ns", ctypes.c_uint64), ("schedule", ctypes.c_int32),
                 ("trace_items", ctypes.c_int32), ("trace", ctypes.c_void_p),
-                ("cluster_pairs", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("cluster_pairs", ctypes.c_int32), ("a_layout", ctypes.c_int32),
+                ("b_layout", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class Plan(ctypes.Structure):
@@ -150,53 +151,48 @@ def _rows(t, name, dtype=None):
     return t.data_ptr(), ld
 
 
-def gemm_f16_nt(A, B, C=None, *, stream=None, options: Options | None = None):
-    """C = A @ B.T for CUDA float16 tensors A [M, K] and B [N, K].
+def _call(A, B, C, stream, options, a_layout, b_layout, bf16):
+    import torch
+    dt = torch.bfloat16 if bf16 else torch.float16
+    M, K = (A.shape[1], A.shape[0]) if a_layout else tuple(A.shape)
+    N, K2 = (B.shape[1], B.shape[0]) if b_layout else tuple(B.shape)
+    if K2 != K:
+        raise ValueError(f"A and B disagree on K ({K} vs {K2})")
+    if C is None:   # row pitch rounded up to 8 elements (16 bytes), as the kernel needs
+        C = torch.empty((M, N + (-N) % 8), dtype=dt, device=A.device)[:, :N]
+    if tuple(C.shape) != (M, N):
+        raise ValueError(f"C must be [{M}, {N}]")
+    if stream is None:
+        stream = torch.cuda.current_stream(A.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    if a_layout or b_layout:
+        options = options if options is not None else Options()
+        options.a_layout, options.b_layout = a_layout, b_layout
+    pa, lda = _rows(A, "A", dt)
+    pb, ldb = _rows(B, "B", dt)
+    pc, ldc = _rows(C, "C", dt)
+    with torch.cuda.device(A.device):
+        gemm_f16_nt_ptr(M, N, K, pa, lda, pb, ldb, pc, ldc, handle, options, bf16=bf16)
+    return C
 
-    C, if given, is an [M, N] float16 view (its row stride may exceed N) and is
-    overwritten; otherwise a new contiguous tensor is returned.  The call is
+
+def gemm_f16_nt(A, B, C=None, *, stream=None, options: Options | None = None,
+                a_layout: int = 0, b_layout: int = 0):
+    """C[m, n] = sum_k A(m, k) B(n, k) for CUDA float16 tensors.
+
+    A is [M, K] (a_layout 0) or [K, M] (a_layout 1); B is [N, K] (b_layout 0)
+    or [K, N] (b_layout 1) — with b_layout 1 this is C = A @ B.  C, if given,
+    is an [M, N] float16 view (its row stride may exceed N) and is
+    overwritten; otherwise a new [M, N] view of a buffer whose row pitch is N
+    rounded up to a multiple of 8 is returned.  The call is
     asynchronous on `stream` (default: torch's current stream)."""
-    import torch
-    M, K = A.shape
-    N, K2 = B.shape
-    if K2 != K:
-        raise ValueError(f"A is [{M}, {K}] but B is [{N}, {K2}]")
-    if C is None:
-        C = torch.empty((M, N), dtype=torch.float16, device=A.device)
-    if tuple(C.shape) != (M, N):
-        raise ValueError(f"C must be [{M}, {N}]")
-    if stream is None:
-        stream = torch.cuda.current_stream(A.device)
-    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    pa, lda = _rows(A, "A")
-    pb, ldb = _rows(B, "B")
-    pc, ldc = _rows(C, "C")
-    with torch.cuda.device(A.device):
-        gemm_f16_nt_ptr(M, N, K, pa, lda, pb, ldb, pc, ldc, handle, options)
-    return C
+    return _call(A, B, C, stream, options, a_layout, b_layout, False)
 
 
-def gemm_bf16_nt(A, B, C=None, *, stream=None, options: Options | None = None):
-    """C = A @ B.T for CUDA bfloat16 tensors A [M, K] and B [N, K] (fp32
-    accumulation, bf16 result); otherwise as gemm_f16_nt."""
-    import torch
-    M, K = A.shape
-    N, K2 = B.shape
-    if K2 != K:
-        raise ValueError(f"A is [{M}, {K}] but B is [{N}, {K2}]")
-    if C is None:
-        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
-    if tuple(C.shape) != (M, N):
-        raise ValueError(f"C must be [{M}, {N}]")
-    if stream is None:
-        stream = torch.cuda.current_stream(A.device)
-    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    pa, lda = _rows(A, "A", torch.bfloat16)
-    pb, ldb = _rows(B, "B", torch.bfloat16)
-    pc, ldc = _rows(C, "C", torch.bfloat16)
-    with torch.cuda.device(A.device):
-        gemm_f16_nt_ptr(M, N, K, pa, lda, pb, ldb, pc, ldc, handle, options, bf16=True)
-    return C
+def gemm_bf16_nt(A, B, C=None, *, stream=None, options: Options | None = None,
+                 a_layout: int = 0, b_layout: int = 0):
+    """As gemm_f16_nt for CUDA bfloat16 tensors (fp32 accumulation, bf16 result)."""
+    return _call(A, B, C, stream, options, a_layout, b_layout, True)
 
 
 def device_status(stream=None) -> int:

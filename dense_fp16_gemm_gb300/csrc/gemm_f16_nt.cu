@@ -131,6 +131,8 @@ struct Params {
     uint64_t timeout_ns;
     uint32_t* watchdog;
     int32_t inject_stall;
+    uint32_t a_mn;     // 1: A stored [K, M] (M contiguous) — MN-major in shared memory
+    uint32_t b_mn;     // 1: B stored [K, N] (N contiguous)
     // stream-K part of the schedule (0 tiles = purely data-parallel)
     uint32_t sk_tiles;     // tiles [0, sk_tiles) are cut into k-block units
     uint64_t sk_units;     // sk_tiles * num_kb
@@ -210,6 +212,18 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
     return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
            (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+// The same for an MN-major tile (M or N contiguous): TMA writes it as 64×64
+// boxes, each 64 K-rows of 128 bytes (64 consecutive M/N elements), swizzled in
+// 8-row (1024-byte) atoms; the boxes for successive 64-element M/N blocks follow
+// each other every 8 KiB.  Leading-byte offset = that 8 KiB step between atoms
+// along M/N, stride-byte offset = 1024 bytes between 8-row groups along K.
+// Advancing K by 16 moves 16 rows: 2048 bytes.
+constexpr uint32_t kMnBoxBytes = 64 * 64 * 2;
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr) {
+    return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(kMnBoxBytes >> 4) << 16) |
+           (uint64_t(1024 >> 4) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
 }
 
 // ---------------------------------------------------------------------------
@@ -390,19 +404,40 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                     if (prank == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * stage, Cfg::kTxBytes);
                     const int32_t k0 = int32_t(kb * kBlockK);
                     const uint32_t bar = full_tgt + 8 * stage;
+                    // A K-major operand is one box {64 k, rows}; an MN-major one is
+                    // rows/64 boxes {64 m|n, 64 k}, 8 KiB apart, at coordinates (m|n, k).
+                    const uint32_t a_dst = sA + stage * Cfg::kABytes;
+                    const uint32_t b_dst = sB + stage * Cfg::kBBytes;
                     if constexpr (CP == 2) {
                         // Both pairs need the same A rows: this CTA loads half of them
                         // into the same-rank CTA of both pairs (TMA multicast).
-                        ptx::tma_load_2d_pair_mcast(sA + stage * Cfg::kABytes + pair * (Cfg::kABytes / 2),
-                                                    &p.tmA, k0, m0 + int32_t(pair * (kBlockM / 2)), bar,
-                                                    uint16_t((1u << prank) | (1u << (prank + 2u))));
-                        ptx::tma_load_2d_pair_hint(sB + stage * Cfg::kBBytes, &p.tmB, k0, n0, bar, keep_b);
-                    } else if constexpr (CG == 2) {
-                        ptx::tma_load_2d_pair(sA + stage * Cfg::kABytes, &p.tmA, k0, m0, bar);
-                        ptx::tma_load_2d_pair_hint(sB + stage * Cfg::kBBytes, &p.tmB, k0, n0, bar, keep_b);
+                        const int32_t r0 = m0 + int32_t(pair * (kBlockM / 2));
+                        const uint16_t mask = uint16_t((1u << prank) | (1u << (prank + 2u)));
+                        if (p.a_mn)
+                            ptx::tma_load_2d_pair_mcast(a_dst + pair * kMnBoxBytes, &p.tmA, r0, k0, bar, mask);
+                        else
+                            ptx::tma_load_2d_pair_mcast(a_dst + pair * (Cfg::kABytes / 2), &p.tmA, k0, r0, bar, mask);
+                    } else if (p.a_mn) {
+                        for (int j = 0; j < kBlockM / 64; ++j) {
+                            if constexpr (CG == 2)
+                                ptx::tma_load_2d_pair(a_dst + j * kMnBoxBytes, &p.tmA, m0 + 64 * j, k0, bar);
+                            else
+                                ptx::tma_load_2d(a_dst + j * kMnBoxBytes, &p.tmA, m0 + 64 * j, k0, bar);
+                        }
                     } else {
-                        ptx::tma_load_2d(sA + stage * Cfg::kABytes, &p.tmA, k0, m0, bar);
-                        ptx::tma_load_2d_hint(sB + stage * Cfg::kBBytes, &p.tmB, k0, n0, bar, keep_b);
+                        if constexpr (CG == 2) ptx::tma_load_2d_pair(a_dst, &p.tmA, k0, m0, bar);
+                        else ptx::tma_load_2d(a_dst, &p.tmA, k0, m0, bar);
+                    }
+                    if (p.b_mn) {
+                        for (int j = 0; j < Cfg::kBRows / 64; ++j) {
+                            if constexpr (CG == 2)
+                                ptx::tma_load_2d_pair_hint(b_dst + j * kMnBoxBytes, &p.tmB, n0 + 64 * j, k0, bar, keep_b);
+                            else
+                                ptx::tma_load_2d_hint(b_dst + j * kMnBoxBytes, &p.tmB, n0 + 64 * j, k0, bar, keep_b);
+                        }
+                    } else {
+                        if constexpr (CG == 2) ptx::tma_load_2d_pair_hint(b_dst, &p.tmB, k0, n0, bar, keep_b);
+                        else ptx::tma_load_2d_hint(b_dst, &p.tmB, k0, n0, bar, keep_b);
                     }
                     ++issued;
                     if (++stage == uint32_t(S)) {
@@ -437,6 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
         if (lane == 0 && prank == 0) {
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
+            // bits 15 / 16: A / B MN-major ("transposed") in shared memory
+            const uint32_t idesc = Cfg::kIdesc | (p.a_mn << 15) | (p.b_mn << 16);
             Work work;
             Item it;
             work_init(work, p, cluster, nclusters);
@@ -464,12 +501,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                     }
                     if (!ok) break;
                     ptx::tc_fence_after();
-                    const uint64_t ad = sdesc_sw128(sA + stage * Cfg::kABytes);
-                    const uint64_t bd = sdesc_sw128(sB + stage * Cfg::kBBytes);
+                    const uint64_t ad = p.a_mn ? sdesc_sw128_mn(sA + stage * Cfg::kABytes)
+                                               : sdesc_sw128(sA + stage * Cfg::kABytes);
+                    const uint64_t bd = p.b_mn ? sdesc_sw128_mn(sB + stage * Cfg::kBBytes)
+                                               : sdesc_sw128(sB + stage * Cfg::kBBytes);
+                    // per 16-k step: 32 bytes along a K-major row, 16 rows (2048 bytes) MN-major
+                    const uint64_t astep = p.a_mn ? (kUmmaK * 128) >> 4 : (kUmmaK * 2) >> 4;
+                    const uint64_t bstep = p.b_mn ? (kUmmaK * 128) >> 4 : (kUmmaK * 2) >> 4;
 #pragma unroll
                     for (int k = 0; k < kBlockK / kUmmaK; ++k) {
-                        const uint64_t koff = uint64_t((k * kUmmaK * 2) >> 4);
-                        ptx::mma_f16<CG>(d, ad + koff, bd + koff, Cfg::kIdesc,
+                        ptx::mma_f16<CG>(d, ad + astep * k, bd + bstep * k, idesc,
                                          (kb != it.kb0 || k != 0) ? 1u : 0u);
                     }
                     // Free this ring slot in every CTA of the pair once these MMAs retire.
@@ -825,14 +866,17 @@ gemm_status_t device_state(DeviceState** out, int* dev_out, bool with_pool) {
 gemm_status_t current_device(DeviceState** out) { return device_state(out, nullptr, true); }
 
 gemm_status_t check_args(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
-                         const uint16_t* B, int64_t ldb, const uint16_t* C, int64_t ldc) {
+                         const uint16_t* B, int64_t ldb, const uint16_t* C, int64_t ldc,
+                         bool a_mn = false, bool b_mn = false) {
     const int64_t lim = int64_t(1) << 31;
     if (M < 0 || N < 0 || K < 0 || M >= lim || N >= lim || K >= lim) return GEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return GEMM_OK;
     const int64_t ld_lim = int64_t(1) << 39;   // TMA strides stay below 2^40 bytes
     if (!C || ldc < N || ldc >= ld_lim) return GEMM_ERR_INVALID_VALUE;
     if (K > 0) {
-        if (!A || !B || lda < K || ldb < K || lda >= ld_lim || ldb >= ld_lim) return GEMM_ERR_INVALID_VALUE;
+        // a row of A holds K elements ([M, K]) or M ([K, M]); likewise B
+        if (!A || !B || lda < (a_mn ? M : K) || ldb < (b_mn ? N : K) || lda >= ld_lim || ldb >= ld_lim)
+            return GEMM_ERR_INVALID_VALUE;
         if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15) ||
             (lda & 7) || (ldb & 7))
             return GEMM_ERR_MISALIGNED;
@@ -969,8 +1013,13 @@ gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t
     // with plain stores and no byte past column N-1 is ever written.
     const int64_t N8 = N & ~int64_t(7);
     const CUtensorMapDataType dt = Cfg::kBF ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    if ((s = encode_2d(&p.tmA, dt, A, uint64_t(K), uint64_t(M), uint64_t(lda), kBlockK, kBlockM / Cfg::kCP)) != GEMM_OK ||
-        (s = encode_2d(&p.tmB, dt, B, uint64_t(K), uint64_t(N), uint64_t(ldb), kBlockK, Cfg::kBRows)) != GEMM_OK ||
+    const bool a_mn = o && o->a_layout == 1, b_mn = o && o->b_layout == 1;
+    if ((s = a_mn ? encode_2d(&p.tmA, dt, A, uint64_t(M), uint64_t(K), uint64_t(lda), 64, 64)
+                  : encode_2d(&p.tmA, dt, A, uint64_t(K), uint64_t(M), uint64_t(lda), kBlockK,
+                              kBlockM / Cfg::kCP)) != GEMM_OK ||
+        (s = b_mn ? encode_2d(&p.tmB, dt, B, uint64_t(N), uint64_t(K), uint64_t(ldb), 64, 64)
+                  : encode_2d(&p.tmB, dt, B, uint64_t(K), uint64_t(N), uint64_t(ldb), kBlockK,
+                              Cfg::kBRows)) != GEMM_OK ||
         (N8 > 0 && (s = encode_2d(&p.tmC, dt, C, uint64_t(N8), uint64_t(M), uint64_t(ldc), kEpiCols, 32)) != GEMM_OK))
         return s;
     p.N8 = int32_t(N8);
@@ -984,6 +1033,8 @@ gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t
     p.timeout_ns = (o && o->timeout_ns) ? o->timeout_ns : kDefaultTimeoutNs;
     p.watchdog = watchdog;
     p.inject_stall = o ? o->inject_stall : 0;
+    p.a_mn = a_mn ? 1u : 0u;
+    p.b_mn = b_mn ? 1u : 0u;
     p.sk_tiles = uint32_t(pl.sk_tiles);
     p.sk_units = uint64_t(pl.sk_tiles) * uint64_t(pl.k_blocks);
     if (pl.sk_tiles > 0) {
@@ -1021,7 +1072,9 @@ gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t
 gemm_status_t run(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B,
                   int64_t ldb, uint16_t* C, int64_t ldc, void* stream_v, const gemm_f16_nt_options_t* o,
                   bool bf16 = false) {
-    gemm_status_t s = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+    if (o && (o->a_layout < 0 || o->a_layout > 1 || o->b_layout < 0 || o->b_layout > 1 || o->reserved != 0))
+        return GEMM_ERR_INVALID_VALUE;
+    gemm_status_t s = check_args(M, N, K, A, lda, B, ldb, C, ldc, o && o->a_layout == 1, o && o->b_layout == 1);
     if (s != GEMM_OK) return s;
     if (o && ((o->cta_group != 0 && o->cta_group != 1 && o->cta_group != 2) || o->swizzle < 0 ||
               o->swizzle > 64 || o->max_clusters < 0 || o->schedule < 0 || o->schedule > 2 ||

@@ -175,6 +175,16 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  *                 lda or ldb is not a multiple of 64 elements (128 bytes: each
  *                 128-byte row slice of a tile then spans two L2 lines and L2
  *                 traffic is the limit) and N > 256, else 1.
+ *   a_layout      0 (default): A is stored [M, K], element (m, k) at
+ *                 A[m*lda + k]; 1: A is stored [K, M] (M contiguous), element
+ *                 (m, k) at A[k*lda + m], lda >= M.
+ *   b_layout      0 (default): B is stored [N, K], element (n, k) at
+ *                 B[n*ldb + k]; 1: B is stored [K, N], element (n, k) at
+ *                 B[k*ldb + n], ldb >= N.
+ *                 The product is always C[M,N] = Σ_k A(m,k)·B(n,k) with C
+ *                 row-major: layouts (0,1) give C = A·B for a row-major [K, N]
+ *                 B, (1,0) give C = Aᵀ·Bᵀ-style transposed storage, etc.  The
+ *                 tensor cores read M/N-contiguous tiles as MN-major operands.
  */
 typedef struct {
     int32_t cta_group;
@@ -186,6 +196,8 @@ typedef struct {
     int32_t trace_items;
     uint64_t *trace;
     int32_t cluster_pairs;
+    int32_t a_layout;
+    int32_t b_layout;
     int32_t reserved;     /* must be 0 */
 } gemm_f16_nt_options_t;
 

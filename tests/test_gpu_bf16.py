@@ -99,3 +99,16 @@ def test_8192_sampled():
     cols = np.concatenate([rng.integers(0, N, 2000), [0, 0, N - 1, N - 1]])
     ref = oracle.gemm_bf16_nt_points(A, B, rows, cols)
     check_close(bf16_to_f64(C[rows, cols]), bf16_to_f64(ref), K, "bf16 8192 sampled", ulp=ulp_bf16)
+
+
+@pytest.mark.parametrize("a_layout,b_layout", [(0, 1), (1, 1)])
+def test_bf16_operand_layouts(a_layout, b_layout):
+    M, N, K = 600, 700, 520
+    A = inputs.draw_bf16((M, K), inputs.U, 411)
+    B = inputs.draw_bf16((N, K), inputs.U, 412)
+    A_st = np.ascontiguousarray(A.T) if a_layout else A
+    B_st = np.ascontiguousarray(B.T) if b_layout else B
+    C = g.gemm_bf16_nt(dev_bf16(A_st), dev_bf16(B_st), a_layout=a_layout, b_layout=b_layout)
+    torch.cuda.synchronize()
+    check_close(bf16_to_f64(host_bits(C)), bf16_to_f64(oracle.gemm_bf16_nt(A, B)), K,
+                f"bf16 layout A{a_layout} B{b_layout}", ulp=ulp_bf16)

@@ -259,3 +259,56 @@ def test_workload_sampled(name):
     rows, cols = sample_points(w.M, w.N)
     ref, _ = oracle.gemm_f16_nt_points(A, B, rows, cols)
     check_close(C[rows, cols], ref, w.K, name)
+
+
+# ---------------------------------------------------------------------------
+# operand layouts: A stored [K, M] and/or B stored [K, N] (MN-major tiles)
+# ---------------------------------------------------------------------------
+
+def run_layout(A_mk, B_nk, a_layout, b_layout, options, bf16=False):
+    """Store A / B in the requested layout (padded pitch), run, return C."""
+    M, K = A_mk.shape
+    N = B_nk.shape[0]
+    A_st = np.ascontiguousarray(A_mk.T) if a_layout else A_mk
+    B_st = np.ascontiguousarray(B_nk.T) if b_layout else B_nk
+    lda = A_st.shape[1] + 8 + (-A_st.shape[1]) % 8
+    ldb = B_st.shape[1] + 16 + (-B_st.shape[1]) % 8
+    Ad, Bd = to_device(A_st, lda), to_device(B_st, ldb)
+    Cd, Cbuf = empty_out(M, N, extra_rows=2)
+    options.a_layout, options.b_layout = a_layout, b_layout
+    g.gemm_f16_nt_ptr(M, N, K, Ad.data_ptr(), lda, Bd.data_ptr(), ldb, Cd.data_ptr(), Cbuf.stride(0),
+                      torch.cuda.current_stream().cuda_stream, options)
+    torch.cuda.synchronize()
+    assert np.isnan(to_host(Cbuf)[M:].astype(np.float32)).all(), "rows past M were written"
+    return to_host(Cd)
+
+
+@pytest.mark.parametrize("a_layout,b_layout", [(0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("cg,cp", [(2, 1), (1, 1), (2, 2)])
+@pytest.mark.parametrize("M,N,K", [(300, 520, 328), (1000, 1100, 700)])
+def test_operand_layouts(M, N, K, cg, cp, a_layout, b_layout):
+    A = inputs.draw((M, K), inputs.U, 501 + M)
+    B = inputs.draw((N, K), inputs.U, 502 + N)
+    C = run_layout(A, B, a_layout, b_layout, g.Options(cta_group=cg, cluster_pairs=cp))
+    check_close(C, oracle.gemm_f16_nt(A, B), K, f"layout A{a_layout} B{b_layout} cg{cg} cp{cp}")
+
+
+def test_operand_layouts_stream_k_and_integers():
+    M, N, K = 700, 900, 3000
+    A = inputs.draw((M, K), inputs.I2, 503)
+    B = inputs.draw((N, K), inputs.I2, 504)
+    ref = oracle.gemm_f16_nt(A, B)
+    for al, bl in ((0, 1), (1, 0), (1, 1)):
+        check_bitexact(run_layout(A, B, al, bl, g.Options(schedule=2, max_clusters=5)), ref,
+                       f"layout A{al} B{bl} stream-K int")
+
+
+def test_layout_pitch_rule():
+    # a [K, M] A needs lda >= M, not lda >= K
+    A = torch.zeros((64, 256), dtype=torch.float16, device="cuda:0")      # K=64 rows of M=256
+    B = torch.zeros((512, 64), dtype=torch.float16, device="cuda:0")
+    C = torch.empty((256, 512), dtype=torch.float16, device="cuda:0")
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_f16_nt_ptr(256, 512, 64, A.data_ptr(), 128, B.data_ptr(), 64, C.data_ptr(), 512, 0,
+                          g.Options(a_layout=1))
+    assert e.value.status == 1

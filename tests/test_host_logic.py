@@ -215,6 +215,15 @@ def test_argument_validation(args, code):
     assert call(**args) == code
 
 
+def test_layout_pitches_validated():
+    # A stored [K, M]: lda counts M; B stored [K, N]: ldb counts N
+    assert call(64, 32, 16, lda=32, ldb=16, opts=g.Options(a_layout=1)) == 1     # lda < M
+    assert call(16, 64, 40, lda=40, ldb=32, opts=g.Options(b_layout=1)) == 1     # ldb < N
+    assert call(16, 64, 36, lda=36, ldb=64, ldc=64, opts=g.Options(b_layout=1)) == 2     # lda % 8 != 0
+    assert call(8, 8, 16, opts=g.Options(a_layout=2)) == 1
+    assert call(8, 8, 16, opts=g.Options(reserved=1)) == 1
+
+
 def test_bad_options_rejected():
     assert call(8, 8, 16, opts=g.Options(cta_group=4)) == 1
     assert call(8, 8, 16, opts=g.Options(swizzle=-1)) == 1
