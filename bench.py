@@ -7,6 +7,9 @@ measures in every version; inputs uniform in [-1, 1], rounded to fp16, seeded).
 The timed region holds only that kernel, back to back on one stream, with the
 operands resident in HBM; A, B and C together (384 MiB at 8192³) are larger
 than the 129 MB L2, so no step finds its operands in L2 from the step before.
+Each launch may start its set-up while the one before drains (programmatic
+dependent launch), as in any chain of GEMMs on one stream; it reads no operand
+before the previous launch has finished.
 
 Printed: one JSON line with the throughput (TFLOP/s = 2·M·N·K / time), the
 roofline fraction of the GEMM kernel against the measured dense 16-bit tensor
@@ -307,9 +310,11 @@ def cublas_context(A_d, B_d, steps: int, stream, flush=None):
         for a, b in evs:
             if flush is not None:
                 flush.zero_()
-            a.record(stream)
-            torch.matmul(A_d, B_d.t(), out=out)
-            b.record(stream)
+                a.record(stream)
+                torch.matmul(A_d, B_d.t(), out=out)
+                b.record(stream)
+            else:
+                torch.matmul(A_d, B_d.t(), out=out)
         t1.record(stream)
         torch.cuda.synchronize()
         if flush is not None:
@@ -372,8 +377,10 @@ def run_ours(args, w):
     for rep in range(args.repeat):
         if rep and args.cooldown > 0:
             time.sleep(args.cooldown)
+        # per-launch events only around flushed launches: between back-to-back
+        # launches they would stop the next GEMM's set-up overlapping this one's tail
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
+               for _ in range(args.steps if flush is not None else 0)]
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         barrier(dist, device)
@@ -383,9 +390,11 @@ def run_ours(args, w):
         for i in range(args.steps):
             if flush is not None:
                 flush.zero_()          # evict the operands from L2 (outside the launch events)
-            evs[i][0].record(stream)
-            step()
-            evs[i][1].record(stream)
+                evs[i][0].record(stream)
+                step()
+                evs[i][1].record(stream)
+            else:
+                step()
         t_end.record(stream)
         torch.cuda.synchronize(device)
         w1 = time.time()
@@ -393,7 +402,10 @@ def run_ours(args, w):
         if sampler:
             sampler.window(w0, w1)
         times.append(t_start.elapsed_time(t_end) / 1e3)
-        launch_ms.extend(a.elapsed_time(b) for a, b in evs)
+        if flush is not None:
+            launch_ms.extend(a.elapsed_time(b) for a, b in evs)
+        else:   # back to back: the region is the launches
+            launch_ms.extend([times[-1] * 1e3 / args.steps] * args.steps)
     clocks = sampler.stop() if sampler else None
     if g.device_status(stream) != 0:
         raise SystemExit("bench.py: watchdog word set during the timed region")

@@ -370,6 +370,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
     ptx::tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(&ctl->tmem_base);
 
+    // Programmatic dependent launch: the next kernel on the stream may start
+    // its own set-up as soon as SMs free up; everything above touched only this
+    // CTA's shared and tensor memory.  Global memory (operands, C, workspace,
+    // watchdog word) is touched only after the previous kernel on the stream has
+    // completed and its writes are visible.
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
+
     Watch w;
     w.limit_ns = p.timeout_ns;
     w.abort_flag = &ctl->abort_flag;
@@ -1049,18 +1057,22 @@ gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t
     }
 
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.gridDim = dim3(uint32_t(pl.grid_ctas), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cfg.stream = stream;
+    cfg.attrs = attr;
+    // may overlap its set-up with the tail of the previous kernel on the stream
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 1;
     if (Cfg::kCtas > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = Cfg::kCtas;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = Cfg::kCtas;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
     if (cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<Cfg>, p) != cudaSuccess) {
         cudaGetLastError();

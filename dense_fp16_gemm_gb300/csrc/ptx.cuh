@@ -52,6 +52,19 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v
     asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(cluster_addr), "r"(v) : "memory");
 }
 
+// ---- programmatic dependent launch -------------------------------------------
+
+// Let the grid launched next on the stream (with programmatic serialization
+// allowed) start as this CTA's resources free up.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the grids this one depends on have completed and their memory
+// operations are visible.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---- mbarrier --------------------------------------------------------------
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

@@ -70,6 +70,13 @@ typedef enum {
  * run mostly empty use a stream-K schedule (see `schedule` below) whose
  * workspace is taken from that pool on `stream` and handed back on it.
  *
+ * Ordering: the kernel is launched with programmatic stream serialization, so
+ * its CTAs may start their set-up (shared memory, barriers, tensor memory)
+ * while the kernel before it on `stream` is still draining.  It reads and
+ * writes no global memory (A, B, C, workspace, watchdog word) until that
+ * kernel has completed and its writes are visible (griddepcontrol.wait), so
+ * stream order holds as for any other launch.
+ *
  * Errors: invalid arguments are reported before anything is enqueued, and C is
  * left unchanged.  The call returns after enqueueing; a fault during execution
  * surfaces at the caller's next synchronisation, and a watchdog expiry (a
