@@ -37,6 +37,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <type_traits>
 
 #include "gemm_f16_nt.h"
 #include "ptx.cuh"
@@ -478,67 +479,85 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && prank == 0) {
-            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-            bool ok = true;
-            // bits 15 / 16: A / B MN-major ("transposed") in shared memory
-            const uint32_t idesc = Cfg::kIdesc | (p.a_mn << 15) | (p.b_mn << 16);
-            Work work;
-            Item it;
-            work_init(work, p, cluster, nclusters);
-            uint32_t item_no = 0;
-            while (ok && work_next(work, p, it)) {
-                if (!wait(acce0 + 8 * acc, acc_phase ^ 1u, w, kSiteMmaAccFree)) break;
-                ptx::tc_fence_after();
-                uint64_t* tr = (p.trace && item_no < p.trace_items)
-                                   ? p.trace + (size_t(cluster) * p.trace_items + item_no) * 8 : nullptr;
-                if (tr) {
-                    tr[0] = uint64_t(it.tile) | (uint64_t(it.kind) << 32);
-                    tr[1] = uint64_t(it.kb0) | (uint64_t(it.kb1) << 32);
-                    tr[2] = ptx::globaltimer();
-                }
-                ++item_no;
-                const uint32_t d = tmem_base + acc * uint32_t(BN);
-                uint64_t starved_ns = 0;   // traced: time spent waiting for filled stages
-                for (uint32_t kb = it.kb0; kb < it.kb1; ++kb) {
-                    if (tr && !ptx::mbar_try_wait(full0 + 8 * stage, phase)) {
-                        const uint64_t ts = ptx::globaltimer();
-                        ok = wait(full0 + 8 * stage, phase, w, kSiteMmaFull);
-                        starved_ns += ptx::globaltimer() - ts;
-                    } else if (!tr) {
-                        ok = wait(full0 + 8 * stage, phase, w, kSiteMmaFull);
+            // One thread issues every MMA of the pair, and a few extra instructions
+            // per k-block are enough to leave the tensor pipe idle between stages:
+            // the loop is compiled once per operand layout, so that inside it a
+            // stage and a 16-k step only move the descriptors' start-address field
+            // by compile-time amounts (16-byte units).
+            auto issue = [&](auto a_mn_tag, auto b_mn_tag) {
+                constexpr bool kAmn = decltype(a_mn_tag)::value;
+                constexpr bool kBmn = decltype(b_mn_tag)::value;
+                // bits 15 / 16: A / B MN-major ("transposed") in shared memory
+                constexpr uint32_t idesc = Cfg::kIdesc | (uint32_t(kAmn) << 15) | (uint32_t(kBmn) << 16);
+                // per 16-k step: 32 bytes along a K-major row, 16 rows (2048 bytes) MN-major
+                constexpr uint32_t a_kstep = kAmn ? (kUmmaK * 128) >> 4 : (kUmmaK * 2) >> 4;
+                constexpr uint32_t b_kstep = kBmn ? (kUmmaK * 128) >> 4 : (kUmmaK * 2) >> 4;
+                uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+                bool ok = true;
+                Work work;
+                Item it;
+                work_init(work, p, cluster, nclusters);
+                uint32_t item_no = 0;
+                while (ok && work_next(work, p, it)) {
+                    if (!wait(acce0 + 8 * acc, acc_phase ^ 1u, w, kSiteMmaAccFree)) break;
+                    ptx::tc_fence_after();
+                    uint64_t* tr = (p.trace && item_no < p.trace_items)
+                                       ? p.trace + (size_t(cluster) * p.trace_items + item_no) * 8 : nullptr;
+                    if (tr) {
+                        tr[0] = uint64_t(it.tile) | (uint64_t(it.kind) << 32);
+                        tr[1] = uint64_t(it.kb0) | (uint64_t(it.kb1) << 32);
+                        tr[2] = ptx::globaltimer();
+                    }
+                    ++item_no;
+                    const uint32_t d = tmem_base + acc * uint32_t(BN);
+                    uint64_t starved_ns = 0;   // traced: time spent waiting for filled stages
+                    for (uint32_t kb = it.kb0; kb < it.kb1; ++kb) {
+                        if (tr && !ptx::mbar_test_wait(full0 + 8 * stage, phase)) {
+                            const uint64_t ts = ptx::globaltimer();
+                            ok = wait(full0 + 8 * stage, phase, w, kSiteMmaFull);
+                            starved_ns += ptx::globaltimer() - ts;
+                        } else if (!tr) {
+                            ok = wait(full0 + 8 * stage, phase, w, kSiteMmaFull);
+                        }
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                        const uint32_t sa = sA + stage * uint32_t(Cfg::kABytes);
+                        const uint32_t sb = sB + stage * uint32_t(Cfg::kBBytes);
+                        const uint64_t ad = kAmn ? sdesc_sw128_mn(sa) : sdesc_sw128(sa);
+                        const uint64_t bd = kBmn ? sdesc_sw128_mn(sb) : sdesc_sw128(sb);
+#pragma unroll
+                        for (int k = 0; k < kBlockK / kUmmaK; ++k) {
+                            ptx::mma_f16<CG>(d, ad + a_kstep * uint32_t(k), bd + b_kstep * uint32_t(k), idesc,
+                                             (kb != it.kb0 || k != 0) ? 1u : 0u);
+                        }
+                        // Free this ring slot in every CTA of the pair once these MMAs retire.
+                        // (with two pairs, the stage is free only once both pairs' MMAs are done)
+                        if constexpr (CG == 2) ptx::mma_commit_pair(empty0 + 8 * stage, CP == 2 ? 0xF : 0x3);
+                        else ptx::mma_commit(empty0 + 8 * stage);
+                        if (++stage == uint32_t(S)) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
                     if (!ok) break;
-                    ptx::tc_fence_after();
-                    const uint64_t ad = p.a_mn ? sdesc_sw128_mn(sA + stage * Cfg::kABytes)
-                                               : sdesc_sw128(sA + stage * Cfg::kABytes);
-                    const uint64_t bd = p.b_mn ? sdesc_sw128_mn(sB + stage * Cfg::kBBytes)
-                                               : sdesc_sw128(sB + stage * Cfg::kBBytes);
-                    // per 16-k step: 32 bytes along a K-major row, 16 rows (2048 bytes) MN-major
-                    const uint64_t astep = p.a_mn ? (kUmmaK * 128) >> 4 : (kUmmaK * 2) >> 4;
-                    const uint64_t bstep = p.b_mn ? (kUmmaK * 128) >> 4 : (kUmmaK * 2) >> 4;
-#pragma unroll
-                    for (int k = 0; k < kBlockK / kUmmaK; ++k) {
-                        ptx::mma_f16<CG>(d, ad + astep * k, bd + bstep * k, idesc,
-                                         (kb != it.kb0 || k != 0) ? 1u : 0u);
+                    if constexpr (CG == 2) ptx::mma_commit_pair(accf0 + 8 * acc, uint16_t(0x3u << lead));
+                    else ptx::mma_commit(accf0 + 8 * acc);
+                    if (tr) {
+                        tr[3] = ptx::globaltimer();
+                        tr[7] = starved_ns;
                     }
-                    // Free this ring slot in every CTA of the pair once these MMAs retire.
-                    // (with two pairs, the stage is free only once both pairs' MMAs are done)
-                    if constexpr (CG == 2) ptx::mma_commit_pair(empty0 + 8 * stage, CP == 2 ? 0xF : 0x3);
-                    else ptx::mma_commit(empty0 + 8 * stage);
-                    if (++stage == uint32_t(S)) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                    acc ^= 1u;
+                    if (acc == 0) acc_phase ^= 1u;
                 }
-                if (!ok) break;
-                if constexpr (CG == 2) ptx::mma_commit_pair(accf0 + 8 * acc, uint16_t(0x3u << lead));
-                else ptx::mma_commit(accf0 + 8 * acc);
-                if (tr) {
-                    tr[3] = ptx::globaltimer();
-                    tr[7] = starved_ns;
-                }
-                acc ^= 1u;
-                if (acc == 0) acc_phase ^= 1u;
+            };
+            using K_ = std::false_type;
+            using T_ = std::true_type;
+            if (p.a_mn) {
+                if (p.b_mn) issue(T_{}, T_{});
+                else issue(T_{}, K_{});
+            } else {
+                if (p.b_mn) issue(K_{}, T_{});
+                else issue(K_{}, K_{});
             }
             // Every MMA must have retired before the tensor memory is released.
             if constexpr (CG == 2) ptx::mma_commit_pair(mma_done, uint16_t(1u << lead));
