@@ -324,6 +324,69 @@ def cublas_context(A_d, B_d, steps: int, stream, flush=None):
         m.allow_fp16_reduced_precision_reduction, m.allow_bf16_reduced_precision_reduction = prev
 
 
+def run_e2e(args, w, A, B, Ad, Bd, Cd, tdt, entry, device, dist, bf16):
+    """Pipelined end-to-end steps; returns (max time over ranks, total flops, steps)."""
+    import torch
+    steps = max(1, min(args.steps, 20))
+    npA = A.view(np.int16) if bf16 else A
+    npB = B.view(np.int16) if bf16 else B
+    hA = torch.empty(Ad.shape, dtype=tdt, pin_memory=True)
+    hB = torch.empty(Bd.shape, dtype=tdt, pin_memory=True)
+    (hA.view(torch.int16) if bf16 else hA).copy_(torch.from_numpy(np.ascontiguousarray(npA)))
+    (hB.view(torch.int16) if bf16 else hB).copy_(torch.from_numpy(np.ascontiguousarray(npB)))
+    hC = [torch.empty(Cd.shape, dtype=tdt, pin_memory=True) for _ in range(2)]
+    dA = [Ad, torch.empty_like(Ad)]
+    dB = [Bd, torch.empty_like(Bd)]
+    dC = [Cd, torch.empty_like(Cd)]
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    s_mm = torch.cuda.current_stream(device)
+    handle = s_mm.cuda_stream
+
+    def gemm(j):
+        st = entry(w.M, w.N, w.K, dA[j].data_ptr(), w.K, dB[j].data_ptr(), w.K, dC[j].data_ptr(), w.N, handle)
+        if st != 0:
+            raise RuntimeError(f"GEMM call failed with status {st}")
+
+    def run(n):
+        ev_in = [torch.cuda.Event() for _ in range(n)]
+        ev_mm = [torch.cuda.Event() for _ in range(n)]
+        ev_out = [torch.cuda.Event() for _ in range(n)]
+        for i in range(n):
+            j = i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_mm[i - 2])      # buffers j free once GEMM i-2 has read them
+                dA[j].copy_(hA, non_blocking=True)
+                dB[j].copy_(hB, non_blocking=True)
+                ev_in[i].record(s_in)
+            s_mm.wait_event(ev_in[i])
+            if i >= 2:
+                s_mm.wait_event(ev_out[i - 2])         # C buffer j read back
+            gemm(j)
+            ev_mm[i].record(s_mm)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_mm[i])
+                hC[j].copy_(dC[j], non_blocking=True)
+                ev_out[i].record(s_out)
+        s_mm.wait_stream(s_out)
+
+    run(2)
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    e0.record(s_mm)
+    run(steps)
+    e1.record(s_mm)
+    torch.cuda.synchronize(device)
+    t, work = reduce_time_and_work(dist, e0.elapsed_time(e1) / 1e3, float(w.flops * steps), device)
+    for h in hC:
+        if torch.isnan(h.float() if bf16 else h).any().item():
+            raise SystemExit("bench.py: end-to-end result has unwritten elements")
+    return t, work, steps
+
+
 def run_ours(args, w):
     import torch
 
@@ -422,32 +485,12 @@ def run_ours(args, w):
     achieved = w.flops / mean_launch_s / 1e12
     peak, peak_sustained, peak_src = measured_peak()
 
-    # end to end through the same C ABI from pinned host memory
-    e2e_steps = max(1, min(args.steps, 10))
-    Ah = Ad.cpu().pin_memory()
-    Bh = Bd.cpu().pin_memory()
-    Ch = torch.empty((w.M, w.N), dtype=tdt).pin_memory()
-
-    def e2e_step():
-        Ad.copy_(Ah, non_blocking=True)
-        Bd.copy_(Bh, non_blocking=True)
-        step()
-        Ch.copy_(Cd, non_blocking=True)
-
-    e2e_step()
-    torch.cuda.synchronize(device)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    barrier(dist, device)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(device)
-    e2e_t, e2e_work = reduce_time_and_work(dist, e0.elapsed_time(e1) / 1e3,
-                                           float(w.flops * e2e_steps), device)
-    if torch.isnan(Ch).any().item():
-        raise SystemExit("bench.py: end-to-end result has unwritten elements")
+    # End to end through the same C ABI from pinned host memory, pipelined the
+    # way a serving loop would run it: two device buffer sets, the host->device
+    # copy of step i+1 and the device->host copy of step i-1 on their own
+    # streams while the GEMM of step i runs.  Every step's inputs are copied in
+    # and its whole result copied out inside the timed region.
+    e2e_t, e2e_work, e2e_steps = run_e2e(args, w, A, B, Ad, Bd, Cd, tdt, entry, device, dist, bf16)
 
     context = None
     if rank == 0 and not args.no_cublas:
@@ -485,7 +528,10 @@ def run_ours(args, w):
                          "frac_of_sustained": round(achieved / peak_sustained, 4) if peak_sustained else None,
                          "kernel": kernel_desc},
             "e2e": {"value": round(e2e_work / e2e_t / 1e12, 2), "unit": UNIT,
-                    "h2d_bytes_per_step": int(A.nbytes + B.nbytes), "d2h_bytes_per_step": int(Ch.numel() * 2)},
+                    "h2d_bytes_per_step": int(Ad.numel() * Ad.element_size() + Bd.numel() * Bd.element_size()),
+                    "d2h_bytes_per_step": int(Cd.numel() * Cd.element_size()), "steps": e2e_steps,
+                    "pipeline": "pinned host buffers, two device buffer sets: the host-to-device copy of "
+                                "step i+1 and the device-to-host copy of step i-1 overlap the GEMM of step i"},
             "gpu_launches": args.steps * args.repeat,
             "clocks": clocks,
             "timing": {"repeats": args.repeat, "cooldown_s": args.cooldown,
