@@ -238,7 +238,8 @@ __device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr) {
 // may start or end inside a tile:
 //   - a piece that does not start at k-block 0 (only ever a cluster's first
 //     item) is written as an fp32 partial tile to the cluster's workspace slot
-//     and published with a release flag;
+//     and published with a release flag; its k-blocks run from the last one
+//     down, so that all clusters' first pieces end at the same k-block;
 //   - the piece that starts at k-block 0 but stops early is the tile's owner:
 //     it waits for the partials of the clusters that took the rest of the tile
 //     (the next ones in order), adds them in that order and stores C.
@@ -405,7 +406,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                 raster_coord(p.raster, it.tile, mt, nt);
                 const int32_t m0 = int32_t(mt * Cfg::kTileM + prank * kBlockM);
                 const int32_t n0 = int32_t((nt * CP + pair) * BN + prank * Cfg::kBRows);
-                for (uint32_t kb = it.kb0; kb < it.kb1; ++kb) {
+                // A partial piece (a cluster's first item) loads its k-blocks from
+                // the last one down, so that at the start of a launch the pieces
+                // of all clusters read the same k-slab at the same time and
+                // neighbouring tiles share it in L2.  The MMA issuer consumes
+                // stages in ring order and needs no change.
+                const bool down = it.kind == kItemPartialOut;
+                for (uint32_t i = it.kb0; i < it.kb1; ++i) {
+                    const uint32_t kb = down ? it.kb1 - 1u - (i - it.kb0) : i;
                     if (!wait(empty0 + 8 * stage, phase ^ 1u, w, kSiteProducerEmpty)) {
                         ok = false;
                         break;
