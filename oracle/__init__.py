@@ -91,6 +91,11 @@ class Oracle:
         lib.oracle_f64_to_f16_array.restype = None
         lib.oracle_f16_to_f64_array.argtypes = [_i64, _p, _p]
         lib.oracle_f16_to_f64_array.restype = None
+        lib.oracle_gemm_f16_nt_acc16.argtypes = [_i64, _i64, _i64, _p, _i64, _p, _i64,
+                                                 _p, _i64, ctypes.c_int]
+        lib.oracle_gemm_f16_nt_acc16.restype = None
+        lib.oracle_gemm_f16_nt_acc16_points.argtypes = [_i64, _p, _i64, _p, _i64, _i64, _p, _p, _p]
+        lib.oracle_gemm_f16_nt_acc16_points.restype = None
         lib.oracle_gemm_bf16_nt.argtypes = [_i64, _i64, _i64, _p, _i64, _p, _i64, _p, _i64,
                                             ctypes.c_int]
         lib.oracle_gemm_bf16_nt.restype = None
@@ -159,6 +164,43 @@ class Oracle:
                                            rows.ctypes.data, cols.ctypes.data,
                                            out.ctypes.data, out64.ctypes.data)
         return out, out64
+
+    # ---- fp16 accumulation: the accumulator rounded to fp16 every 16 k ----
+
+    def gemm_f16_nt_acc16(self, A: np.ndarray, B: np.ndarray, C: np.ndarray | None = None,
+                          threads: int | None = None) -> np.ndarray:
+        """The fp16-accumulation variant: acc <- RNE_fp16(acc + the fp64 sum of
+        the next 16 products), k ascending, from acc = +0; C = the last acc."""
+        M, K = A.shape
+        N, K2 = B.shape
+        if K2 != K:
+            raise ValueError("A and B disagree on K")
+        if C is None:
+            C = np.empty((M, N), dtype=np.float16)
+        if C.shape != (M, N):
+            raise ValueError("C has the wrong shape")
+        pa, lda = _rows(A, "A")
+        pb, ldb = _rows(B, "B")
+        pc, ldc = _rows(C, "C")
+        self.lib.oracle_gemm_f16_nt_acc16(M, N, K, pa, lda, pb, ldb, pc, ldc,
+                                          threads or default_threads())
+        return C
+
+    def gemm_f16_nt_acc16_points(self, A: np.ndarray, B: np.ndarray, rows, cols) -> np.ndarray:
+        """The fp16-accumulation variant at the listed (row, col) positions."""
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        cols = np.ascontiguousarray(cols, dtype=np.int64)
+        M, K = A.shape
+        N, _ = B.shape
+        if rows.size and (rows.min() < 0 or rows.max() >= M
+                          or cols.min() < 0 or cols.max() >= N):
+            raise IndexError("sample position out of range")
+        out = np.empty(rows.shape, dtype=np.float16)
+        pa, lda = _rows(A, "A")
+        pb, ldb = _rows(B, "B")
+        self.lib.oracle_gemm_f16_nt_acc16_points(K, pa, lda, pb, ldb, rows.size, rows.ctypes.data,
+                                                 cols.ctypes.data, out.ctypes.data)
+        return out
 
     # ---- bfloat16: arrays hold bf16 bit patterns as numpy.uint16 ----------
 
@@ -251,6 +293,14 @@ def round_f64_to_f16(x):
 
 def widen_f16_to_f64(h):
     return default().widen_f16_to_f64(h)
+
+
+def gemm_f16_nt_acc16(A, B, C=None, threads=None):
+    return default().gemm_f16_nt_acc16(A, B, C, threads)
+
+
+def gemm_f16_nt_acc16_points(A, B, rows, cols):
+    return default().gemm_f16_nt_acc16_points(A, B, rows, cols)
 
 
 def gemm_bf16_nt(A, B, C=None, threads=None):

@@ -33,6 +33,8 @@
  * The same product with bfloat16 operands and result (oracle_gemm_bf16_nt and
  * its helpers, at the end of this file) serves the bf16 variant of the
  * method: the sum is again a sequential fp64 sum, rounded once, to bf16.
+ * oracle_gemm_f16_nt_acc16 serves the fp16-accumulation variant: the
+ * accumulator is rounded to fp16 after every 16-wide k step (see dot_acc16).
  */
 #include <math.h>
 #include <pthread.h>
@@ -122,12 +124,40 @@ static double dot_f64(int64_t K, const uint16_t *a, const uint16_t *b)
     return s;
 }
 
+/*
+ * fp16 accumulation, the variant the pages set against fp32 accumulation
+ * ("6. Register Reallocation, Multicast, and a Persistent Kernel", the closing
+ * Note on an earlier version that accumulated with wgmma f16.f16.f16, and its
+ * error over a K = 8192 reduction).  The pages do not say how the fp16
+ * accumulator is rounded.  The reading taken: the tensor-core instruction adds
+ * one 16-wide k step at a time (K = 16 for 16-bit operands), and the
+ * accumulator is a binary16 value after every step:
+ *
+ *     acc_0 = +0,   acc_{j+1} = RNE_fp16( acc_j + sum_{k=16j}^{min(16j+16,K)-1} A[m,k]·B[n,k] ),
+ *
+ * C[m,n] = acc after the last step, each step's sum in fp64, k ascending.
+ */
+#define ORACLE_ACC16_STEP 16
+
+static uint16_t dot_acc16(int64_t K, const uint16_t *a, const uint16_t *b)
+{
+    uint16_t acc = 0;
+    for (int64_t k0 = 0; k0 < K; k0 += ORACLE_ACC16_STEP) {
+        int64_t k1 = k0 + ORACLE_ACC16_STEP < K ? k0 + ORACLE_ACC16_STEP : K;
+        double s = g_f16_table[acc];
+        for (int64_t k = k0; k < k1; ++k) s += g_f16_table[a[k]] * g_f16_table[b[k]];
+        acc = oracle_f64_to_f16(s);
+    }
+    return acc;
+}
+
 typedef struct {
     int64_t m0, m1, N, K;
     const uint16_t *A; int64_t lda;
     const uint16_t *B; int64_t ldb;
     uint16_t *C; int64_t ldc;       /* rounded output, or NULL */
     double *S; int64_t lds;         /* unrounded output, or NULL */
+    int acc16;                      /* fp16 accumulation instead of one final rounding */
 } rows_job;
 
 static void *rows_worker(void *p)
@@ -135,6 +165,10 @@ static void *rows_worker(void *p)
     rows_job *j = (rows_job *)p;
     for (int64_t m = j->m0; m < j->m1; ++m) {
         for (int64_t n = 0; n < j->N; ++n) {
+            if (j->acc16) {
+                j->C[m * j->ldc + n] = dot_acc16(j->K, j->A + m * j->lda, j->B + n * j->ldb);
+                continue;
+            }
             double s = dot_f64(j->K, j->A + m * j->lda, j->B + n * j->ldb);
             if (j->C) j->C[m * j->ldc + n] = oracle_f64_to_f16(s);
             if (j->S) j->S[m * j->lds + n] = s;
@@ -145,7 +179,7 @@ static void *rows_worker(void *p)
 
 static void run_rows(int64_t M, int64_t N, int64_t K,
                      const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
-                     uint16_t *C, int64_t ldc, double *S, int64_t lds, int nthreads)
+                     uint16_t *C, int64_t ldc, double *S, int64_t lds, int acc16, int nthreads)
 {
     pthread_once(&g_table_once, build_table);
     if (M <= 0 || N <= 0) return;
@@ -161,7 +195,7 @@ static void run_rows(int64_t M, int64_t N, int64_t K,
         int64_t m0 = t * per, m1 = m0 + per;
         if (m0 >= M) break;
         if (m1 > M) m1 = M;
-        job[t] = (rows_job){m0, m1, N, K, A, lda, B, ldb, C, ldc, S, lds};
+        job[t] = (rows_job){m0, m1, N, K, A, lda, B, ldb, C, ldc, S, lds, acc16};
         created[t] = 0;
         njobs = t + 1;
     }
@@ -181,7 +215,7 @@ void oracle_gemm_f16_nt(int64_t M, int64_t N, int64_t K,
                         const uint16_t *B, int64_t ldb,
                         uint16_t *C, int64_t ldc, int nthreads)
 {
-    run_rows(M, N, K, A, lda, B, ldb, C, ldc, NULL, 0, nthreads);
+    run_rows(M, N, K, A, lda, B, ldb, C, ldc, NULL, 0, 0, nthreads);
 }
 
 /* The same sums before the final rounding, S[m*lds+n] (fp64). */
@@ -190,7 +224,7 @@ void oracle_gemm_f16_nt_f64(int64_t M, int64_t N, int64_t K,
                             const uint16_t *B, int64_t ldb,
                             double *S, int64_t lds, int nthreads)
 {
-    run_rows(M, N, K, A, lda, B, ldb, NULL, 0, S, lds, nthreads);
+    run_rows(M, N, K, A, lda, B, ldb, NULL, 0, S, lds, 0, nthreads);
 }
 
 /* Selected elements only: out[i] = C_ref[rows[i], cols[i]], one by one.  For
@@ -207,6 +241,27 @@ void oracle_gemm_f16_nt_points(int64_t K,
         if (out) out[i] = oracle_f64_to_f16(s);
         if (out_f64) out_f64[i] = s;
     }
+}
+
+/* C[m*ldc+n] = acc after the last 16-wide step of the fp16-accumulation
+ * recurrence above, for all m < M, n < N. */
+void oracle_gemm_f16_nt_acc16(int64_t M, int64_t N, int64_t K,
+                              const uint16_t *A, int64_t lda,
+                              const uint16_t *B, int64_t ldb,
+                              uint16_t *C, int64_t ldc, int nthreads)
+{
+    run_rows(M, N, K, A, lda, B, ldb, C, ldc, NULL, 0, 1, nthreads);
+}
+
+/* Selected elements of the fp16-accumulation variant, one by one. */
+void oracle_gemm_f16_nt_acc16_points(int64_t K,
+                                     const uint16_t *A, int64_t lda,
+                                     const uint16_t *B, int64_t ldb,
+                                     int64_t npts, const int64_t *rows, const int64_t *cols,
+                                     uint16_t *out)
+{
+    pthread_once(&g_table_once, build_table);
+    for (int64_t i = 0; i < npts; ++i) out[i] = dot_acc16(K, A + rows[i] * lda, B + cols[i] * ldb);
 }
 
 /* Vectorised conversions for the tests. */

@@ -2,7 +2,9 @@
 
 Each case below plants one mistake in a copy of the oracle's C source (on the
 CPU, in a temporary directory), compiles it, and runs every pin of
-test_oracle_pins.py and test_oracle_pins_bf16.py against the planted copy: at least one pin has to fail.
+test_oracle_pins.py, test_oracle_pins_bf16.py and test_oracle_pins_acc16.py
+against the planted copy: at least one pin has to fail.  A mutation is one
+(old, new) replacement or a list of them.
 The committed oracle is never modified.
 """
 import inspect
@@ -12,6 +14,7 @@ import pytest
 
 import oracle
 import tests.test_oracle_pins as pins
+import tests.test_oracle_pins_acc16 as pins_acc16
 import tests.test_oracle_pins_bf16 as pins_bf16
 
 _SRC = os.path.join(os.path.dirname(oracle.__file__), "gemm_oracle.c")
@@ -45,6 +48,15 @@ MUTATIONS = {
                                 "if (E > 127) return sign | 0x7f7f;\n    if (E < -126)"),
     "bf16_reversed_k_index": ("g_bf16_table[a[k]] * g_bf16_table[b[k]]",
                               "g_bf16_table[a[k]] * g_bf16_table[b[K - 1 - k]]"),
+    "acc16_step_32": ("#define ORACLE_ACC16_STEP 16", "#define ORACLE_ACC16_STEP 32"),
+    "acc16_step_8": ("#define ORACLE_ACC16_STEP 16", "#define ORACLE_ACC16_STEP 8"),
+    "acc16_accumulator_not_carried": ("double s = g_f16_table[acc];", "double s = 0.0;"),
+    "acc16_rounded_only_at_end": [
+        ("    uint16_t acc = 0;\n    for (int64_t k0 = 0;", "    uint16_t acc = 0;\n    double carry = 0.0;\n    for (int64_t k0 = 0;"),
+        ("double s = g_f16_table[acc];", "double s = carry;"),
+        ("        acc = oracle_f64_to_f16(s);\n", "        carry = s;\n        acc = oracle_f64_to_f16(s);\n")],
+    "acc16_last_partial_step_dropped": ("int64_t k1 = k0 + ORACLE_ACC16_STEP < K ? k0 + ORACLE_ACC16_STEP : K;",
+                                        "int64_t k1 = k0 + ORACLE_ACC16_STEP < K ? k0 + ORACLE_ACC16_STEP : k0;"),
 }
 
 
@@ -52,7 +64,8 @@ def _pin_calls():
     """Every (name, function, kwargs) of the pin modules, parametrizations expanded."""
     calls = []
     for name, fn in (inspect.getmembers(pins, inspect.isfunction)
-                     + inspect.getmembers(pins_bf16, inspect.isfunction)):
+                     + inspect.getmembers(pins_bf16, inspect.isfunction)
+                     + inspect.getmembers(pins_acc16, inspect.isfunction)):
         if not name.startswith("test_"):
             continue
         marks = [m for m in getattr(fn, "pytestmark", []) if m.name == "parametrize"]
@@ -69,11 +82,14 @@ def _pin_calls():
 
 @pytest.mark.parametrize("mutation", sorted(MUTATIONS))
 def test_planted_mistake_is_caught(mutation, tmp_path):
-    old, new = MUTATIONS[mutation]
+    edits = MUTATIONS[mutation]
+    edits = edits if isinstance(edits, list) else [edits]
     src = open(_SRC).read()
-    assert src.count(old) >= 1, f"mutation anchor for {mutation} not found"
+    for old, new in edits:
+        assert src.count(old) >= 1, f"mutation anchor for {mutation} not found: {old!r}"
+        src = src.replace(old, new)
     mutated = tmp_path / "gemm_oracle_mutated.c"
-    mutated.write_text(src.replace(old, new))
+    mutated.write_text(src)
     planted = oracle.Oracle(oracle.compile_source(str(mutated), str(tmp_path / "lib.so")))
     caught = []
     for name, fn, kw in _pin_calls():
