@@ -27,6 +27,7 @@ needs no exchange between GPUs.  The slowest rank's time sets the figure.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -256,18 +257,24 @@ class ClockSampler:
 # CPU oracle leg (the reported baseline)
 # ---------------------------------------------------------------------------
 
-def cpu_oracle_sample(w, A, B, target_s: float = 15.0):
+def oracle_fn(acc16: bool):
+    import oracle
+    return oracle.gemm_f16_nt_acc16 if acc16 else oracle.gemm_f16_nt
+
+
+def cpu_oracle_sample(w, A, B, target_s: float = 15.0, acc16: bool = False):
     """Time the oracle on the first R rows of C, R sized for about target_s."""
     import oracle
+    fn = oracle_fn(acc16)
     threads = oracle.default_threads()
     r0 = max(threads, 1)
     t0 = time.perf_counter()
-    oracle.gemm_f16_nt(A[:r0], B, threads=threads)
+    fn(A[:r0], B, threads=threads)
     dt = time.perf_counter() - t0
     rows = int(min(w.M, max(r0, r0 * target_s / max(dt, 1e-3))))
     rows = max(threads, rows - rows % threads)
     t0 = time.perf_counter()
-    oracle.gemm_f16_nt(A[:rows], B, threads=threads)
+    fn(A[:rows], B, threads=threads)
     dt = time.perf_counter() - t0
     flops = 2.0 * rows * w.N * w.K
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -279,13 +286,13 @@ def cpu_oracle_sample(w, A, B, target_s: float = 15.0):
 # arms
 # ---------------------------------------------------------------------------
 
-def workload_config(w, flushed: bool = False):
+def workload_config(w, flushed: bool = False, accumulate: str = "f32"):
     l2 = (f"L2 flushed between steps (256 MiB write); value from per-launch events "
           f"(A+B+C = {w.compulsory_bytes / 2**20:.0f} MiB)" if flushed else
           f"operands larger than L2: A+B+C = {w.compulsory_bytes / 2**20:.0f} MiB > 129 MB")
     return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
             "layout": "A[M,K] B[N,K] C[M,N] row-major, C = A·Bᵀ",
-            "accumulate": "f32", "inputs": f"A {w.dist_a}, B {w.dist_b}, seeds {w.seed_a},{w.seed_b}",
+            "accumulate": accumulate, "inputs": f"A {w.dist_a}, B {w.dist_b}, seeds {w.seed_a},{w.seed_b}",
             "l2": l2, "parallelism": "replicas"}
 
 
@@ -414,7 +421,14 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(device)
     handle = stream.cuda_stream
     lib = g.library()
-    entry = lib.gemm_bf16_nt if bf16 else lib.gemm_f16_nt
+    acc16 = args.accumulate == "f16"
+    if acc16:   # the fp16-accumulation variant, through the options entry point
+        acc_opts = g.Options(accumulate=1)
+
+        def entry(*a):
+            return lib.gemm_f16_nt_ex(*a, ctypes.byref(acc_opts))
+    else:
+        entry = lib.gemm_bf16_nt if bf16 else lib.gemm_f16_nt
 
     def step():
         st = entry(w.M, w.N, w.K, Ad.data_ptr(), w.K, Bd.data_ptr(), w.K, Cd.data_ptr(), w.N, handle)
@@ -502,15 +516,17 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not bf16:
-        cpu = cpu_oracle_sample(w, A, B, args.cpu_seconds)
+        cpu = cpu_oracle_sample(w, A, B, args.cpu_seconds, acc16)
 
     if rank == 0:
         traffic = recorded_traffic(w.name)
         lim = g.device_limits()
-        pl = g.plan(w.M, w.N, w.K, num_sms=lim["sms"])
-        pl = g.plan(w.M, w.N, w.K, num_sms=lim["sms"],
+        popts = g.Options(accumulate=1 if acc16 else 0)
+        pl = g.plan(w.M, w.N, w.K, num_sms=lim["sms"], options=popts)
+        pl = g.plan(w.M, w.N, w.K, num_sms=lim["sms"], options=popts,
                     max_clusters=lim["resident_pair_pairs"] if pl["cluster_pairs"] == 2 else lim["resident_pairs"])
-        kernel_desc = (f"gemm_f16_nt_kernel<KCfg<{pl['cta_group']},256,{pl['stages']},{pl['cluster_pairs']}>>: "
+        kernel_desc = (f"gemm_f16_nt_kernel<KCfg<{pl['cta_group']},256,{pl['stages']},{pl['cluster_pairs']},"
+                       f"{int(bf16)},{int(acc16)}>>: "
                        f"{pl['clusters']} clusters x {pl['grid_ctas'] // pl['clusters']} CTAs, "
                        f"{pl['tile_m']}x{pl['tile_n']} cluster tiles, {pl['sk_tiles']} of {pl['num_tiles']} "
                        f"split in k")
@@ -520,7 +536,7 @@ def run_ours(args, w):
             "ms_per_step": round(t_max / args.steps * 1e3, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if bf16 else "f16",
-            "data": "synthetic", "config": workload_config(w, flush is not None),
+            "data": "synthetic", "config": workload_config(w, flush is not None, args.accumulate),
             "pct_of_peak": round(100.0 * achieved / peak, 2),
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                          "unit": UNIT, "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -549,21 +565,22 @@ def run_reference(args, w):
     if rank != 0:
         return
     import oracle
+    fn = oracle_fn(args.accumulate == "f16")
     A, B = inputs.operands(w)
     threads = oracle.default_threads()
     # each step: a bounded sample of the workload, the first R rows of C
     probe = max(threads, 1)
     t0 = time.perf_counter()
-    oracle.gemm_f16_nt(A[:probe], B, threads=threads)
+    fn(A[:probe], B, threads=threads)
     dt = time.perf_counter() - t0
     per_step_target = max(0.5, args.cpu_seconds / max(args.steps + args.warmup, 1))
     rows = int(min(w.M, max(probe, probe * per_step_target / max(dt, 1e-3))))
     rows = max(threads, rows - rows % threads)
     for _ in range(args.warmup):
-        oracle.gemm_f16_nt(A[:rows], B, threads=threads)
+        fn(A[:rows], B, threads=threads)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.gemm_f16_nt(A[:rows], B, threads=threads)
+        fn(A[:rows], B, threads=threads)
     dt = time.perf_counter() - t0
     flops = 2.0 * rows * w.N * w.K * args.steps
     value = flops / dt / 1e12
@@ -571,7 +588,8 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(w),
+        "data": "synthetic", "config": {**workload_config(w, accumulate=args.accumulate),
+                                        "l2": "host cores (no GPU cache involved)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"each step: rows 0..{rows - 1} of C ({rows}x{w.N}x{w.K})"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -589,6 +607,8 @@ def main(argv=None):
     ap.add_argument("--dtype", choices=["f16", "bf16"], default="f16",
                     help="operand/result type: f16 (the method's) or the bf16 variant")
     ap.add_argument("--workload", default="gemm_8192", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--accumulate", choices=["f32", "f16"], default="f32",
+                    help="accumulator type: f32 (the method) or the fp16-accumulation variant")
     ap.add_argument("--repeat", type=int, default=1,
                     help="timed regions of K steps per process (the median is reported)")
     ap.add_argument("--cooldown", type=float, default=1.0, help="seconds of idle before each repeat")
@@ -601,6 +621,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.accumulate == "f16" and args.dtype == "bf16":
+        ap.error("--accumulate f16 needs fp16 operands")
     world, _, _ = dist_env()
     if args.gpus != world and world > 1:
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")

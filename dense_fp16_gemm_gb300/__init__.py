@@ -47,7 +47,7 @@ class Options(ctypes.Structure):
                 ("timeout_ns", ctypes.c_uint64), ("schedule", ctypes.c_int32),
                 ("trace_items", ctypes.c_int32), ("trace", ctypes.c_void_p),
                 ("cluster_pairs", ctypes.c_int32), ("a_layout", ctypes.c_int32),
-                ("b_layout", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("b_layout", ctypes.c_int32), ("accumulate", ctypes.c_int32)]
 
 
 class Plan(ctypes.Structure):

@@ -74,10 +74,11 @@ enum : uint32_t { kItemWhole = 0, kItemPartialOut = 1, kItemOwner = 2 };
 
 __device__ uint32_t g_watchdog_word;
 
-template <int CG, int BN, int STAGES, int CP = 1, bool BF = false>
+template <int CG, int BN, int STAGES, int CP = 1, bool BF = false, bool A16 = false>
 struct KCfg {
     static constexpr int kCG = CG;
     static constexpr bool kBF = BF;                  // bf16 operands and result instead of fp16
+    static constexpr bool kA16 = A16;                // fp16 accumulator instead of fp32
     static constexpr int kCP = CP;                   // CTA pairs per cluster (A shared by multicast)
     static constexpr int kCtas = CG * CP;            // CTAs per cluster
     static constexpr int kBN = BN;                   // columns of C per tile
@@ -93,10 +94,11 @@ struct KCfg {
     static constexpr int kOutBytes = kEpiWarps * kOutBufs * kOutBufBytes;
     static constexpr int kCtlBytes = 256;
     static constexpr int kSmemBytes = 1024 + kRingBytes + kOutBytes + kCtlBytes;
-    // tcgen05 instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B
-    // fp16 (bits 7-9, 10-12 = 0) or bf16 (= 1), both K-major (bits 15, 16 = 0),
-    // N>>3 at bit 17, M>>4 at bit 24.
-    static constexpr uint32_t kIdesc = (1u << 4) | (uint32_t(BF) << 7) | (uint32_t(BF) << 10) |
+    // tcgen05 instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1) or fp16
+    // (= 0), A and B fp16 (bits 7-9, 10-12 = 0) or bf16 (= 1), both K-major
+    // (bits 15, 16 = 0), N>>3 at bit 17, M>>4 at bit 24.  An fp16 D takes the
+    // same TMEM columns as fp32: one value per 32-bit column, in its low half.
+    static constexpr uint32_t kIdesc = (uint32_t(!A16) << 4) | (uint32_t(BF) << 7) | (uint32_t(BF) << 10) |
                                        (uint32_t(BN >> 3) << 17) | (uint32_t(kTileM >> 4) << 24);
 
     static_assert(2 * BN <= 512, "two accumulator buffers must fit in the 512 TMEM columns");
@@ -104,6 +106,7 @@ struct KCfg {
     static_assert(kBRows <= 256, "a TMA box is at most 256 rows");
     static_assert(kSmemBytes <= 232448, "dynamic shared memory limit per CTA");
     static_assert(CP == 1 || (CG == 2 && CP == 2), "two pairs per cluster only with CTA pairs");
+    static_assert(!(A16 && BF), "an fp16 accumulator needs fp16 operands");
 };
 
 template <int STAGES>
@@ -672,14 +675,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                     }
                 }
                 uint32_t h[32];
+                if constexpr (Cfg::kA16) {
+                    // fp16 accumulator: each column's low half already is the result
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    h[j] = Cfg::kBF ? ptx::pack_bf16x2_rn(lo[2 * j], lo[2 * j + 1])
-                                    : ptx::pack_f16x2_rn(lo[2 * j], lo[2 * j + 1]);
+                    for (int j = 0; j < 16; ++j) h[j] = (lo[2 * j] & 0xFFFFu) | (lo[2 * j + 1] << 16);
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    h[16 + j] = Cfg::kBF ? ptx::pack_bf16x2_rn(hi[2 * j], hi[2 * j + 1])
-                                         : ptx::pack_f16x2_rn(hi[2 * j], hi[2 * j + 1]);
+                    for (int j = 0; j < 16; ++j) h[16 + j] = (hi[2 * j] & 0xFFFFu) | (hi[2 * j + 1] << 16);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        h[j] = Cfg::kBF ? ptx::pack_bf16x2_rn(lo[2 * j], lo[2 * j + 1])
+                                        : ptx::pack_f16x2_rn(lo[2 * j], lo[2 * j + 1]);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        h[16 + j] = Cfg::kBF ? ptx::pack_bf16x2_rn(hi[2 * j], hi[2 * j + 1])
+                                             : ptx::pack_f16x2_rn(hi[2 * j], hi[2 * j + 1]);
+                }
 
                 // The staging buffer about to be written was last read by the
                 // store issued two chunks ago.
@@ -755,6 +766,9 @@ using Cfg1 = KCfg<1, 256, 4>;      // single CTA, 128×256 tile, 4-stage ring
 using Cfg2Bf = KCfg<2, 256, 6, 1, true>;    // the same three with bf16 operands and result
 using Cfg2x2Bf = KCfg<2, 256, 6, 2, true>;
 using Cfg1Bf = KCfg<1, 256, 4, 1, true>;
+using Cfg2A16 = KCfg<2, 256, 6, 1, false, true>;   // the fp16 ones with an fp16 accumulator
+using Cfg2x2A16 = KCfg<2, 256, 6, 2, false, true>;
+using Cfg1A16 = KCfg<1, 256, 4, 1, false, true>;
 
 template <class Cfg>
 bool allow_smem() {
@@ -810,7 +824,8 @@ gemm_status_t setup_device(int dev, DeviceState& st) {
         g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
     if (!allow_smem<Cfg2>() || !allow_smem<Cfg2x2>() || !allow_smem<Cfg1>() ||
-        !allow_smem<Cfg2Bf>() || !allow_smem<Cfg2x2Bf>() || !allow_smem<Cfg1Bf>()) {
+        !allow_smem<Cfg2Bf>() || !allow_smem<Cfg2x2Bf>() || !allow_smem<Cfg1Bf>() ||
+        !allow_smem<Cfg2A16>() || !allow_smem<Cfg2x2A16>() || !allow_smem<Cfg1A16>()) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
@@ -962,8 +977,9 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
     const int sw = (o && o->swizzle) ? o->swizzle : kDefaultSwizzle;
     const int sched = o ? o->schedule : 0;
     const int cp = (o && o->cluster_pairs) ? o->cluster_pairs : 1;
+    const int acc = o ? o->accumulate : 0;
     if ((cg != 1 && cg != 2) || sw < 1 || sw > 64 || (o && o->max_clusters < 0) || sched < 0 ||
-        sched > 2 || cp < 1 || cp > 2 || (cp == 2 && cg != 2))
+        sched > 2 || cp < 1 || cp > 2 || (cp == 2 && cg != 2) || acc < 0 || acc > 1)
         return GEMM_ERR_INVALID_VALUE;
     memset(pl, 0, sizeof(*pl));
     pl->cta_group = cg;
@@ -999,7 +1015,9 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
     const int64_t kb = pl->k_blocks;
     int64_t clusters = tiles < resident ? tiles : resident;
     int64_t sk_tiles = 0;
-    if (tiles > 0 && kb > 0 && sched != 1) {
+    // An fp16 accumulator runs whole tiles: a split would add fp32 partials of
+    // fp16 accumulators, a different rounding sequence.
+    if (tiles > 0 && kb > 0 && sched != 1 && acc == 0) {
         if (tiles >= resident) {
             const int64_t rem = tiles % resident;
             const int64_t slots = (tiles + resident - 1) / resident * resident;
@@ -1111,7 +1129,8 @@ gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t
 gemm_status_t run(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B,
                   int64_t ldb, uint16_t* C, int64_t ldc, void* stream_v, const gemm_f16_nt_options_t* o,
                   bool bf16 = false) {
-    if (o && (o->a_layout < 0 || o->a_layout > 1 || o->b_layout < 0 || o->b_layout > 1 || o->reserved != 0))
+    if (o && (o->a_layout < 0 || o->a_layout > 1 || o->b_layout < 0 || o->b_layout > 1 ||
+              o->accumulate < 0 || o->accumulate > 1 || (bf16 && o->accumulate != 0)))
         return GEMM_ERR_INVALID_VALUE;
     gemm_status_t s = check_args(M, N, K, A, lda, B, ldb, C, ldc, o && o->a_layout == 1, o && o->b_layout == 1);
     if (s != GEMM_OK) return s;
@@ -1153,6 +1172,10 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t ld
         if (cg == 1) s = launch<Cfg1Bf>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
         else if (cp == 2) s = launch<Cfg2x2Bf>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
         else s = launch<Cfg2Bf>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
+    } else if (ro.accumulate == 1) {
+        if (cg == 1) s = launch<Cfg1A16>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
+        else if (cp == 2) s = launch<Cfg2x2A16>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
+        else s = launch<Cfg2A16>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
     } else {
         if (cg == 1) s = launch<Cfg1>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
         else if (cp == 2) s = launch<Cfg2x2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);

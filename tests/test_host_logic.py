@@ -221,7 +221,19 @@ def test_layout_pitches_validated():
     assert call(16, 64, 40, lda=40, ldb=32, opts=g.Options(b_layout=1)) == 1     # ldb < N
     assert call(16, 64, 36, lda=36, ldb=64, ldc=64, opts=g.Options(b_layout=1)) == 2     # lda % 8 != 0
     assert call(8, 8, 16, opts=g.Options(a_layout=2)) == 1
-    assert call(8, 8, 16, opts=g.Options(reserved=1)) == 1
+    assert call(8, 8, 16, opts=g.Options(accumulate=2)) == 1
+
+
+def test_fp16_accumulation_option_validated():
+    lib = g.library()
+    # fp16 accumulator with bf16 operands: rejected before anything is enqueued
+    assert lib.gemm_bf16_nt_ex(8, 8, 16, 0x10000, 16, 0x20000, 16, 0x30000, 8, None,
+                               g.Options(accumulate=1)) == 1
+    assert call(8, 8, 16, opts=g.Options(accumulate=-1)) == 1
+    # the fp16 accumulator always runs whole tiles
+    assert g.plan(4096, 4096, 4096, options=g.Options(accumulate=1))["sk_tiles"] == 0
+    assert g.plan(4096, 4096, 4096, options=g.Options(accumulate=1, schedule=2))["sk_tiles"] == 0
+    assert g.plan(256, 256, 8192, options=g.Options(accumulate=1))["clusters"] == 1
 
 
 def test_bad_options_rejected():
