@@ -199,13 +199,13 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  *                 accumulator, so the result carries one fp16 rounding per 16
  *                 k instead of one in all.  This is the variant the pages set
  *                 against fp32 accumulation ("6. Register Reallocation,
- *                 Multicast, and a Persistent Kernel", the closing Note on an
- *                 earlier version: over K = 8192 with unit-variance outputs,
- *                 mean absolute error 0.0023 against 0.00014, maximum 0.047).
- *                 It runs whole tiles only (no stream-K split), at the same
- *                 speed: on these tensor cores the fp16 accumulator takes the
- *                 same tensor-memory columns as fp32 (one value per 32-bit
- *                 column).  Any other value, or 1 with bf16 operands, returns
+ *                 Multicast, and a Persistent Kernel", §Shared-Memory
+ *                 Epilogue, the Note on an earlier version: over K = 8192 with
+ *                 unit-variance outputs, mean absolute error 0.0023 against
+ *                 0.00014, maximum 0.047).  It runs whole tiles only (no
+ *                 stream-K split).  On these tensor cores the fp16 accumulator
+ *                 takes the same tensor-memory columns as fp32 (one value per
+ *                 32-bit column), so the tile shapes are the same.  Any other value, or 1 with bf16 operands, returns
  *                 GEMM_ERR_INVALID_VALUE.
  */
 typedef struct {

@@ -126,9 +126,9 @@ static double dot_f64(int64_t K, const uint16_t *a, const uint16_t *b)
 
 /*
  * fp16 accumulation, the variant the pages set against fp32 accumulation
- * ("6. Register Reallocation, Multicast, and a Persistent Kernel", the closing
- * Note on an earlier version that accumulated with wgmma f16.f16.f16, and its
- * error over a K = 8192 reduction).  The pages do not say how the fp16
+ * ("6. Register Reallocation, Multicast, and a Persistent Kernel",
+ * §Shared-Memory Epilogue, the Note on an earlier version that accumulated
+ * with wgmma f16.f16.f16, and its error over a K = 8192 reduction).  The pages do not say how the fp16
  * accumulator is rounded.  The reading taken: the tensor-core instruction adds
  * one 16-wide k step at a time (K = 16 for 16-bit operands), and the
  * accumulator is a binary16 value after every step:

@@ -15,7 +15,7 @@ The bar:
   * the error against the exact sum has the pages' statistics: mean 0.0023 over
     a K = 8192 reduction with unit-variance outputs (0.00014 with fp32
     accumulation), maximum 0.047 ("6. Register Reallocation, Multicast, and a
-    Persistent Kernel", the closing Note).
+    Persistent Kernel", §Shared-Memory Epilogue, the Note).
 """
 import numpy as np
 import pytest

@@ -16,17 +16,14 @@ oracle itself:
                            the mean absolute error against the exact sum is
                            0.0023 with fp16 accumulation and 0.00014 with fp32
                            ("6. Register Reallocation, Multicast, and a
-                           Persistent Kernel", the closing Note on the earlier
-                           fp16-accumulating version); the maximum there was 0.047.
+                           Persistent Kernel", §Shared-Memory Epilogue, the Note
+                           on an earlier fp16-accumulating version); the
+                           maximum there was 0.047.
 """
 import numpy as np
 import pytest
 
 from dense_fp16_gemm_gb300 import inputs
-
-
-def _h(*vals):
-    return np.array(vals, dtype=np.float16)
 
 
 @pytest.mark.parametrize("K", [1, 5, 16])
