@@ -60,7 +60,8 @@ class Plan(ctypes.Structure):
                 ("grid_ctas", ctypes.c_int32), ("swizzle", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("tmem_cols", ctypes.c_int32),
                 ("sk_tiles", ctypes.c_int32), ("cluster_pairs", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_int64)]
+                ("workspace_bytes", ctypes.c_int64), ("tail_tiles", ctypes.c_int32),
+                ("tail_split", ctypes.c_int32)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -123,6 +123,7 @@ struct Ctl {
 struct Params {
     CUtensorMap tmA;   // A: dims {K, M}, box {64, 128}
     CUtensorMap tmB;   // B: dims {K, N}, box {64, BN/CG}
+    CUtensorMap tmBp;  // B for N-split tail tiles: box {64, BN/CG/tail_split}
     CUtensorMap tmC;   // C: dims {N8, M}, box {64, 32}; only when N8 > 0
     Raster raster;
     uint32_t num_tiles;
@@ -143,6 +144,10 @@ struct Params {
     float* partials;       // [cluster][cta rank][BN/4][128 rows] float4 partial tiles
     uint64_t* flags;       // [cluster][cta rank][epilogue warp]: launch_id once written
     uint64_t launch_id;    // unique per launch, so stale flags never match
+    // N-split tail: tiles [tail_first, num_tiles) are each cut into tail_split
+    // tiles of BN/tail_split columns (tail_first = num_tiles: no split)
+    uint32_t tail_first;
+    uint32_t tail_split;
     uint64_t* trace;       // optional per-item timestamps (debugging)
     uint32_t trace_items;
 };
@@ -249,15 +254,25 @@ __device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr) {
 // Owner pieces come at the end of a cluster's range and partial pieces at the
 // start, so an owner seldom waits.
 
+//
+// After the whole tiles come the N-split items: the last tiles of the raster,
+// [tail_first, num_tiles), each cut into tail_split column slices of
+// BN/tail_split, dealt round-robin like the whole tiles.  No cluster depends
+// on another's result.  A slice's main loop is as long as a whole tile's (a
+// narrower MMA is not faster per k-block); its epilogue drains 1/tail_split of
+// the accumulator.
+
 struct Item {
     uint32_t tile;
     uint32_t kb0, kb1;   // k-block range [kb0, kb1)
     uint32_t kind;
+    uint32_t part, parts;   // column slice `part` of `parts` (1 = the whole tile)
 };
 
 struct Work {
     uint64_t u, u_end;   // this cluster's stream-K units still to do
     uint32_t t;          // next whole tile
+    uint32_t q;          // next N-split tail item
     uint32_t G;          // clusters
 };
 
@@ -269,6 +284,7 @@ __device__ __forceinline__ void work_init(Work& s, const Params& p, uint32_t c, 
     s.u = sk_begin(p, c, G);
     s.u_end = sk_begin(p, c + 1, G);
     s.t = p.sk_tiles + c;
+    s.q = c;
     s.G = G;
 }
 
@@ -282,15 +298,26 @@ __device__ __forceinline__ bool work_next(Work& s, const Params& p, Item& it) {
         it.kb0 = kb0;
         it.kb1 = kb1;
         it.kind = kb0 > 0 ? kItemPartialOut : (kb1 < p.num_kb ? kItemOwner : kItemWhole);
+        it.part = 0;
+        it.parts = 1;
         s.u += kb1 - kb0;
         return true;
     }
-    if (s.t < p.num_tiles) {
+    it.kb0 = 0;
+    it.kb1 = p.num_kb;
+    it.kind = kItemWhole;
+    if (s.t < p.tail_first) {
         it.tile = s.t;
-        it.kb0 = 0;
-        it.kb1 = p.num_kb;
-        it.kind = kItemWhole;
+        it.part = 0;
+        it.parts = 1;
         s.t += s.G;
+        return true;
+    }
+    if (s.q < (p.num_tiles - p.tail_first) * p.tail_split) {
+        it.tile = p.tail_first + s.q / p.tail_split;
+        it.part = s.q % p.tail_split;
+        it.parts = p.tail_split;
+        s.q += s.G;
         return true;
     }
     return false;
@@ -408,7 +435,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                 uint32_t mt, nt;
                 raster_coord(p.raster, it.tile, mt, nt);
                 const int32_t m0 = int32_t(mt * Cfg::kTileM + prank * kBlockM);
-                const int32_t n0 = int32_t((nt * CP + pair) * BN + prank * Cfg::kBRows);
+                // an N-split tail item loads BRows/parts rows of B at its column slice
+                const int32_t brows = Cfg::kBRows / int32_t(it.parts);
+                const int32_t n0 = int32_t((nt * CP + pair) * BN + it.part * (BN / it.parts)) + prank * brows;
+                const uint32_t tx = it.parts == 1 ? uint32_t(Cfg::kTxBytes)
+                                                  : uint32_t(Cfg::kABytes + Cfg::kBBytes / int32_t(it.parts)) * CG;
                 // A partial piece (a cluster's first item) loads its k-blocks from
                 // the last one down, so that at the start of a launch the pieces
                 // of all clusters read the same k-slab at the same time and
@@ -421,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                         ok = false;
                         break;
                     }
-                    if (prank == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * stage, Cfg::kTxBytes);
+                    if (prank == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * stage, tx);
                     const int32_t k0 = int32_t(kb * kBlockK);
                     const uint32_t bar = full_tgt + 8 * stage;
                     // A K-major operand is one box {64 k, rows}; an MN-major one is
@@ -456,8 +487,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                                 ptx::tma_load_2d_hint(b_dst + j * kMnBoxBytes, &p.tmB, n0 + 64 * j, k0, bar, keep_b);
                         }
                     } else {
-                        if constexpr (CG == 2) ptx::tma_load_2d_pair_hint(b_dst, &p.tmB, k0, n0, bar, keep_b);
-                        else ptx::tma_load_2d_hint(b_dst, &p.tmB, k0, n0, bar, keep_b);
+                        // (tail items exist only for K-major B with one pair per cluster)
+                        const CUtensorMap* mb = it.parts == 1 ? &p.tmB : &p.tmBp;
+                        if constexpr (CG == 2) ptx::tma_load_2d_pair_hint(b_dst, mb, k0, n0, bar, keep_b);
+                        else ptx::tma_load_2d_hint(b_dst, mb, k0, n0, bar, keep_b);
                     }
                     ++issued;
                     if (++stage == uint32_t(S)) {
@@ -521,6 +554,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                     }
                     ++item_no;
                     const uint32_t d = tmem_base + acc * uint32_t(BN);
+                    // a tail item's MMAs are BN/parts wide (instruction descriptor N at bit 17)
+                    const uint32_t id = it.parts == 1
+                                            ? idesc
+                                            : (idesc & ~(0x3Fu << 17)) | (((uint32_t(BN) / it.parts) >> 3) << 17);
                     uint64_t starved_ns = 0;   // traced: time spent waiting for filled stages
                     for (uint32_t kb = it.kb0; kb < it.kb1; ++kb) {
                         if (tr && !ptx::mbar_test_wait(full0 + 8 * stage, phase)) {
@@ -538,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                         const uint64_t bd = kBmn ? sdesc_sw128_mn(sb) : sdesc_sw128(sb);
 #pragma unroll
                         for (int k = 0; k < kBlockK / kUmmaK; ++k) {
-                            ptx::mma_f16<CG>(d, ad + a_kstep * uint32_t(k), bd + b_kstep * uint32_t(k), idesc,
+                            ptx::mma_f16<CG>(d, ad + a_kstep * uint32_t(k), bd + b_kstep * uint32_t(k), id,
                                              (kb != it.kb0 || k != 0) ? 1u : 0u);
                         }
                         // Free this ring slot in every CTA of the pair once these MMAs retire.
@@ -598,7 +635,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
             uint32_t mt, nt;
             raster_coord(p.raster, it.tile, mt, nt);
             const int32_t row0 = int32_t(mt * Cfg::kTileM + prank * kBlockM + q * 32u);
-            const int32_t col0 = int32_t((nt * CP + pair) * BN);
+            const int32_t col0 = int32_t((nt * CP + pair) * BN + it.part * (BN / it.parts));
+            const int nchunks = (BN / kEpiCols) / int(it.parts);
             uint64_t* tr = (p.trace && item_no < p.trace_items && rank == 0 && warp == 2 && lane == 0)
                                ? p.trace + (size_t(cluster) * p.trace_items + item_no) * 8 : nullptr;
             ++item_no;
@@ -626,12 +664,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
             if (tr) tr[5] = ptx::globaltimer();
             const uint32_t tacc = tmem_base + lane_off + acc * uint32_t(BN);
 #pragma unroll 1
-            for (int c = 0; c < BN / kEpiCols; ++c) {
+            for (int c = 0; c < nchunks; ++c) {
                 uint32_t lo[32], hi[32];
                 ptx::tmem_ld_32x32b_x32(tacc + uint32_t(c * kEpiCols), lo);
                 ptx::tmem_ld_32x32b_x32(tacc + uint32_t(c * kEpiCols + 32), hi);
                 ptx::tmem_wait_ld();
-                if (c == BN / kEpiCols - 1) {
+                if (c == nchunks - 1) {
                     // The whole accumulator is in registers: hand the buffer back.
                     ptx::tc_fence_before();
                     __syncwarp();
@@ -979,7 +1017,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
     const int cp = (o && o->cluster_pairs) ? o->cluster_pairs : 1;
     const int acc = o ? o->accumulate : 0;
     if ((cg != 1 && cg != 2) || sw < 1 || sw > 64 || (o && o->max_clusters < 0) || sched < 0 ||
-        sched > 2 || cp < 1 || cp > 2 || (cp == 2 && cg != 2) || acc < 0 || acc > 1)
+        sched > 3 || cp < 1 || cp > 2 || (cp == 2 && cg != 2) || acc < 0 || acc > 1)
         return GEMM_ERR_INVALID_VALUE;
     memset(pl, 0, sizeof(*pl));
     pl->cta_group = cg;
@@ -1014,10 +1052,10 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
     // loses 1.4 % when split.  1 = whole tiles only; 2 = stream-K whenever it can.
     const int64_t kb = pl->k_blocks;
     int64_t clusters = tiles < resident ? tiles : resident;
-    int64_t sk_tiles = 0;
-    // An fp16 accumulator runs whole tiles: a split would add fp32 partials of
+    int64_t sk_tiles = 0, tail_tiles = 0, tail_split = 1;
+    // An fp16 accumulator never splits in k: that would add fp32 partials of
     // fp16 accumulators, a different rounding sequence.
-    if (tiles > 0 && kb > 0 && sched != 1 && acc == 0) {
+    if (tiles > 0 && kb > 0 && sched != 1 && sched != 3 && acc == 0) {
         if (tiles >= resident) {
             const int64_t rem = tiles % resident;
             const int64_t slots = (tiles + resident - 1) / resident * resident;
@@ -1034,10 +1072,32 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
             }
         }
     }
+    // N-split: with fewer tiles than clusters and no stream-K split (too few
+    // k-blocks for one to pay), each tile is cut into s = 2 or 4 column slices
+    // (the largest with tiles·s <= clusters) that run on their own pairs.  A
+    // narrower MMA takes no fewer cycles per k-block on these tensor cores, so
+    // this cannot shorten a compute-bound wave; what it shortens is each
+    // cluster's epilogue, which is most of a small problem's time.  With 3 it
+    // is also used for the last wave of a larger problem (tests).  One pair per
+    // cluster and B stored [N, K] only.
+    const bool can_split = cg == 2 && cp == 1 && !(o && o->b_layout == 1);
+    if (sk_tiles == 0 && tiles > 0 && kb > 0 && can_split &&
+        ((sched == 0 && tiles < resident) || sched == 3)) {
+        const int64_t R = tiles % resident;          // all tiles when tiles < resident
+        int64_t s = 1;
+        while (s < 4 && R > 0 && R * s * 2 <= resident) s *= 2;
+        if (s > 1) {
+            tail_tiles = R;
+            tail_split = s;
+            clusters = tiles >= resident ? resident : R * s;
+        }
+    }
     pl->clusters = int32_t(clusters);
     pl->grid_ctas = int32_t(clusters * cg * cp);
     pl->sk_tiles = int32_t(sk_tiles);
     pl->workspace_bytes = sk_tiles > 0 ? workspace_bytes(cg * cp, clusters) : 0;
+    pl->tail_tiles = int32_t(tail_tiles);
+    pl->tail_split = int32_t(tail_split);
     return GEMM_OK;
 }
 
@@ -1096,6 +1156,13 @@ gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t
         p.partials = reinterpret_cast<float*>(ws + flags_bytes(Cfg::kCtas, pl.clusters));
     }
     p.launch_id = ++g_launch_seq;
+    p.tail_split = uint32_t(pl.tail_split > 1 ? pl.tail_split : 1);
+    p.tail_first = uint32_t(pl.num_tiles - (pl.tail_split > 1 ? pl.tail_tiles : 0));
+    if (pl.tail_split > 1 &&
+        (b_mn || Cfg::kCP != 1 ||
+         (s = encode_2d(&p.tmBp, dt, B, uint64_t(K), uint64_t(N), uint64_t(ldb), kBlockK,
+                        Cfg::kBRows / pl.tail_split)) != GEMM_OK))
+        return b_mn || Cfg::kCP != 1 ? GEMM_ERR_INVALID_VALUE : s;
     if (o && o->trace && o->trace_items > 0) {
         p.trace = o->trace;
         p.trace_items = uint32_t(o->trace_items);
@@ -1135,7 +1202,7 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t ld
     gemm_status_t s = check_args(M, N, K, A, lda, B, ldb, C, ldc, o && o->a_layout == 1, o && o->b_layout == 1);
     if (s != GEMM_OK) return s;
     if (o && ((o->cta_group != 0 && o->cta_group != 1 && o->cta_group != 2) || o->swizzle < 0 ||
-              o->swizzle > 64 || o->max_clusters < 0 || o->schedule < 0 || o->schedule > 2 ||
+              o->swizzle > 64 || o->max_clusters < 0 || o->schedule < 0 || o->schedule > 3 ||
               o->cluster_pairs < 0 || o->cluster_pairs > 2 || (o->cluster_pairs == 2 && o->cta_group == 1) ||
               o->trace_items < 0 || (o->trace && (reinterpret_cast<uintptr_t>(o->trace) & 7))))
         return GEMM_ERR_INVALID_VALUE;

@@ -155,7 +155,19 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  *                 tiles) is split evenly across all clusters (stream-K),
  *                 with fp32 partial tiles summed by each tile's first piece in
  *                 a fixed order (results are reproducible run to run);
- *                 1: whole tiles only; 2: stream-K whenever possible (tests).
+ *                 1: whole tiles only; 2: stream-K whenever possible (tests);
+ *                 3: N-split whenever possible (tests).
+ *                 N-split: when there are fewer tiles than clusters and the
+ *                 stream-K rule does not split them (too few k-blocks), each
+ *                 tile is cut along N into s = 2 or 4 narrower tiles (256×128
+ *                 or 256×64, s the largest with tiles·s <= clusters) that run
+ *                 on their own CTA pairs; nothing is summed across clusters.
+ *                 A narrower MMA takes no fewer cycles per k-block on these
+ *                 tensor cores, so this shortens each cluster's epilogue, not
+ *                 its main loop: it is for small, latency-bound problems.
+ *                 With 3 the last R tiles of a larger problem are cut the same
+ *                 way when 2R <= clusters.  Only with one CTA pair per cluster
+ *                 and B stored [N, K].
  *                 A stream-K launch needs a workspace (gemm_f16_nt_plan's
  *                 workspace_bytes); the call takes it from a memory pool
  *                 private to this library on `stream` (cudaMallocFromPoolAsync)
@@ -312,6 +324,8 @@ typedef struct {
     int32_t sk_tiles;      /* tiles [0, sk_tiles) are split in k across all clusters (stream-K) */
     int32_t cluster_pairs; /* CTA pairs per cluster (tile_n = 256 · cluster_pairs) */
     int64_t workspace_bytes; /* device workspace a stream-K launch needs (0 if none) */
+    int32_t tail_tiles;    /* the last tail_tiles tiles are each split in N (N-split) ... */
+    int32_t tail_split;    /* ... into tail_split narrower tiles (1 = no split) */
 } gemm_f16_nt_plan_t;
 
 gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms,

@@ -93,6 +93,40 @@ def test_stream_k_split_tiles(cg, max_clusters, shape):
     assert np.array_equal(C1.view(np.uint16), C2.view(np.uint16))
 
 
+@pytest.mark.parametrize("shape,max_clusters,schedule,split", [
+    ((1100, 2100, 520), 7, 3, 2),   # forced: 45 tiles on 7 pairs, the last 3 cut in two
+    ((1100, 2100, 520), 20, 3, 4),  # forced: the last 5 cut in four; N = 2100: slices past N store nothing
+    ((300, 520, 328), 0, 0, 4),     # 6 tiles of 6 k-blocks, all cut in four, over 24 pairs
+    ((1, 1, 1), 0, 0, 4),
+    ((1536, 1000, 256), 0, 0, 2),   # 24 tiles: cut in two; N % 8 == 0, M edge exact
+    ((513, 1025, 200), 9, 3, 1),    # 15 tiles on 9 pairs: 6 left over, 6·2 > 9: no split
+])
+def test_n_split(shape, max_clusters, schedule, split):
+    M, N, K = shape
+    A = inputs.draw((M, K), inputs.U, 95 + M)
+    B = inputs.draw((N, K), inputs.U, 96 + N)
+    o = g.Options(cluster_pairs=1, max_clusters=max_clusters, schedule=schedule)
+    pl = g.plan(M, N, K, options=o)
+    assert pl["tail_split"] == split and pl["sk_tiles"] == 0
+    C = run(A, B, options=o)
+    check_close(C, oracle.gemm_f16_nt(A, B), K, f"N-split {shape}")
+    # each output's k order is the same whatever the MMA width: identical to whole tiles
+    whole = run(A, B, options=g.Options(cluster_pairs=1, max_clusters=max_clusters, schedule=1))
+    assert np.array_equal(C.view(np.uint16), whole.view(np.uint16))
+
+
+def test_n_split_integers_and_fp16_accumulator():
+    M, N, K = 1300, 1000, 320                     # 24 tiles of 5 k-blocks: all cut in two
+    A = inputs.draw((M, K), inputs.I2, 97)
+    B = inputs.draw((N, K), inputs.I2, 98)
+    one = g.Options(cluster_pairs=1)
+    assert g.plan(M, N, K, options=one)["tail_split"] == 2
+    check_bitexact(run(A, B, options=one), oracle.gemm_f16_nt(A, B), "N-split int")
+    A16 = (A * (np.arange(K) % 4 == 0)).astype(np.float16)   # partial sums exact in fp16
+    C16 = run(A16, B, options=g.Options(cluster_pairs=1, accumulate=1))
+    assert np.array_equal(C16.astype(np.float64), A16.astype(np.float64) @ B.astype(np.float64).T)
+
+
 @pytest.mark.parametrize("shape,max_clusters,schedule", [
     ((1100, 2100, 520), 0, 0),      # 5 x 5 cluster tiles of 256 x 512
     ((1100, 2100, 520), 2, 1),      # persistent: 12-13 cluster tiles per cluster

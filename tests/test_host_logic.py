@@ -112,28 +112,52 @@ def test_plan_stream_k_schedule():
     # 4096^3: 256 tiles over 76 pairs leave 48 of 304 slots (16 %) idle: the
     # last wave (28 tiles) plus one full wave is split in k over all pairs
     p = g.plan(4096, 4096, 4096, num_sms=152)
-    assert p["sk_tiles"] == 28 + 76
+    assert p["sk_tiles"] == 28 + 76 and p["tail_split"] == 1
     assert p["workspace_bytes"] == 76 * 2 * 4 * 8 + 76 * 2 * 128 * 256 * 4
     # 8192^3: 40 of 1064 slots (3.8 %) idle: whole tiles, unless forced
     assert g.plan(8192, 8192, 8192, num_sms=152)["sk_tiles"] == 0
+    assert g.plan(8192, 8192, 8192, num_sms=152)["tail_split"] == 1
     assert g.plan(8192, 8192, 8192, options=g.Options(schedule=2))["sk_tiles"] == 36 + 76
     # whole tiles only on request, or when the last wave is nearly full
-    assert g.plan(4096, 4096, 4096, options=g.Options(schedule=1))["sk_tiles"] == 0
-    assert g.plan(4096, 4096, 4096, options=g.Options(schedule=1))["workspace_bytes"] == 0
+    p = g.plan(4096, 4096, 4096, options=g.Options(schedule=1))
+    assert (p["sk_tiles"], p["workspace_bytes"], p["tail_split"]) == (0, 0, 1)
     p = g.plan(256 * 19, 256 * 8, 4096, num_sms=152)      # 152 tiles = 2 full waves
-    assert p["sk_tiles"] == 0
+    assert (p["sk_tiles"], p["tail_split"]) == (0, 1)
     p = g.plan(256 * 15, 256 * 10, 4096, num_sms=152)     # 150 tiles: last wave 74/76 full
-    assert p["sk_tiles"] == 0
+    assert (p["sk_tiles"], p["tail_split"]) == (0, 1)
     # fewer tiles than pairs: spread when each share keeps >= 8 k-blocks
     one = g.Options(cluster_pairs=1)
     p = g.plan(1000, 700, 1000, options=one)              # 12 tiles x 16 k-blocks
-    assert (p["sk_tiles"], p["clusters"]) == (12, 24)
-    p = g.plan(256, 256, 256)                             # 1 tile x 4 k-blocks: not worth it
-    assert (p["sk_tiles"], p["clusters"]) == (0, 1)
+    assert (p["sk_tiles"], p["clusters"], p["tail_split"]) == (12, 24, 1)
     p = g.plan(256, 256, 4096, options=g.Options(schedule=2))   # forced: one k-block per pair
     assert (p["sk_tiles"], p["clusters"]) == (1, 64)
     with pytest.raises(g.GemmError):
-        g.plan(256, 256, 256, options=g.Options(schedule=3))
+        g.plan(256, 256, 256, options=g.Options(schedule=4))
+
+
+def test_plan_n_split():
+    # fewer tiles than pairs and too few k-blocks for stream-K: each tile is cut
+    # along N into s = 2 or 4 slices, the largest with tiles·s <= pairs
+    p = g.plan(256, 256, 256)                             # 1 tile x 4 k-blocks
+    assert (p["tail_tiles"], p["tail_split"], p["clusters"], p["grid_ctas"], p["sk_tiles"]) == (1, 4, 4, 8, 0)
+    p = g.plan(300, 520, 328, options=g.Options(cluster_pairs=1))   # 6 tiles x 6 k-blocks
+    assert (p["tail_tiles"], p["tail_split"], p["clusters"]) == (6, 4, 24)
+    p = g.plan(256 * 6, 256 * 5, 256)                     # 30 tiles: 30·2 <= 76 < 30·4
+    assert (p["tail_tiles"], p["tail_split"], p["clusters"]) == (30, 2, 60)
+    # not for full waves (a narrower MMA is not faster per k-block), unless forced (3)
+    for shape in ((8192, 8192, 8192), (16384, 14336, 4096)):
+        assert g.plan(*shape, num_sms=152)["tail_split"] == 1
+    p = g.plan(8192, 8192, 8192, options=g.Options(schedule=3))
+    assert (p["tail_tiles"], p["tail_split"], p["sk_tiles"], p["clusters"]) == (36, 2, 0, 76)
+    p = g.plan(16384, 14336, 4096, options=g.Options(schedule=3))
+    assert (p["tail_tiles"], p["tail_split"]) == (12, 4)
+    assert g.plan(256 * 15, 256 * 10, 4096, options=g.Options(schedule=3))["tail_split"] == 1   # R = 74
+    # not with two pairs per cluster, one CTA, B stored [K, N], or another forced schedule
+    for o in (g.Options(cluster_pairs=2), g.Options(cta_group=1), g.Options(b_layout=1),
+              g.Options(schedule=1), g.Options(schedule=2)):
+        assert g.plan(256, 256, 256, options=o)["tail_split"] == 1
+    # the fp16 accumulator may use it (each output's sum is unchanged)
+    assert g.plan(256, 256, 256, options=g.Options(accumulate=1))["tail_split"] == 4
 
 
 def test_plan_two_pairs_per_cluster():
@@ -164,7 +188,10 @@ def test_plan_edges_and_options():
     assert (p["cluster_pairs"], p["m_tiles"], p["n_tiles"]) == (2, 16, 6)
     assert g.plan(8192, 8192, 8192)["cluster_pairs"] == 1
     assert g.plan(4000, 256, 5000)["cluster_pairs"] == 1      # too narrow for two pairs
-    p = g.plan(100, 100, 8)                        # one pair tile, rank-1 rows all out of range
+    p = g.plan(100, 100, 8)                        # one pair tile, rank-1 rows all out of range,
+    # cut into four 64-column slices (the last two lie wholly past N and store nothing)
+    assert (p["num_tiles"], p["clusters"], p["grid_ctas"], p["tail_split"]) == (1, 4, 8, 4)
+    p = g.plan(100, 100, 8, options=g.Options(schedule=1))
     assert (p["num_tiles"], p["clusters"], p["grid_ctas"]) == (1, 1, 2)
     p1 = g.plan(4000, 3000, 5000, options=g.Options(cta_group=1))
     assert (p1["tile_m"], p1["m_tiles"], p1["grid_ctas"]) == (128, 32, 152)
@@ -230,10 +257,10 @@ def test_fp16_accumulation_option_validated():
     assert lib.gemm_bf16_nt_ex(8, 8, 16, 0x10000, 16, 0x20000, 16, 0x30000, 8, None,
                                g.Options(accumulate=1)) == 1
     assert call(8, 8, 16, opts=g.Options(accumulate=-1)) == 1
-    # the fp16 accumulator always runs whole tiles
+    # the fp16 accumulator never splits in k
     assert g.plan(4096, 4096, 4096, options=g.Options(accumulate=1))["sk_tiles"] == 0
     assert g.plan(4096, 4096, 4096, options=g.Options(accumulate=1, schedule=2))["sk_tiles"] == 0
-    assert g.plan(256, 256, 8192, options=g.Options(accumulate=1))["clusters"] == 1
+    assert g.plan(256, 256, 8192, options=g.Options(accumulate=1, schedule=1))["clusters"] == 1
 
 
 def test_bad_options_rejected():
