@@ -1,4 +1,5 @@
-// GB300 (sm_103a) dense fp16 NT GEMM:  C[M,N] = A[M,K] · B[N,K]ᵀ, fp32 accumulation.
+// GB300 (sm_103a) dense fp16 NT GEMM:  C[M,N] = A[M,K] · B[N,K]ᵀ, fp32 accumulation
+// (an fp16 accumulator and bf16 operands on request).
 //
 // One persistent kernel, warp-specialised:
 //   warp 0      TMA producer: fills an S-stage shared-memory ring (A tile + B
@@ -13,6 +14,14 @@
 // 2-SM MMAs (cta_group::2) on a 256×256 tile: each CTA loads its own 128 rows of
 // A and one half of the B tile, and the pair's single MMA reads both halves, so
 // the shared operand crosses L2 once per pair.
+//
+// Variants, all in this one kernel template (KCfg): a cluster of two pairs that
+// share A by TMA multicast; one CTA per tile (cta_group::1); bf16 operands and
+// result; an fp16 accumulator; A and/or B stored M/N-contiguous (MN-major
+// operands).  The work schedule (see "work schedule") mixes whole tiles, a
+// stream-K split of the last wave in k, and column slices of small problems'
+// tiles.  Launches use programmatic dependent launch: a CTA sets up, then
+// waits for the previous kernel on the stream before touching global memory.
 //
 // Design lineage (prior art, re-derived for tcgen05): the Tilus matmul-hopper
 // tutorial's V2 ring buffer ("2. Multi-Stage Software Pipelining"), V3 role
