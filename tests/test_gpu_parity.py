@@ -296,6 +296,34 @@ def test_workload_sampled(name):
 
 
 # ---------------------------------------------------------------------------
+# maximum sizes: 64-bit offsets, a very long k loop, a very tall problem
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,N,K,why", [
+    (70000, 32768, 64, "C is 4.6 GB: row offsets past 2^31 elements"),
+    (256, 512, 1 << 20, "2^20-deep k loop, split in k over every pair"),
+    (1 << 20, 72, 128, "a million rows, N % 64 != 0"),
+])
+def test_maximum_sizes_sampled(M, N, K, why):
+    A = inputs.draw((M, K), inputs.U, 601 + M % 97)
+    B = inputs.draw((N, K), inputs.U, 602 + N % 97)
+    Ad, Bd = to_device(A), to_device(B)
+    Cd, _ = empty_out(M, N)
+    g.gemm_f16_nt(Ad, Bd, Cd)
+    torch.cuda.synchronize()
+    assert not torch.isnan(Cd).any().item(), f"unwritten (NaN) elements in C ({why})"
+    rows, cols = sample_points(M, N, n_random=2000 if K < 4096 else 200)
+    if K >= 4096:   # each point is a 2^20-term dot product on the host: keep the sample small
+        keep = np.random.default_rng(1).choice(rows.size, 300, replace=False)
+        rows, cols = rows[keep], cols[keep]
+    got = Cd[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].cpu().numpy()
+    ref, _ = oracle.gemm_f16_nt_points(A, B, rows, cols)
+    check_close(got, ref, K, why)
+    del Cd, Ad, Bd
+    torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
 # operand layouts: A stored [K, M] and/or B stored [K, N] (MN-major tiles)
 # ---------------------------------------------------------------------------
 
