@@ -1016,7 +1016,8 @@ int resident_clusters_for(const DeviceState& st, const gemm_f16_nt_options_t& r)
 }
 
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t max_resident,
-                        const gemm_f16_nt_options_t* o, gemm_f16_nt_plan_t* pl) {
+                        const gemm_f16_nt_options_t* o, gemm_f16_nt_plan_t* pl,
+                        bool allow_split_k = true) {
     const int64_t lim = int64_t(1) << 31;
     if (!pl || M < 0 || N < 0 || K < 0 || M >= lim || N >= lim || K >= lim || num_sms < 1)
         return GEMM_ERR_INVALID_VALUE;
@@ -1064,7 +1065,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
     int64_t sk_tiles = 0, tail_tiles = 0, tail_split = 1;
     // An fp16 accumulator never splits in k: that would add fp32 partials of
     // fp16 accumulators, a different rounding sequence.
-    if (tiles > 0 && kb > 0 && sched != 1 && sched != 3 && acc == 0) {
+    if (allow_split_k && tiles > 0 && kb > 0 && sched != 1 && sched != 3 && acc == 0) {
         if (tiles >= resident) {
             const int64_t rem = tiles % resident;
             const int64_t slots = (tiles + resident - 1) / resident * resident;
@@ -1229,9 +1230,19 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t ld
     }
     const gemm_f16_nt_options_t ro = resolve_options(o, N, lda, ldb);
     const int cg = ro.cta_group, cp = ro.cluster_pairs;
+    // A captured launch is replayed with the parameters it was captured with.
+    // The stream-K split tags its completion flags with a per-launch id, which
+    // a replay would repeat (an owner could then take a partner's partial from
+    // an earlier replay), so a call made under stream capture runs without it.
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &capture) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    const bool allow_split_k = capture == cudaStreamCaptureStatusNone;
     gemm_f16_nt_plan_t pl;
     const int resident = resident_clusters_for(*st, ro);
-    if ((s = make_plan(M, N, K, st->sms, resident, &ro, &pl)) != GEMM_OK) return s;
+    if ((s = make_plan(M, N, K, st->sms, resident, &ro, &pl, allow_split_k)) != GEMM_OK) return s;
     void* ws = nullptr;
     if (pl.sk_tiles > 0) {
         // The workspace is taken from the library's pool on the caller's stream

@@ -77,6 +77,14 @@ typedef enum {
  * kernel has completed and its writes are visible (griddepcontrol.wait), so
  * stream order holds as for any other launch.
  *
+ * Stream capture: a call made while `stream` is being captured into a CUDA
+ * graph is planned without the stream-K split (schedule 2 included), because
+ * a replay repeats the launch's parameters and the split's completion flags
+ * are tagged per launch.  The captured kernel then touches only A, B, C, the
+ * watchdog word and (if requested) the trace buffer, so the graph can be
+ * replayed any number of times.  Make the first call on a device outside any
+ * capture: it sets the device up (kernel attributes, the memory pool).
+ *
  * Errors: invalid arguments are reported before anything is enqueued, and C is
  * left unchanged.  The call returns after enqueueing; a fault during execution
  * surfaces at the caller's next synchronisation, and a watchdog expiry (a
