@@ -563,39 +563,49 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                     }
                     ++item_no;
                     const uint32_t d = tmem_base + acc * uint32_t(BN);
-                    // a tail item's MMAs are BN/parts wide (instruction descriptor N at bit 17)
-                    const uint32_t id = it.parts == 1
-                                            ? idesc
-                                            : (idesc & ~(0x3Fu << 17)) | (((uint32_t(BN) / it.parts) >> 3) << 17);
                     uint64_t starved_ns = 0;   // traced: time spent waiting for filled stages
-                    for (uint32_t kb = it.kb0; kb < it.kb1; ++kb) {
-                        if (tr && !ptx::mbar_test_wait(full0 + 8 * stage, phase)) {
-                            const uint64_t ts = ptx::globaltimer();
-                            ok = wait(full0 + 8 * stage, phase, w, kSiteMmaFull);
-                            starved_ns += ptx::globaltimer() - ts;
-                        } else if (!tr) {
-                            ok = wait(full0 + 8 * stage, phase, w, kSiteMmaFull);
-                        }
-                        if (!ok) break;
-                        ptx::tc_fence_after();
-                        const uint32_t sa = sA + stage * uint32_t(Cfg::kABytes);
-                        const uint32_t sb = sB + stage * uint32_t(Cfg::kBBytes);
-                        const uint64_t ad = kAmn ? sdesc_sw128_mn(sa) : sdesc_sw128(sa);
-                        const uint64_t bd = kBmn ? sdesc_sw128_mn(sb) : sdesc_sw128(sb);
+                    // The k-block loop, compiled once per MMA width so that the
+                    // instruction descriptor stays a compile-time constant (a
+                    // descriptor in a register slows the issuing thread by ~2 %).
+                    auto kloop = [&](auto id_tag) {
+                        constexpr uint32_t id = decltype(id_tag)::value;
+                        for (uint32_t kb = it.kb0; kb < it.kb1; ++kb) {
+                            if (tr && !ptx::mbar_test_wait(full0 + 8 * stage, phase)) {
+                                const uint64_t ts = ptx::globaltimer();
+                                ok = wait(full0 + 8 * stage, phase, w, kSiteMmaFull);
+                                starved_ns += ptx::globaltimer() - ts;
+                            } else if (!tr) {
+                                ok = wait(full0 + 8 * stage, phase, w, kSiteMmaFull);
+                            }
+                            if (!ok) break;
+                            ptx::tc_fence_after();
+                            const uint32_t sa = sA + stage * uint32_t(Cfg::kABytes);
+                            const uint32_t sb = sB + stage * uint32_t(Cfg::kBBytes);
+                            const uint64_t ad = kAmn ? sdesc_sw128_mn(sa) : sdesc_sw128(sa);
+                            const uint64_t bd = kBmn ? sdesc_sw128_mn(sb) : sdesc_sw128(sb);
 #pragma unroll
-                        for (int k = 0; k < kBlockK / kUmmaK; ++k) {
-                            ptx::mma_f16<CG>(d, ad + a_kstep * uint32_t(k), bd + b_kstep * uint32_t(k), id,
-                                             (kb != it.kb0 || k != 0) ? 1u : 0u);
+                            for (int k = 0; k < kBlockK / kUmmaK; ++k) {
+                                ptx::mma_f16<CG>(d, ad + a_kstep * uint32_t(k), bd + b_kstep * uint32_t(k), id,
+                                                 (kb != it.kb0 || k != 0) ? 1u : 0u);
+                            }
+                            // Free this ring slot in every CTA of the pair once these MMAs retire.
+                            // (with two pairs, the stage is free only once both pairs' MMAs are done)
+                            if constexpr (CG == 2) ptx::mma_commit_pair(empty0 + 8 * stage, CP == 2 ? 0xF : 0x3);
+                            else ptx::mma_commit(empty0 + 8 * stage);
+                            if (++stage == uint32_t(S)) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
                         }
-                        // Free this ring slot in every CTA of the pair once these MMAs retire.
-                        // (with two pairs, the stage is free only once both pairs' MMAs are done)
-                        if constexpr (CG == 2) ptx::mma_commit_pair(empty0 + 8 * stage, CP == 2 ? 0xF : 0x3);
-                        else ptx::mma_commit(empty0 + 8 * stage);
-                        if (++stage == uint32_t(S)) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
-                    }
+                    };
+                    // an N-split item's MMAs are BN/parts wide (descriptor N>>3 at bit 17)
+                    constexpr uint32_t kNoN = idesc & ~(0x3Fu << 17);
+                    if (it.parts == 1)
+                        kloop(std::integral_constant<uint32_t, idesc>{});
+                    else if (it.parts == 2)
+                        kloop(std::integral_constant<uint32_t, kNoN | (uint32_t(BN / 2 / 8) << 17)>{});
+                    else
+                        kloop(std::integral_constant<uint32_t, kNoN | (uint32_t(BN / 4 / 8) << 17)>{});
                     if (!ok) break;
                     if constexpr (CG == 2) ptx::mma_commit_pair(accf0 + 8 * acc, uint16_t(0x3u << lead));
                     else ptx::mma_commit(accf0 + 8 * acc);
