@@ -257,15 +257,18 @@ class ClockSampler:
 # CPU oracle leg (the reported baseline)
 # ---------------------------------------------------------------------------
 
-def oracle_fn(acc16: bool):
+def oracle_fn(acc16: bool, bf16: bool = False):
+    """The oracle function matching the arm's arithmetic."""
     import oracle
+    if bf16:
+        return oracle.gemm_bf16_nt
     return oracle.gemm_f16_nt_acc16 if acc16 else oracle.gemm_f16_nt
 
 
-def cpu_oracle_sample(w, A, B, target_s: float = 15.0, acc16: bool = False):
+def cpu_oracle_sample(w, A, B, target_s: float = 15.0, acc16: bool = False, bf16: bool = False):
     """Time the oracle on the first R rows of C, R sized for about target_s."""
     import oracle
-    fn = oracle_fn(acc16)
+    fn = oracle_fn(acc16, bf16)
     threads = oracle.default_threads()
     r0 = max(threads, 1)
     t0 = time.perf_counter()
@@ -515,8 +518,8 @@ def run_ours(args, w):
                            "context only (not the target, not part of the value)"}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not bf16:
-        cpu = cpu_oracle_sample(w, A, B, args.cpu_seconds, acc16)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_sample(w, A, B, args.cpu_seconds, acc16, bf16)
 
     if rank == 0:
         traffic = recorded_traffic(w.name)
@@ -565,8 +568,13 @@ def run_reference(args, w):
     if rank != 0:
         return
     import oracle
-    fn = oracle_fn(args.accumulate == "f16")
-    A, B = inputs.operands(w)
+    bf16 = args.dtype == "bf16"
+    fn = oracle_fn(args.accumulate == "f16", bf16)
+    if bf16:   # bf16 bit patterns, same distributions and seeds
+        A = inputs.draw_bf16((w.M, w.K), w.dist_a, w.seed_a)
+        B = inputs.draw_bf16((w.N, w.K), w.dist_b, w.seed_b)
+    else:
+        A, B = inputs.operands(w)
     threads = oracle.default_threads()
     # each step: a bounded sample of the workload, the first R rows of C
     probe = max(threads, 1)

@@ -53,9 +53,10 @@ def _bench(args, env=None):
                           capture_output=True, text=True, env=e, timeout=600, cwd=ROOT)
 
 
-def test_reference_arm_prints_one_line():
+@pytest.mark.parametrize("extra", [[], ["--dtype", "bf16"], ["--accumulate", "f16"]])
+def test_reference_arm_prints_one_line(extra):
     r = _bench(["--impl", "reference", "--workload", "gemm_256", "--steps", "3", "--warmup", "3",
-                "--cpu-seconds", "1"])
+                "--cpu-seconds", "1", *extra])
     assert r.returncode == 0, r.stderr
     lines = [l for l in r.stdout.splitlines() if l.strip()]
     assert len(lines) == 1
@@ -65,6 +66,13 @@ def test_reference_arm_prints_one_line():
     assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
     assert d["config"]["workload"] == "gemm_256" and d["higher_is_better"] is True
+    assert d["config"]["accumulate"] == ("f16" if "--accumulate" in extra else "f32")
+
+
+def test_fp16_accumulator_with_bf16_rejected():
+    r = _bench(["--impl", "reference", "--workload", "gemm_256", "--steps", "3", "--warmup", "3",
+                "--dtype", "bf16", "--accumulate", "f16"])
+    assert r.returncode != 0
 
 
 def test_reference_arm_non_zero_rank_is_silent():
