@@ -257,6 +257,29 @@ class ClockSampler:
 # CPU oracle leg (the reported baseline)
 # ---------------------------------------------------------------------------
 
+def cpu_model() -> str:
+    """The host CPU's model name, as the kernel reports it."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                if key.strip().lower() in ("model name", "cpu model", "hardware") and val.strip():
+                    return val.strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def l2_to_sm_bytes(pl) -> int:
+    """Operand bytes the plan delivers into shared memory: every cluster tile
+    receives, over the whole k range, its B rows and, in each of its CTA
+    pairs, the tile's A rows (with two pairs A is read from L2 once and
+    multicast, but received twice)."""
+    tiles, kb = pl["num_tiles"], pl["k_blocks"]
+    return int(tiles * kb * 64 * 2 * (pl["tile_m"] * pl["cluster_pairs"] + pl["tile_n"]))
+
+
 def oracle_fn(acc16: bool, bf16: bool = False):
     """The oracle function matching the arm's arithmetic."""
     import oracle
@@ -281,6 +304,7 @@ def cpu_oracle_sample(w, A, B, target_s: float = 15.0, acc16: bool = False, bf16
     dt = time.perf_counter() - t0
     flops = 2.0 * rows * w.N * w.K
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "cpu": cpu_model(),
             "sample": f"rows 0..{rows - 1} of C ({rows}x{w.N}x{w.K}, {flops:.3e} flop) "
                       f"in {dt:.1f} s"}
 
@@ -545,7 +569,10 @@ def run_ours(args, w):
                          "unit": UNIT, "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_source": f"{peak_src} bf16 dense burst (fp16 runs at the bf16 rate)",
                          "frac_of_sustained": round(achieved / peak_sustained, 4) if peak_sustained else None,
-                         "kernel": kernel_desc},
+                         "kernel": kernel_desc,
+                         "compulsory_bytes_per_flop": round(w.compulsory_bytes / w.flops, 7),
+                         "dram_bytes_per_flop": round(traffic / w.flops, 7) if traffic else None,
+                         "l2_to_sm_bytes_per_flop": round(l2_to_sm_bytes(pl) / w.flops, 7)},
             "e2e": {"value": round(e2e_work / e2e_t / 1e12, 2), "unit": UNIT,
                     "h2d_bytes_per_step": int(Ad.numel() * Ad.element_size() + Bd.numel() * Bd.element_size()),
                     "d2h_bytes_per_step": int(Cd.numel() * Cd.element_size()), "steps": e2e_steps,
@@ -599,6 +626,7 @@ def run_reference(args, w):
         "data": "synthetic", "config": {**workload_config(w, accumulate=args.accumulate),
                                         "l2": "host cores (no GPU cache involved)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "cpu": cpu_model(),
                          "sample": f"each step: rows 0..{rows - 1} of C ({rows}x{w.N}x{w.K})"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
