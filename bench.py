@@ -267,6 +267,14 @@ def cpu_model() -> str:
                     return val.strip()
     except OSError:
         pass
+    try:   # Arm hosts list no model name in /proc/cpuinfo; lscpu decodes the part number
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            key, _, val = line.partition(":")
+            if key.strip() == "Model name" and val.strip():
+                return val.strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
     import platform
     return platform.processor() or platform.machine()
 
