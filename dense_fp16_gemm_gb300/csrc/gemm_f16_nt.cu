@@ -857,6 +857,8 @@ EncodeTiledFn g_encode = nullptr;
 std::atomic<uint64_t> g_launch_seq{0};
 
 constexpr int kMinSplitKb = 8;   // smallest stream-K share worth its fix-up, in k-blocks
+constexpr int kSmallSplitGainKb = 32;   // k-blocks a split must save each cluster (fewer tiles than clusters)
+constexpr int kMaxPiecesPerTile = 4;    // ... and the pieces it may cut one tile into
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -1083,10 +1085,20 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
             if (sched == 2 || worth) sk_tiles = rem + resident;
             if (sk_tiles > tiles) sk_tiles = tiles;
         } else {
+            // Fewer tiles than clusters: spreading them over g clusters saves each
+            // cluster kb·(1 - tiles/g) k-blocks but costs the fix-up, in which a
+            // tile's owner adds its partners' partials one after another.  So a
+            // tile is cut into at most kMaxPiecesPerTile pieces, and only for deep
+            // k.  Measured with L2 flushed: 1024^3 (16 tiles of 16 k-blocks over
+            // 32 clusters) 22.3 us split against 16.8 us whole; 2048^3 31.7
+            // against 21.3; one 256x256x4096 tile over 8 clusters 32.5 against
+            // 29.2, over 64 clusters 134 us.
             int64_t g = tiles * kb / kMinSplitKb;      // clusters that still get kMinSplitKb each
+            if (sched != 2 && g > kMaxPiecesPerTile * tiles) g = kMaxPiecesPerTile * tiles;
             if (sched == 2) g = tiles * kb;            // forced: up to one k-block each
             if (g > resident) g = resident;
-            if (g > tiles) {
+            const bool worth = sched == 2 || kb * (g - tiles) >= kSmallSplitGainKb * g;
+            if (g > tiles && worth) {
                 clusters = g;
                 sk_tiles = tiles;
             }

@@ -125,10 +125,19 @@ def test_plan_stream_k_schedule():
     assert (p["sk_tiles"], p["tail_split"]) == (0, 1)
     p = g.plan(256 * 15, 256 * 10, 4096, num_sms=152)     # 150 tiles: last wave 74/76 full
     assert (p["sk_tiles"], p["tail_split"]) == (0, 1)
-    # fewer tiles than pairs: spread when each share keeps >= 8 k-blocks
+    # fewer tiles than pairs: split in k only for deep k, at most 4 pieces a tile,
+    # and only if each cluster is spared >= 32 k-blocks
     one = g.Options(cluster_pairs=1)
-    p = g.plan(1000, 700, 1000, options=one)              # 12 tiles x 16 k-blocks
-    assert (p["sk_tiles"], p["clusters"], p["tail_split"]) == (12, 24, 1)
+    p = g.plan(1024, 1024, 8192, options=one)             # 16 tiles x 128 k-blocks
+    assert (p["sk_tiles"], p["clusters"], p["tail_split"]) == (16, 64, 1)
+    p = g.plan(256, 256, 8192, options=one)               # 1 tile x 128 k-blocks: 4 pieces
+    assert (p["sk_tiles"], p["clusters"]) == (1, 4)
+    p = g.plan(1024, 1024, 1024, options=one)             # 16 x 16 k-blocks: not worth it
+    assert (p["sk_tiles"], p["tail_split"]) == (0, 4)
+    p = g.plan(2048, 2048, 2048, options=one)             # 64 x 32 k-blocks: not worth it
+    assert (p["sk_tiles"], p["clusters"]) == (0, 64)
+    p = g.plan(1000, 700, 1000, options=one)              # 12 x 16 k-blocks: N-split instead
+    assert (p["sk_tiles"], p["clusters"], p["tail_split"]) == (0, 48, 4)
     p = g.plan(256, 256, 4096, options=g.Options(schedule=2))   # forced: one k-block per pair
     assert (p["sk_tiles"], p["clusters"]) == (1, 64)
     with pytest.raises(g.GemmError):

@@ -30,7 +30,7 @@ def _call(fn, A, B, C, stream):
 
 
 @pytest.mark.parametrize("M,N,K,uses_scratch", [
-    (1000, 704, 1000, True),      # 12 pair tiles split in k over 24 pairs
+    (1024, 1024, 8192, True),     # 16 pair tiles split in k over 64 pairs
     (3584, 2304, 2048, True),     # 126 tiles: last wave 50/76 full, 17 % of slots idle: stream-K part
     (300, 520, 328, False),       # whole tiles, no scratch needed
 ])
