@@ -158,11 +158,14 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  *   schedule      0 (default): whole tiles round-robin over the persistent
  *                 clusters, except that when at least 10 % of that schedule's
  *                 tile slots would sit idle in its last wave (one pair per
- *                 cluster), or when there are fewer tiles than clusters, the
- *                 k-block work of the last wave plus one full wave (or of all
- *                 tiles) is split evenly across all clusters (stream-K),
- *                 with fp32 partial tiles summed by each tile's first piece in
- *                 a fixed order (results are reproducible run to run);
+ *                 cluster), the k-block work of the last wave plus one full
+ *                 wave is split evenly across all clusters (stream-K), with
+ *                 fp32 partial tiles summed by each tile's first piece in a
+ *                 fixed order (results are reproducible run to run).  With
+ *                 fewer tiles than clusters the tiles are split in k the same
+ *                 way only for deep k: at most 4 pieces a tile, and only when
+ *                 that spares each cluster at least 32 k-blocks (otherwise the
+ *                 N-split below applies);
  *                 1: whole tiles only; 2: stream-K whenever possible (tests);
  *                 3: N-split whenever possible (tests).
  *                 N-split: when there are fewer tiles than clusters and the
