@@ -859,6 +859,7 @@ std::atomic<uint64_t> g_launch_seq{0};
 constexpr int kMinSplitKb = 8;   // smallest stream-K share worth its fix-up, in k-blocks
 constexpr int kSmallSplitGainKb = 32;   // k-blocks a split must save each cluster (fewer tiles than clusters)
 constexpr int kMaxPiecesPerTile = 4;    // ... and the pieces it may cut one tile into
+constexpr int kSplitTailMaxKb = 32;     // deepest k for which the default N-splits a last wave
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -1079,9 +1080,18 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
     // fp16 accumulators, a different rounding sequence.
     if (allow_split_k && tiles > 0 && kb > 0 && sched != 1 && sched != 3 && acc == 0) {
         if (tiles >= resident) {
+            // Split only if it spares each cluster >= kSmallSplitGainKb k-blocks
+            // (kb·(rounds - tiles/clusters) of them) and at least one full wave
+            // of whole tiles remains.  Measured with L2 flushed: 4096^3 (64
+            // k-blocks, 256 tiles) 84.9 us split against 90.2 whole; but
+            // 4096x4096x1024 (16 k-blocks) 36.7 against 33.5, 3584x2304x2048
+            // (32) 36.2 against 31.5, and 2048x4096x8192 (128 tiles, all split)
+            // 99.9 against 90.6.
             const int64_t rem = tiles % resident;
             const int64_t slots = (tiles + resident - 1) / resident * resident;
-            const bool worth = rem != 0 && cp == 1 && (slots - tiles) * 10 >= slots && kb >= kMinSplitKb;
+            const bool deep = kb * (slots - tiles) >= kSmallSplitGainKb * resident;
+            const bool worth = rem != 0 && cp == 1 && (slots - tiles) * 10 >= slots && kb >= kMinSplitKb &&
+                               deep && tiles >= 2 * resident;
             if (sched == 2 || worth) sk_tiles = rem + resident;
             if (sk_tiles > tiles) sk_tiles = tiles;
         } else {
@@ -1104,17 +1114,19 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
             }
         }
     }
-    // N-split: with fewer tiles than clusters and no stream-K split (too few
-    // k-blocks for one to pay), each tile is cut into s = 2 or 4 column slices
-    // (the largest with tiles·s <= clusters) that run on their own pairs.  A
-    // narrower MMA takes no fewer cycles per k-block on these tensor cores, so
-    // this cannot shorten a compute-bound wave; what it shortens is each
-    // cluster's epilogue, which is most of a small problem's time.  With 3 it
-    // is also used for the last wave of a larger problem (tests).  One pair per
-    // cluster and B stored [N, K] only.
+    // N-split: with no stream-K split, the R tiles of a last wave that fills at
+    // most half of the clusters (all tiles, with fewer tiles than clusters) are
+    // each cut into s = 2 or 4 column slices (the largest with R·s <= clusters)
+    // that run on their own pairs.  A narrower MMA takes no fewer cycles per
+    // k-block on these tensor cores, so this cannot shorten a compute-bound
+    // wave; what it shortens is each cluster's epilogue.  So the default uses
+    // it for small problems, and for the last wave only when k is shallow:
+    // 4096x4096x1024 ran 31.2 us against 33.5 whole, while at 8192^3 the split
+    // last wave measured 693.8 against 688.8 us.  One pair per cluster and B
+    // stored [N, K] only.
     const bool can_split = cg == 2 && cp == 1 && !(o && o->b_layout == 1);
     if (sk_tiles == 0 && tiles > 0 && kb > 0 && can_split &&
-        ((sched == 0 && tiles < resident) || sched == 3)) {
+        ((sched == 0 && (tiles < resident || kb <= kSplitTailMaxKb)) || sched == 3)) {
         const int64_t R = tiles % resident;          // all tiles when tiles < resident
         int64_t s = 1;
         while (s < 4 && R > 0 && R * s * 2 <= resident) s *= 2;

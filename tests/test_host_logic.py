@@ -114,6 +114,15 @@ def test_plan_stream_k_schedule():
     p = g.plan(4096, 4096, 4096, num_sms=152)
     assert p["sk_tiles"] == 28 + 76 and p["tail_split"] == 1
     assert p["workspace_bytes"] == 76 * 2 * 4 * 8 + 76 * 2 * 128 * 256 * 4
+    # ... only for deep k (each cluster spared >= 32 k-blocks) and with a full
+    # wave of whole tiles left; shallow last waves take the N-split instead
+    assert g.plan(6144, 4096, 4096, num_sms=152)["sk_tiles"] == 4 + 76
+    p = g.plan(4096, 4096, 1024, num_sms=152)             # 16 k-blocks
+    assert (p["sk_tiles"], p["tail_split"], p["tail_tiles"]) == (0, 2, 28)
+    p = g.plan(3584, 2304, 2048, num_sms=152)             # 32 k-blocks, 126 tiles
+    assert (p["sk_tiles"], p["tail_split"]) == (0, 1)
+    p = g.plan(2048, 4096, 8192, num_sms=152)             # 128 tiles: no full wave would stay whole
+    assert (p["sk_tiles"], p["tail_split"]) == (0, 1)
     # 8192^3: 40 of 1064 slots (3.8 %) idle: whole tiles, unless forced
     assert g.plan(8192, 8192, 8192, num_sms=152)["sk_tiles"] == 0
     assert g.plan(8192, 8192, 8192, num_sms=152)["tail_split"] == 1

@@ -31,7 +31,7 @@ def _call(fn, A, B, C, stream):
 
 @pytest.mark.parametrize("M,N,K,uses_scratch", [
     (1024, 1024, 8192, True),     # 16 pair tiles split in k over 64 pairs
-    (3584, 2304, 2048, True),     # 126 tiles: last wave 50/76 full, 17 % of slots idle: stream-K part
+    (6144, 4096, 4096, True),     # 384 tiles: last wave 4/76 full, deep k: stream-K part
     (300, 520, 328, False),       # whole tiles, no scratch needed
 ])
 def test_noalloc_matches_gemm_f16_nt_on_two_calls(M, N, K, uses_scratch):
