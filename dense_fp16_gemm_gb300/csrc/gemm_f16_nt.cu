@@ -857,8 +857,10 @@ EncodeTiledFn g_encode = nullptr;
 std::atomic<uint64_t> g_launch_seq{0};
 
 constexpr int kMinSplitKb = 8;   // smallest stream-K share worth its fix-up, in k-blocks
-constexpr int kSmallSplitGainKb = 32;   // k-blocks a split must save each cluster (fewer tiles than clusters)
+constexpr int kTailSplitGainKb = 32;    // k-blocks a split of the last wave must save each cluster
+constexpr int kSmallSplitGainKb = 64;   // the same with fewer tiles than clusters ...
 constexpr int kMaxPiecesPerTile = 4;    // ... and the pieces it may cut one tile into
+constexpr int kTailSplitIdlePct = 8;    // idle tile slots (%) above which the last wave may be split
 constexpr int kSplitTailMaxKb = 32;     // deepest k for which the default N-splits a last wave
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -1068,11 +1070,13 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
     // k-block units of (the partial wave + one full wave) evenly instead; with
     // fewer tiles than clusters it spreads all of them.  Splitting costs fp32
     // partial tiles through L2 (and DRAM), so auto mode (0) splits only when at
-    // least 10 % of the whole-tile schedule's tile slots would sit idle, with one
-    // pair per cluster (two-pair clusters are picked when L2 traffic already
-    // limits), and every share keeps at least kMinSplitKb k-blocks.  Measured on
-    // GB300: 4096^3 (16 % idle) gains 5.6 %; 8192^3 (3.8 % idle, power-capped)
-    // loses 1.4 % when split.  1 = whole tiles only; 2 = stream-K whenever it can.
+    // least kTailSplitIdlePct % of the whole-tile schedule's tile slots would sit
+    // idle, with one pair per cluster (two-pair clusters are picked when L2
+    // traffic already limits), and every share keeps at least kMinSplitKb
+    // k-blocks.  Measured on GB300: 4096^3 (16 % idle) gains 5.6 %,
+    // 4096x11008x4096 (9.5 %) 3 %; 6144^3 (5.3 %) ties; 8192^3 (3.8 % idle,
+    // power-capped) loses 1.4 % when split.  1 = whole tiles only; 2 = stream-K
+    // whenever it can; 3 = N-split whenever it can.
     const int64_t kb = pl->k_blocks;
     int64_t clusters = tiles < resident ? tiles : resident;
     int64_t sk_tiles = 0, tail_tiles = 0, tail_split = 1;
@@ -1089,9 +1093,9 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
             // 99.9 against 90.6.
             const int64_t rem = tiles % resident;
             const int64_t slots = (tiles + resident - 1) / resident * resident;
-            const bool deep = kb * (slots - tiles) >= kSmallSplitGainKb * resident;
-            const bool worth = rem != 0 && cp == 1 && (slots - tiles) * 10 >= slots && kb >= kMinSplitKb &&
-                               deep && tiles >= 2 * resident;
+            const bool deep = kb * (slots - tiles) >= kTailSplitGainKb * resident;
+            const bool worth = rem != 0 && cp == 1 && (slots - tiles) * 100 >= kTailSplitIdlePct * slots &&
+                               kb >= kMinSplitKb && deep && tiles >= 2 * resident;
             if (sched == 2 || worth) sk_tiles = rem + resident;
             if (sk_tiles > tiles) sk_tiles = tiles;
         } else {
@@ -1102,7 +1106,9 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
             // k.  Measured with L2 flushed: 1024^3 (16 tiles of 16 k-blocks over
             // 32 clusters) 22.3 us split against 16.8 us whole; 2048^3 31.7
             // against 21.3; one 256x256x4096 tile over 8 clusters 32.5 against
-            // 29.2, over 64 clusters 134 us.
+            // 29.2, over 64 clusters 134 us; 512x4096x4096 (37 k-blocks spared)
+            // 35.4 against 29.0, while 1024x1024x8192 (96 spared) 35.5 against
+            // 45.3.
             int64_t g = tiles * kb / kMinSplitKb;      // clusters that still get kMinSplitKb each
             if (sched != 2 && g > kMaxPiecesPerTile * tiles) g = kMaxPiecesPerTile * tiles;
             if (sched == 2) g = tiles * kb;            // forced: up to one k-block each

@@ -156,7 +156,7 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  *                 sets the watchdog word, releases its tensor memory and
  *                 exits without writing C.
  *   schedule      0 (default): whole tiles round-robin over the persistent
- *                 clusters, except that when at least 10 % of that schedule's
+ *                 clusters, except that when at least 8 % of that schedule's
  *                 tile slots would sit idle in its last wave (one pair per
  *                 cluster), the k-block work of the last wave plus one full
  *                 wave is split evenly across all clusters (stream-K), with
@@ -164,8 +164,10 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  *                 fixed order (results are reproducible run to run).  With
  *                 fewer tiles than clusters the tiles are split in k the same
  *                 way only for deep k: at most 4 pieces a tile, and only when
- *                 that spares each cluster at least 32 k-blocks (otherwise the
- *                 N-split below applies);
+ *                 that spares each cluster at least 64 k-blocks (otherwise the
+ *                 N-split below applies).  The last-wave split, too, needs deep
+ *                 k (at least 32 k-blocks spared a cluster) and at least one
+ *                 full wave of whole tiles beside it;
  *                 1: whole tiles only; 2: stream-K whenever possible (tests);
  *                 3: N-split whenever possible (tests).
  *                 N-split: when there are fewer tiles than clusters and the

@@ -32,7 +32,7 @@ def _operands(M, N, K, seed):
     return A, B
 
 
-@pytest.mark.parametrize("M,N,K", [(1024, 1024, 8192), (256, 256, 4096)])
+@pytest.mark.parametrize("M,N,K", [(1024, 1024, 8192), (256, 256, 8192)])
 def test_captured_gemm_replays_with_new_inputs(M, N, K):
     lim = g.device_limits()
     assert g.plan(M, N, K, num_sms=lim["sms"], max_clusters=lim["resident_pairs"])["sk_tiles"] > 0

@@ -117,6 +117,9 @@ def test_plan_stream_k_schedule():
     # ... only for deep k (each cluster spared >= 32 k-blocks) and with a full
     # wave of whole tiles left; shallow last waves take the N-split instead
     assert g.plan(6144, 4096, 4096, num_sms=152)["sk_tiles"] == 4 + 76
+    assert g.plan(4096, 11008, 4096, num_sms=152)["sk_tiles"] == 4 + 76   # 9.5 % of slots idle
+    p = g.plan(512, 4096, 4096, num_sms=152)              # 32 tiles: only 37 k-blocks spared
+    assert (p["sk_tiles"], p["tail_split"]) == (0, 2)
     p = g.plan(4096, 4096, 1024, num_sms=152)             # 16 k-blocks
     assert (p["sk_tiles"], p["tail_split"], p["tail_tiles"]) == (0, 2, 28)
     p = g.plan(3584, 2304, 2048, num_sms=152)             # 32 k-blocks, 126 tiles
