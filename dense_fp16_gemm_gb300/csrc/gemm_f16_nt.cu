@@ -267,9 +267,9 @@ __device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr) {
 // After the whole tiles come the N-split items: the last tiles of the raster,
 // [tail_first, num_tiles), each cut into tail_split column slices of
 // BN/tail_split, dealt round-robin like the whole tiles.  No cluster depends
-// on another's result.  A slice's main loop is as long as a whole tile's (a
-// narrower MMA is not faster per k-block); its epilogue drains 1/tail_split of
-// the accumulator.
+// on another's result.  A slice's main loop is nearly as long as a whole tile's
+// (a narrower MMA is not proportionally faster); its epilogue drains
+// 1/tail_split of the accumulator.
 
 struct Item {
     uint32_t tile;
@@ -688,6 +688,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                 ptx::tmem_ld_32x32b_x32(tacc + uint32_t(c * kEpiCols), lo);
                 ptx::tmem_ld_32x32b_x32(tacc + uint32_t(c * kEpiCols + 32), hi);
                 ptx::tmem_wait_ld();
+                ptx::reg_fence(lo);
+                ptx::reg_fence(hi);
                 if (c == nchunks - 1) {
                     // The whole accumulator is in registers: hand the buffer back.
                     ptx::tc_fence_before();
@@ -1123,9 +1125,11 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
     // N-split: with no stream-K split, the R tiles of a last wave that fills at
     // most half of the clusters (all tiles, with fewer tiles than clusters) are
     // each cut into s = 2 or 4 column slices (the largest with R·s <= clusters)
-    // that run on their own pairs.  A narrower MMA takes no fewer cycles per
-    // k-block on these tensor cores, so this cannot shorten a compute-bound
-    // wave; what it shortens is each cluster's epilogue.  So the default uses
+    // that run on their own pairs.  A narrower MMA is not proportionally faster
+    // (with no loads, N = 128 takes 69 % and N = 64 62 % of the 256-wide time
+    // per k-block), and with their loads split slices measured no faster than
+    // whole tiles, so this does not shorten a compute-bound wave; what it
+    // shortens is each cluster's epilogue.  So the default uses
     // it for small problems, and for the last wave only when k is shallow:
     // 4096x4096x1024 ran 31.2 us against 33.5 whole, while at 8192^3 the split
     // last wave measured 693.8 against 688.8 us.  One pair per cluster and B

@@ -175,9 +175,12 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  *                 tile is cut along N into s = 2 or 4 narrower tiles (256×128
  *                 or 256×64, s the largest with tiles·s <= clusters) that run
  *                 on their own CTA pairs; nothing is summed across clusters.
- *                 A narrower MMA takes no fewer cycles per k-block on these
- *                 tensor cores, so this shortens each cluster's epilogue, not
- *                 its main loop: it is for small, latency-bound problems.
+ *                 A narrower MMA is not proportionally faster on these tensor
+ *                 cores (with no loads, N = 128 takes 69 % and N = 64 62 % of
+ *                 the 256-wide time per k-block), and with their operand loads
+ *                 the slices measured no faster than whole tiles, so this
+ *                 mainly shortens each cluster's epilogue: it is for small,
+ *                 latency-bound problems.
  *                 With 3 the last R tiles of a larger problem are cut the same
  *                 way when 2R <= clusters.  Only with one CTA pair per cluster
  *                 and B stored [N, K].
