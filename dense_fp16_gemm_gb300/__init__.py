@@ -15,6 +15,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import threading
 
 from . import _build_ext
 
@@ -68,11 +69,22 @@ class Plan(ctypes.Structure):
 
 
 _lib = None
+_lib_lock = threading.Lock()
 _i64, _i32, _u32, _p = ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32, ctypes.c_void_p
 
 
 def library(path: str | None = None):
-    """Load the C-ABI library (building it first if the sources are newer)."""
+    """Load the C-ABI library (building it first if the sources are newer).
+
+    Thread-safe: the first caller builds and loads it, the others wait."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lib_lock:
+        return _load_library(path)
+
+
+def _load_library(path: str | None):
     global _lib
     if _lib is None:
         if path is None:
