@@ -52,7 +52,9 @@ G16_HD uint32_t fastdiv_q(const FastDiv& f, uint32_t n) {
 // persistent grid, therefore share a few B column strips and a few A row
 // strips, and those stay in L2.  Tilus matmul-hopper tutorial, "4. Pipeline
 // Abstraction and Two Consumer Warp Groups", §Tile Rasterization (the mapping
-// and its narrower last group).
+// and its narrower last group).  One change to it: odd groups take their rows
+// in reverse (a serpentine), so that a group starts on the A row strips the
+// previous group's last wave has just read, instead of on rows read long ago.
 struct Raster {
     uint32_t m_tiles;
     uint32_t n_tiles;
@@ -83,7 +85,7 @@ G16_HD void raster_coord(const Raster& r, uint32_t t, uint32_t& m_tile, uint32_t
     uint32_t first_n = g * r.swizzle;
     const FastDiv& w = (first_n + r.swizzle <= r.n_tiles) ? r.full : r.last;
     uint32_t mm = fastdiv_q(w, in);
-    m_tile = mm;
+    m_tile = (g & 1u) ? r.m_tiles - 1u - mm : mm;
     n_tile = first_n + (in - mm * w.d);
 }
 

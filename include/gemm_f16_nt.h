@@ -352,9 +352,11 @@ gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms,
 /*
  * The tile raster: linear tile index -> (m_tile, n_tile).  N tiles are taken
  * in groups of `swizzle` columns (the last group may be narrower); inside a
- * group tiles go row-major.  A bijection of [0, m_tiles·n_tiles) onto the
- * grid (Tilus tutorial "4. Pipeline Abstraction and Two Consumer Warp
- * Groups", §Tile Rasterization).  This is the same function the kernel runs.
+ * group tiles go row-major (Tilus tutorial "4. Pipeline Abstraction and Two
+ * Consumer Warp Groups", §Tile Rasterization), with rows taken in reverse in
+ * odd groups, so that each group starts on the row strips where the one
+ * before it ended.  A bijection of [0, m_tiles·n_tiles) onto the grid.  This
+ * is the same function the kernel runs.
  */
 gemm_status_t gemm_f16_nt_tile_coord(int64_t linear, int32_t m_tiles, int32_t n_tiles,
                                      int32_t swizzle, int32_t *m_tile, int32_t *n_tile);

@@ -79,11 +79,23 @@ def test_raster_is_bijection(sw):
 
 
 def test_raster_groups_are_row_major_with_narrow_last_group():
-    # 5 x 7 grid, groups of 3 columns: groups {0,1,2}, {3,4,5}, {6} (narrower)
+    # 5 x 7 grid, groups of 3 columns: groups {0,1,2}, {3,4,5}, {6} (narrower);
+    # the odd group takes its rows from the bottom up
     order = [g.tile_coord(t, 5, 7, 3) for t in range(35)]
     assert order[:6] == [(0, 0), (0, 1), (0, 2), (1, 0), (1, 1), (1, 2)]
-    assert order[15:18] == [(0, 3), (0, 4), (0, 5)]
+    assert order[15:21] == [(4, 3), (4, 4), (4, 5), (3, 3), (3, 4), (3, 5)]
+    assert order[27:30] == [(0, 3), (0, 4), (0, 5)]
     assert order[30:] == [(0, 6), (1, 6), (2, 6), (3, 6), (4, 6)]
+
+
+@pytest.mark.parametrize("mt,nt,sw", [(32, 32, 8), (64, 56, 8), (7, 20, 3), (9, 5, 2)])
+def test_raster_groups_meet_on_the_same_rows(mt, nt, sw):
+    # serpentine: the last tile of a group and the first of the next share a row
+    order = [g.tile_coord(t, mt, nt, sw) for t in range(mt * nt)]
+    starts = [t for t in range(1, mt * nt) if order[t][1] // sw != order[t - 1][1] // sw]
+    assert starts
+    for t in starts:
+        assert order[t][0] == order[t - 1][0], (t, order[t - 1], order[t])
 
 
 def test_raster_reproduces_the_pages_wave_example():
