@@ -144,8 +144,8 @@ def recorded_traffic(workload: str):
 
 
 class ClockSampler:
-    """Samples the SM clock, its maximum, board power and the clock-event
-    (throttle) reasons while the timed region runs.  Reads only: it queries
+    """Samples the SM clock, its maximum, board power (NVML's one-second
+    average) and the clock-event (throttle) reasons while the timed region runs.  Reads only: it queries
     NVML through ctypes (libnvidia-ml ships with the driver) every few ms from a
     background thread, and falls back to `nvidia-smi -lms` if NVML cannot be
     loaded.  Each sample carries a host timestamp so that only samples taken
@@ -249,7 +249,10 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(s[1] for s in inside),
                 "sm_mhz_min": min(s[1] for s in inside),
                 "sm_max_mhz": max(s[2] for s in inside), "reasons": sorted(reasons),
-                "samples": len(inside), "power_w_median": statistics.median(s[3] for s in inside),
+                "samples": len(inside),
+                # NVML reports board power averaged over the last second, so a
+                # region shorter than that also counts the idle time before it
+                "power_w_1s_average_median": statistics.median(s[3] for s in inside),
                 "source": "nvml" if self._nvml else "nvidia-smi"}
 
 
