@@ -146,7 +146,8 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  *                 in a group are visited row-major so that concurrently
  *                 running tiles share B columns in L2 (Tilus tutorial
  *                 "4. Pipeline Abstraction and Two Consumer Warp Groups",
- *                 §Tile Rasterization).  Range 1..64.
+ *                 §Tile Rasterization), odd groups from the last row up
+ *                 (see gemm_f16_nt_tile_coord).  Range 1..64; default 8.
  *   max_clusters  upper bound on the persistent grid, in CTA pairs (or CTAs
  *                 for cta_group 1); 0 = as many as can be resident.
  *   timeout_ns    watchdog limit for any single pipeline wait, in ns
