@@ -19,8 +19,8 @@ import threading
 
 from . import _build_ext
 
-__all__ = ["gemm_f16_nt", "gemm_bf16_nt", "gemm_f16_nt_ptr", "device_status", "device_limits", "plan", "tile_coord",
-           "fast_divmod", "GemmError", "Options", "Plan", "library", "STATUS"]
+__all__ = ["gemm_f16_nt", "gemm_bf16_nt", "gemm_f16_nt_ptr", "device_status", "device_limits", "plan", "schedule",
+           "tile_coord", "fast_divmod", "GemmError", "Options", "Plan", "Item", "library", "STATUS"]
 
 STATUS = {
     0: "GEMM_OK",
@@ -63,6 +63,16 @@ class Plan(ctypes.Structure):
                 ("sk_tiles", ctypes.c_int32), ("cluster_pairs", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("tail_tiles", ctypes.c_int32),
                 ("tail_split", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+class Item(ctypes.Structure):
+    """gemm_f16_nt_item_t: one work item of a persistent cluster."""
+    _fields_ = [("tile", ctypes.c_int32), ("m_tile", ctypes.c_int32), ("n_tile", ctypes.c_int32),
+                ("kb0", ctypes.c_int32), ("kb1", ctypes.c_int32), ("kind", ctypes.c_int32),
+                ("part", ctypes.c_int32), ("parts", ctypes.c_int32), ("partners", ctypes.c_int32)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -112,6 +122,9 @@ def _load_library(path: str | None):
         lib.gemm_f16_nt_plan.argtypes = [_i64, _i64, _i64, _i32, _i32, ctypes.POINTER(Options),
                                          ctypes.POINTER(Plan)]
         lib.gemm_f16_nt_plan.restype = ctypes.c_int
+        lib.gemm_f16_nt_schedule.argtypes = [_i64, _i64, _i64, _i32, _i32, ctypes.POINTER(Options), _i32,
+                                             ctypes.POINTER(Item), _i32, ctypes.POINTER(_i32)]
+        lib.gemm_f16_nt_schedule.restype = ctypes.c_int
         lib.gemm_f16_nt_tile_coord.argtypes = [_i64, _i32, _i32, _i32, ctypes.POINTER(_i32),
                                                ctypes.POINTER(_i32)]
         lib.gemm_f16_nt_tile_coord.restype = ctypes.c_int
@@ -239,6 +252,21 @@ def plan(M: int, N: int, K: int, num_sms: int = 152, max_clusters: int = 0,
                                     ctypes.byref(out))
     _check(st, "gemm_f16_nt_plan")
     return out.as_dict()
+
+
+def schedule(M: int, N: int, K: int, cluster: int, num_sms: int = 152, max_clusters: int = 0,
+             options: Options | None = None) -> list:
+    """The work items persistent cluster `cluster` runs, in order, as dicts
+    (host computation with the kernel's own schedule code; no GPU needed)."""
+    lib = library()
+    opt = ctypes.byref(options) if options is not None else None
+    n = _i32(0)
+    _check(lib.gemm_f16_nt_schedule(M, N, K, num_sms, max_clusters, opt, cluster, None, 0, ctypes.byref(n)),
+           "gemm_f16_nt_schedule")
+    items = (Item * max(1, n.value))()
+    _check(lib.gemm_f16_nt_schedule(M, N, K, num_sms, max_clusters, opt, cluster, items, n.value,
+                                    ctypes.byref(n)), "gemm_f16_nt_schedule")
+    return [items[i].as_dict() for i in range(n.value)]
 
 
 def tile_coord(linear: int, m_tiles: int, n_tiles: int, swizzle: int):

@@ -78,9 +78,6 @@ enum : uint32_t {
     kSiteStreamK = 7,
 };
 
-// Work items (see work_next)
-enum : uint32_t { kItemWhole = 0, kItemPartialOut = 1, kItemOwner = 2 };
-
 __device__ uint32_t g_watchdog_word;
 
 template <int CG, int BN, int STAGES, int CP = 1, bool BF = false, bool A16 = false>
@@ -242,94 +239,6 @@ constexpr uint32_t kMnBoxBytes = 64 * 64 * 2;
 __device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr) {
     return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(kMnBoxBytes >> 4) << 16) |
            (uint64_t(1024 >> 4) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
-}
-
-// ---------------------------------------------------------------------------
-// work schedule
-// ---------------------------------------------------------------------------
-//
-// The tiles [0, sk_tiles) form the stream-K part: their sk_tiles * num_kb
-// k-block units are split into G equal contiguous ranges, one per cluster, so
-// the last, partly filled wave of a purely tile-parallel schedule is spread
-// over every cluster.  The rest of the tiles go round-robin, whole.  A range
-// may start or end inside a tile:
-//   - a piece that does not start at k-block 0 (only ever a cluster's first
-//     item) is written as an fp32 partial tile to the cluster's workspace slot
-//     and published with a release flag; its k-blocks run from the last one
-//     down, so that all clusters' first pieces end at the same k-block;
-//   - the piece that starts at k-block 0 but stops early is the tile's owner:
-//     it waits for the partials of the clusters that took the rest of the tile
-//     (the next ones in order), adds them in that order and stores C.
-// Owner pieces come at the end of a cluster's range and partial pieces at the
-// start, so an owner seldom waits.
-
-//
-// After the whole tiles come the N-split items: the last tiles of the raster,
-// [tail_first, num_tiles), each cut into tail_split column slices of
-// BN/tail_split, dealt round-robin like the whole tiles.  No cluster depends
-// on another's result.  A slice's main loop is nearly as long as a whole tile's
-// (a narrower MMA is not proportionally faster); its epilogue drains
-// 1/tail_split of the accumulator.
-
-struct Item {
-    uint32_t tile;
-    uint32_t kb0, kb1;   // k-block range [kb0, kb1)
-    uint32_t kind;
-    uint32_t part, parts;   // column slice `part` of `parts` (1 = the whole tile)
-};
-
-struct Work {
-    uint64_t u, u_end;   // this cluster's stream-K units still to do
-    uint32_t t;          // next whole tile
-    uint32_t q;          // next N-split tail item
-    uint32_t G;          // clusters
-};
-
-__device__ __forceinline__ uint64_t sk_begin(const Params& p, uint32_t c, uint32_t G) {
-    return p.sk_units * c / G;
-}
-
-__device__ __forceinline__ void work_init(Work& s, const Params& p, uint32_t c, uint32_t G) {
-    s.u = sk_begin(p, c, G);
-    s.u_end = sk_begin(p, c + 1, G);
-    s.t = p.sk_tiles + c;
-    s.q = c;
-    s.G = G;
-}
-
-__device__ __forceinline__ bool work_next(Work& s, const Params& p, Item& it) {
-    if (s.u < s.u_end) {
-        const uint32_t t = uint32_t(s.u / p.num_kb);
-        const uint32_t kb0 = uint32_t(s.u - uint64_t(t) * p.num_kb);
-        const uint64_t left = s.u_end - s.u;
-        const uint32_t kb1 = left >= uint64_t(p.num_kb - kb0) ? p.num_kb : kb0 + uint32_t(left);
-        it.tile = t;
-        it.kb0 = kb0;
-        it.kb1 = kb1;
-        it.kind = kb0 > 0 ? kItemPartialOut : (kb1 < p.num_kb ? kItemOwner : kItemWhole);
-        it.part = 0;
-        it.parts = 1;
-        s.u += kb1 - kb0;
-        return true;
-    }
-    it.kb0 = 0;
-    it.kb1 = p.num_kb;
-    it.kind = kItemWhole;
-    if (s.t < p.tail_first) {
-        it.tile = s.t;
-        it.part = 0;
-        it.parts = 1;
-        s.t += s.G;
-        return true;
-    }
-    if (s.q < (p.num_tiles - p.tail_first) * p.tail_split) {
-        it.tile = p.tail_first + s.q / p.tail_split;
-        it.part = s.q % p.tail_split;
-        it.parts = p.tail_split;
-        s.q += s.G;
-        return true;
-    }
-    return false;
 }
 
 // Wait until *flag == want (the partner's release store); false on watchdog.
@@ -668,9 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
             // An owner adds the partials of the clusters that took the rest of its tile.
             uint32_t npart = 0;
             if (it.kind == kItemOwner) {
-                const uint64_t tile_end = uint64_t(it.tile + 1) * p.num_kb;
-                while (cluster + 1 + npart < nclusters && sk_begin(p, cluster + 1 + npart, nclusters) < tile_end)
-                    ++npart;
+                npart = owner_partners(p, it.tile, cluster, nclusters);
                 uint32_t okf = 1;
                 if (lane == 0)
                     for (uint32_t i = 0; i < npart && okf; ++i)
@@ -1193,8 +1100,7 @@ gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t
     p.C = C;
     p.ldc = ldc;
     p.raster = make_raster(uint32_t(pl.m_tiles), uint32_t(pl.n_tiles), uint32_t(pl.swizzle));
-    p.num_tiles = uint32_t(pl.num_tiles);
-    p.num_kb = uint32_t(pl.k_blocks);
+    set_schedule(p, pl);
     p.M = int32_t(M);
     p.N = int32_t(N);
     p.timeout_ns = (o && o->timeout_ns) ? o->timeout_ns : kDefaultTimeoutNs;
@@ -1202,16 +1108,12 @@ gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t
     p.inject_stall = o ? o->inject_stall : 0;
     p.a_mn = a_mn ? 1u : 0u;
     p.b_mn = b_mn ? 1u : 0u;
-    p.sk_tiles = uint32_t(pl.sk_tiles);
-    p.sk_units = uint64_t(pl.sk_tiles) * uint64_t(pl.k_blocks);
     if (pl.sk_tiles > 0) {
         uint8_t* ws = static_cast<uint8_t*>(workspace);
         p.flags = reinterpret_cast<uint64_t*>(ws);
         p.partials = reinterpret_cast<float*>(ws + flags_bytes(Cfg::kCtas, pl.clusters));
     }
     p.launch_id = ++g_launch_seq;
-    p.tail_split = uint32_t(pl.tail_split > 1 ? pl.tail_split : 1);
-    p.tail_first = uint32_t(pl.num_tiles - (pl.tail_split > 1 ? pl.tail_tiles : 0));
     if (pl.tail_split > 1 &&
         (b_mn || Cfg::kCP != 1 ||
          (s = encode_2d(&p.tmBp, dt, B, uint64_t(K), uint64_t(N), uint64_t(ldb), kBlockK,
@@ -1492,6 +1394,49 @@ G16_EXPORT gemm_status_t gemm_f16_nt_tile_coord(int64_t linear, int32_t m_tiles,
     g16::raster_coord(r, uint32_t(linear), m, n);
     *m_tile = int32_t(m);
     *n_tile = int32_t(n);
+    return GEMM_OK;
+}
+
+G16_EXPORT gemm_status_t gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t num_sms,
+                                              int32_t max_clusters, const gemm_f16_nt_options_t* opts,
+                                              int32_t cluster, gemm_f16_nt_item_t* items,
+                                              int32_t max_items, int32_t* n_items) {
+    if (!n_items || max_items < 0 || (max_items > 0 && !items)) return GEMM_ERR_INVALID_VALUE;
+    gemm_f16_nt_plan_t pl;
+    const gemm_status_t s = gemm_f16_nt_plan(M, N, K, num_sms, max_clusters, opts, &pl);
+    if (s != GEMM_OK) return s;
+    if (cluster < 0 || cluster >= pl.clusters) return GEMM_ERR_INVALID_VALUE;
+    // the launch's schedule fields, set exactly as the launch sets them
+    struct {
+        uint32_t num_tiles, num_kb, sk_tiles;
+        uint64_t sk_units;
+        uint32_t tail_first, tail_split;
+    } sp;
+    g16::set_schedule(sp, pl);
+    const g16::Raster r = g16::make_raster(uint32_t(pl.m_tiles), uint32_t(pl.n_tiles), uint32_t(pl.swizzle));
+    const uint32_t G = uint32_t(pl.clusters), c = uint32_t(cluster);
+    g16::Work w;
+    g16::Item it;
+    g16::work_init(w, sp, c, G);
+    int32_t n = 0;
+    while (g16::work_next(w, sp, it)) {
+        if (n < max_items) {
+            gemm_f16_nt_item_t& o = items[n];
+            uint32_t mt, nt;
+            g16::raster_coord(r, it.tile, mt, nt);
+            o.tile = int32_t(it.tile);
+            o.m_tile = int32_t(mt);
+            o.n_tile = int32_t(nt);
+            o.kb0 = int32_t(it.kb0);
+            o.kb1 = int32_t(it.kb1);
+            o.kind = int32_t(it.kind);
+            o.part = int32_t(it.part);
+            o.parts = int32_t(it.parts);
+            o.partners = it.kind == g16::kItemOwner ? int32_t(g16::owner_partners(sp, it.tile, c, G)) : 0;
+        }
+        ++n;
+    }
+    *n_items = n;
     return GEMM_OK;
 }
 

@@ -89,4 +89,123 @@ G16_HD void raster_coord(const Raster& r, uint32_t t, uint32_t& m_tile, uint32_t
     n_tile = first_n + (in - mm * w.d);
 }
 
+// Kinds of work item (see work_next)
+enum : uint32_t { kItemWhole = 0, kItemPartialOut = 1, kItemOwner = 2 };
+
+// ---------------------------------------------------------------------------
+// work schedule
+// ---------------------------------------------------------------------------
+// The functions below take the launch's parameters as any struct P with the
+// fields num_tiles, num_kb, sk_tiles, sk_units, tail_first and tail_split, so
+// that the host tests enumerate exactly the items the kernel runs.
+//
+// The tiles [0, sk_tiles) form the stream-K part: their sk_tiles * num_kb
+// k-block units are split into G equal contiguous ranges, one per cluster, so
+// the last, partly filled wave of a purely tile-parallel schedule is spread
+// over every cluster.  The rest of the tiles go round-robin, whole.  A range
+// may start or end inside a tile:
+//   - a piece that does not start at k-block 0 (only ever a cluster's first
+//     item) is written as an fp32 partial tile to the cluster's workspace slot
+//     and published with a release flag; its k-blocks run from the last one
+//     down, so that all clusters' first pieces end at the same k-block;
+//   - the piece that starts at k-block 0 but stops early is the tile's owner:
+//     it waits for the partials of the clusters that took the rest of the tile
+//     (the next ones in order), adds them in that order and stores C.
+// Owner pieces come at the end of a cluster's range and partial pieces at the
+// start, so an owner seldom waits.
+//
+// After the whole tiles come the N-split items: the last tiles of the raster,
+// [tail_first, num_tiles), each cut into tail_split column slices of
+// BN/tail_split, dealt round-robin like the whole tiles.  No cluster depends
+// on another's result.  A slice's main loop is nearly as long as a whole tile's
+// (a narrower MMA is not proportionally faster); its epilogue drains
+// 1/tail_split of the accumulator.
+
+struct Item {
+    uint32_t tile;
+    uint32_t kb0, kb1;   // k-block range [kb0, kb1)
+    uint32_t kind;
+    uint32_t part, parts;   // column slice `part` of `parts` (1 = the whole tile)
+};
+
+struct Work {
+    uint64_t u, u_end;   // this cluster's stream-K units still to do
+    uint32_t t;          // next whole tile
+    uint32_t q;          // next N-split tail item
+    uint32_t G;          // clusters
+};
+
+template <class P>
+G16_HD uint64_t sk_begin(const P& p, uint32_t c, uint32_t G) {
+    return p.sk_units * c / G;
+}
+
+template <class P>
+G16_HD void work_init(Work& s, const P& p, uint32_t c, uint32_t G) {
+    s.u = sk_begin(p, c, G);
+    s.u_end = sk_begin(p, c + 1, G);
+    s.t = p.sk_tiles + c;
+    s.q = c;
+    s.G = G;
+}
+
+template <class P>
+G16_HD bool work_next(Work& s, const P& p, Item& it) {
+    if (s.u < s.u_end) {
+        const uint32_t t = uint32_t(s.u / p.num_kb);
+        const uint32_t kb0 = uint32_t(s.u - uint64_t(t) * p.num_kb);
+        const uint64_t left = s.u_end - s.u;
+        const uint32_t kb1 = left >= uint64_t(p.num_kb - kb0) ? p.num_kb : kb0 + uint32_t(left);
+        it.tile = t;
+        it.kb0 = kb0;
+        it.kb1 = kb1;
+        it.kind = kb0 > 0 ? kItemPartialOut : (kb1 < p.num_kb ? kItemOwner : kItemWhole);
+        it.part = 0;
+        it.parts = 1;
+        s.u += kb1 - kb0;
+        return true;
+    }
+    it.kb0 = 0;
+    it.kb1 = p.num_kb;
+    it.kind = kItemWhole;
+    if (s.t < p.tail_first) {
+        it.tile = s.t;
+        it.part = 0;
+        it.parts = 1;
+        s.t += s.G;
+        return true;
+    }
+    if (s.q < (p.num_tiles - p.tail_first) * p.tail_split) {
+        it.tile = p.tail_first + s.q / p.tail_split;
+        it.part = s.q % p.tail_split;
+        it.parts = p.tail_split;
+        s.q += s.G;
+        return true;
+    }
+    return false;
+}
+
+// The number of clusters after cluster c whose stream-K ranges start inside
+// `tile`: the partners whose partial tiles the owner of `tile` (cluster c, the
+// piece from k-block 0) adds, in cluster order, which is k order.
+template <class P>
+G16_HD uint32_t owner_partners(const P& p, uint32_t tile, uint32_t c, uint32_t G) {
+    const uint64_t tile_end = uint64_t(tile + 1) * p.num_kb;
+    uint32_t n = 0;
+    while (c + 1 + n < G && sk_begin(p, c + 1 + n, G) < tile_end) ++n;
+    return n;
+}
+
+// The schedule fields of a launch's parameters, from its plan.  PlanT is the
+// library's plan struct; P any struct with the fields read above.
+template <class P, class PlanT>
+inline void set_schedule(P& p, const PlanT& pl) {
+    p.num_tiles = uint32_t(pl.num_tiles);
+    p.num_kb = uint32_t(pl.k_blocks);
+    p.sk_tiles = uint32_t(pl.sk_tiles);
+    p.sk_units = uint64_t(pl.sk_tiles) * uint64_t(pl.k_blocks);
+    p.tail_split = uint32_t(pl.tail_split > 1 ? pl.tail_split : 1);
+    p.tail_first = uint32_t(pl.num_tiles - (pl.tail_split > 1 ? pl.tail_tiles : 0));
+}
+
 }  // namespace g16

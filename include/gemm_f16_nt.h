@@ -351,6 +351,42 @@ gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms,
                                gemm_f16_nt_plan_t *plan);
 
 /*
+ * One work item of the persistent schedule (gemm_f16_nt_schedule).
+ */
+typedef struct {
+    int32_t tile;       /* linear index in the tile raster */
+    int32_t m_tile;     /* its coordinates (gemm_f16_nt_tile_coord); with two */
+    int32_t n_tile;     /*   CTA pairs per cluster, in 256×512 cluster tiles  */
+    int32_t kb0, kb1;   /* k-block range [kb0, kb1), 64 k per block           */
+    int32_t kind;       /* 0: whole k range; 1: stream-K piece that does not
+                           start at k-block 0 (written as an fp32 partial tile
+                           to the cluster's workspace slot); 2: stream-K piece
+                           from k-block 0 that ends early (the tile's owner:
+                           adds the partners' partials and stores C)          */
+    int32_t part;       /* column slice `part` of `parts` (N-split);          */
+    int32_t parts;      /*   parts = 1: the whole tile width                  */
+    int32_t partners;   /* kind 2: the number of following clusters whose
+                           partial pieces it adds, in cluster order; else 0   */
+} gemm_f16_nt_item_t;
+
+/*
+ * gemm_f16_nt_schedule — the work items, in order, that persistent cluster
+ * `cluster` of the launch gemm_f16_nt_ex(M, N, K, …, opts) would run on a GPU
+ * with `num_sms` SMs and at most `max_clusters` resident clusters (0: as many
+ * as fit), from the same plan (gemm_f16_nt_plan) and the same schedule code
+ * the kernel runs.  Host only, for tests and tools; no GPU is needed.
+ *   items      caller-owned array of max_items entries (may be NULL if 0);
+ *              the first min(n, max_items) items are written.
+ *   n_items    receives n, the cluster's total number of items.
+ * Returns GEMM_ERR_INVALID_VALUE for a bad argument or a cluster outside
+ * [0, plan.clusters), and the plan's error for an invalid problem.
+ */
+gemm_status_t gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t num_sms,
+                                   int32_t max_clusters, const gemm_f16_nt_options_t *opts,
+                                   int32_t cluster, gemm_f16_nt_item_t *items, int32_t max_items,
+                                   int32_t *n_items);
+
+/*
  * The tile raster: linear tile index -> (m_tile, n_tile).  N tiles are taken
  * in groups of `swizzle` columns (the last group may be narrower); inside a
  * group tiles go row-major (Tilus tutorial "4. Pipeline Abstraction and Two

@@ -1,0 +1,120 @@
+"""The persistent schedule, enumerated on the host with the kernel's own code.
+
+gemm_f16_nt_schedule runs the same work_init / work_next / owner_partners
+functions the kernel runs (they are compiled for both sides), from the same
+plan.  These tests check, for many shapes and options, what the kernel relies
+on without checking it itself:
+  - every (tile, column quarter, k-block) is computed exactly once;
+  - a cluster has at most one partial piece, and it is its first item (the
+    workspace holds one partial tile per cluster);
+  - a tile's owner adds exactly the partial pieces of that tile, and they are
+    held by the clusters right after it, in k order;
+  - the stream-K ranges are balanced across clusters to one k-block;
+  - each item's coordinates are the raster's.
+"""
+import pytest
+
+import dense_fp16_gemm_gb300 as g
+
+WHOLE, PARTIAL, OWNER = 0, 1, 2
+
+CASES = [
+    # M, N, K, options, max_clusters
+    (4096, 4096, 4096, {}, 76),                       # stream-K: last wave + one wave
+    (6144, 4096, 4096, {}, 76),
+    (4096, 11008, 4096, {}, 76),
+    (8192, 8192, 8192, {}, 76),                       # whole tiles
+    (8192, 8192, 8192, {"schedule": 2}, 76),          # stream-K forced
+    (8192, 8192, 8192, {"schedule": 3}, 76),          # N-split tail forced
+    (256, 256, 256, {}, 76),                          # N-split in four
+    (256, 256, 8192, {}, 76),                         # one tile cut in k
+    (1024, 1024, 8192, {}, 64),                       # 16 tiles cut in k
+    (1024, 1024, 1024, {}, 76),
+    (4096, 4096, 1024, {}, 76),                       # shallow last wave: N-split
+    (4000, 3000, 5000, {}, 36),                       # two pairs per cluster
+    (4000, 3000, 5000, {"schedule": 2, "cluster_pairs": 1}, 76),
+    (300, 520, 328, {"schedule": 2}, 76),
+    (1300, 1000, 320, {"schedule": 3, "cluster_pairs": 1}, 76),
+    (700, 900, 1000, {"cta_group": 1}, 152),
+    (700, 900, 1000, {"cta_group": 1, "schedule": 2}, 152),
+    (1, 1, 1, {}, 76),
+    (70000, 300, 64, {}, 76),
+    (256, 512, 1 << 20, {}, 76),
+]
+
+
+def _all_items(M, N, K, opts, max_clusters):
+    o = g.Options(**opts)
+    pl = g.plan(M, N, K, max_clusters=max_clusters, options=o)
+    items = [g.schedule(M, N, K, c, max_clusters=max_clusters, options=o) for c in range(pl["clusters"])]
+    return pl, items
+
+
+@pytest.mark.parametrize("M,N,K,opts,mc", CASES, ids=lambda v: str(v))
+def test_every_unit_exactly_once(M, N, K, opts, mc):
+    pl, items = _all_items(M, N, K, opts, mc)
+    kb = pl["k_blocks"]
+    seen = {}
+    for c, its in enumerate(items):
+        for it in its:
+            q = 4 // it["parts"]
+            for quarter in range(it["part"] * q, (it["part"] + 1) * q):
+                for k in range(it["kb0"], it["kb1"]):
+                    key = (it["tile"], quarter, k)
+                    assert key not in seen, (key, c, seen.get(key))
+                    seen[key] = c
+    assert len(seen) == pl["num_tiles"] * 4 * kb
+
+
+@pytest.mark.parametrize("M,N,K,opts,mc", CASES, ids=lambda v: str(v))
+def test_partial_pieces_and_owners(M, N, K, opts, mc):
+    pl, items = _all_items(M, N, K, opts, mc)
+    kb = pl["k_blocks"]
+    partial_of = {}                                   # tile -> [(cluster, kb0, kb1)]
+    for c, its in enumerate(items):
+        partials = [i for i, it in enumerate(its) if it["kind"] == PARTIAL]
+        assert partials in ([], [0]), (c, its)        # one workspace slot per cluster
+        for it in its:
+            if it["kind"] != WHOLE:
+                assert it["parts"] == 1 and it["tile"] < pl["sk_tiles"]
+            if it["kind"] == PARTIAL:
+                assert 0 < it["kb0"] < it["kb1"] <= kb     # a middle piece ends inside the tile
+                partial_of.setdefault(it["tile"], []).append((c, it["kb0"], it["kb1"]))
+            elif it["kind"] == OWNER:
+                assert it["kb0"] == 0 < it["kb1"] < kb
+            else:
+                assert (it["kb0"], it["kb1"]) == (0, kb) and it["partners"] == 0
+    owners = 0
+    for c, its in enumerate(items):
+        for it in its:
+            if it["kind"] != OWNER:
+                continue
+            owners += 1
+            parts = partial_of.pop(it["tile"])
+            assert [p[0] for p in parts] == list(range(c + 1, c + 1 + it["partners"]))
+            edges = [it["kb1"]] + [p[2] for p in parts]
+            assert [p[1] for p in parts] == edges[:-1] and edges[-1] == kb   # k order, no gap
+    assert not partial_of                              # every partial piece has an owner
+    if pl["sk_tiles"] == 0:
+        assert owners == 0
+
+
+@pytest.mark.parametrize("M,N,K,opts,mc", CASES, ids=lambda v: str(v))
+def test_stream_k_balance_and_coordinates(M, N, K, opts, mc):
+    pl, items = _all_items(M, N, K, opts, mc)
+    sk = [sum(it["kb1"] - it["kb0"] for it in its if it["tile"] < pl["sk_tiles"]) for its in items]
+    if pl["sk_tiles"]:
+        assert max(sk) - min(sk) <= 1
+        assert sum(sk) == pl["sk_tiles"] * pl["k_blocks"]
+    for its in items:
+        for it in its:
+            assert (it["m_tile"], it["n_tile"]) == g.tile_coord(it["tile"], pl["m_tiles"], pl["n_tiles"],
+                                                                pl["swizzle"])
+
+
+def test_schedule_rejects_a_cluster_out_of_range():
+    pl = g.plan(4096, 4096, 4096, max_clusters=76)
+    with pytest.raises(g.GemmError):
+        g.schedule(4096, 4096, 4096, pl["clusters"], max_clusters=76)
+    with pytest.raises(g.GemmError):
+        g.schedule(4096, 4096, 4096, -1, max_clusters=76)
