@@ -43,6 +43,25 @@ CASES = [
 ]
 
 
+def _random_cases(n=60, seed=20261203):
+    """Seeded random problems and options, sizes log-uniform in 1..20000 (K up to 2^17)."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    size = lambda hi: int(np.clip(np.round(np.exp(rng.uniform(0.0, np.log(hi)))), 1, hi))
+    out = []
+    for _ in range(n):
+        cg = 1 if rng.random() < 0.25 else 2
+        opts = {"cta_group": cg, "schedule": int(rng.choice([0, 0, 1, 2, 3]))}
+        if cg == 2:
+            opts["cluster_pairs"] = int(rng.choice([0, 1, 2]))
+        mc = int(rng.choice([0, 0, 7, 36, 64, 76, 152]))
+        out.append((size(20000), size(20000), size(1 << 17), opts, mc))
+    return out
+
+
+CASES = CASES + _random_cases()
+
+
 def _all_items(M, N, K, opts, max_clusters):
     o = g.Options(**opts)
     pl = g.plan(M, N, K, max_clusters=max_clusters, options=o)
