@@ -10,6 +10,7 @@ on without checking it itself:
   - a tile's owner adds exactly the partial pieces of that tile, and they are
     held by the clusters right after it, in k order;
   - the stream-K ranges are balanced across clusters to one k-block;
+  - the plan's N-split is what the clusters run;
   - each item's coordinates are the raster's.
 """
 import pytest
@@ -69,13 +70,17 @@ def _all_items(M, N, K, opts, max_clusters):
     return pl, items
 
 
-@pytest.mark.parametrize("M,N,K,opts,mc", CASES, ids=lambda v: str(v))
-def test_every_unit_exactly_once(M, N, K, opts, mc):
-    pl, items = _all_items(M, N, K, opts, mc)
+def check_coverage(pl, items):
+    """Every (tile, column quarter, k-block) exactly once; the plan's N-split realized."""
     kb = pl["k_blocks"]
     seen = {}
+    sliced = 0
     for c, its in enumerate(items):
         for it in its:
+            assert it["parts"] in (1, pl["tail_split"]), it
+            if it["parts"] > 1:
+                sliced += 1
+                assert it["tile"] >= pl["num_tiles"] - pl["tail_tiles"], it
             q = 4 // it["parts"]
             for quarter in range(it["part"] * q, (it["part"] + 1) * q):
                 for k in range(it["kb0"], it["kb1"]):
@@ -83,11 +88,12 @@ def test_every_unit_exactly_once(M, N, K, opts, mc):
                     assert key not in seen, (key, c, seen.get(key))
                     seen[key] = c
     assert len(seen) == pl["num_tiles"] * 4 * kb
+    assert sliced == (pl["tail_tiles"] * pl["tail_split"] if pl["tail_split"] > 1 else 0)
 
 
-@pytest.mark.parametrize("M,N,K,opts,mc", CASES, ids=lambda v: str(v))
-def test_partial_pieces_and_owners(M, N, K, opts, mc):
-    pl, items = _all_items(M, N, K, opts, mc)
+def check_partials_and_owners(pl, items):
+    """One partial piece per cluster at most, as its first item; owners add exactly
+    the partial pieces of their tile, held by the next clusters, contiguous in k."""
     kb = pl["k_blocks"]
     partial_of = {}                                   # tile -> [(cluster, kb0, kb1)]
     for c, its in enumerate(items):
@@ -118,17 +124,37 @@ def test_partial_pieces_and_owners(M, N, K, opts, mc):
         assert owners == 0
 
 
-@pytest.mark.parametrize("M,N,K,opts,mc", CASES, ids=lambda v: str(v))
-def test_stream_k_balance_and_coordinates(M, N, K, opts, mc):
-    pl, items = _all_items(M, N, K, opts, mc)
+def check_balance_and_coordinates(pl, items, tile_coord=g.tile_coord):
+    """Stream-K ranges balanced to one k-block; coordinates are the raster's."""
     sk = [sum(it["kb1"] - it["kb0"] for it in its if it["tile"] < pl["sk_tiles"]) for its in items]
     if pl["sk_tiles"]:
         assert max(sk) - min(sk) <= 1
         assert sum(sk) == pl["sk_tiles"] * pl["k_blocks"]
     for its in items:
         for it in its:
-            assert (it["m_tile"], it["n_tile"]) == g.tile_coord(it["tile"], pl["m_tiles"], pl["n_tiles"],
-                                                                pl["swizzle"])
+            assert (it["m_tile"], it["n_tile"]) == tile_coord(it["tile"], pl["m_tiles"], pl["n_tiles"],
+                                                              pl["swizzle"])
+
+
+def check_schedule(pl, items, tile_coord=g.tile_coord):
+    check_coverage(pl, items)
+    check_partials_and_owners(pl, items)
+    check_balance_and_coordinates(pl, items, tile_coord)
+
+
+@pytest.mark.parametrize("M,N,K,opts,mc", CASES, ids=lambda v: str(v))
+def test_every_unit_exactly_once(M, N, K, opts, mc):
+    check_coverage(*_all_items(M, N, K, opts, mc))
+
+
+@pytest.mark.parametrize("M,N,K,opts,mc", CASES, ids=lambda v: str(v))
+def test_partial_pieces_and_owners(M, N, K, opts, mc):
+    check_partials_and_owners(*_all_items(M, N, K, opts, mc))
+
+
+@pytest.mark.parametrize("M,N,K,opts,mc", CASES, ids=lambda v: str(v))
+def test_stream_k_balance_and_coordinates(M, N, K, opts, mc):
+    check_balance_and_coordinates(*_all_items(M, N, K, opts, mc))
 
 
 def test_schedule_rejects_a_cluster_out_of_range():
