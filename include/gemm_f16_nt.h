@@ -67,7 +67,7 @@ typedef enum {
  * The first call on a device performs one-time set-up on that device (device
  * query, kernel attributes, the watchdog word's address, a private memory
  * pool); later calls do none.  Shapes whose last wave of output tiles would
- * run mostly empty use a stream-K schedule (see `schedule` below) whose
+ * leave enough SMs idle use a stream-K schedule (see `schedule` below) whose
  * workspace is taken from that pool on `stream` and handed back on it.
  *
  * Ordering: the kernel is launched with programmatic stream serialization, so
@@ -171,20 +171,22 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  *                 full wave of whole tiles beside it;
  *                 1: whole tiles only; 2: stream-K whenever possible (tests);
  *                 3: N-split whenever possible (tests).
- *                 N-split: when there are fewer tiles than clusters and the
- *                 stream-K rule does not split them (too few k-blocks), each
- *                 tile is cut along N into s = 2 or 4 narrower tiles (256×128
- *                 or 256×64, s the largest with tiles·s <= clusters) that run
- *                 on their own CTA pairs; nothing is summed across clusters.
+ *                 N-split: when the stream-K rule does not split the problem
+ *                 and either there are fewer tiles than clusters or k is
+ *                 shallow (at most 32 k-blocks), the R tiles of the last wave
+ *                 (all tiles, with fewer tiles than clusters) are each cut
+ *                 along N into s = 2 or 4 narrower tiles (256×128 or 256×64, s
+ *                 the largest with R·s <= clusters) that run on their own CTA
+ *                 pairs; nothing is summed across clusters.
  *                 A narrower MMA is not proportionally faster on these tensor
  *                 cores (with no loads, N = 128 takes 69 % and N = 64 62 % of
  *                 the 256-wide time per k-block), and with their operand loads
  *                 the slices measured no faster than whole tiles, so this
  *                 mainly shortens each cluster's epilogue: it is for small,
  *                 latency-bound problems.
- *                 With 3 the last R tiles of a larger problem are cut the same
- *                 way when 2R <= clusters.  Only with one CTA pair per cluster
- *                 and B stored [N, K].
+ *                 With 3 the last R tiles of any problem are cut the same way
+ *                 when 2R <= clusters.  Only with one CTA pair per cluster and
+ *                 B stored [N, K].
  *                 A stream-K launch needs a workspace (gemm_f16_nt_plan's
  *                 workspace_bytes); the call takes it from a memory pool
  *                 private to this library on `stream` (cudaMallocFromPoolAsync)
