@@ -298,8 +298,8 @@ gemm_status_t gemm_bf16_nt_ex(int64_t M, int64_t N, int64_t K,
  * s = 1 producer waiting for a free ring slot, 2 MMA issuer waiting for a
  * filled slot, 3 MMA issuer waiting for a free accumulator, 4 epilogue waiting
  * for a finished accumulator, 5 producer teardown waiting for its copies,
- * 6 MMA teardown waiting for its MMAs.  The word is shared by every call on
- * that device.
+ * 6 MMA teardown waiting for its MMAs, 7 a stream-K owner waiting for a
+ * partner's partial tile.  The word is shared by every call on that device.
  */
 gemm_status_t gemm_f16_nt_device_status(void *stream, uint32_t *flags);
 
@@ -336,7 +336,7 @@ typedef struct {
     int32_t k_blocks;      /* cdiv(K, block_k) */
     int64_t num_tiles;     /* m_tiles · n_tiles */
     int32_t clusters;      /* persistent clusters launched */
-    int32_t grid_ctas;     /* clusters · cta_group */
+    int32_t grid_ctas;     /* clusters · cta_group · cluster_pairs */
     int32_t swizzle;       /* raster group width actually used */
     int32_t smem_bytes;    /* dynamic shared memory per CTA */
     int32_t tmem_cols;     /* tensor-memory columns allocated per CTA */
