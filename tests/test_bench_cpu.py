@@ -85,3 +85,27 @@ def test_reference_arm_non_zero_rank_is_silent():
 def test_warmup_floor_enforced():
     r = _bench(["--impl", "reference", "--workload", "gemm_256", "--steps", "3", "--warmup", "2"])
     assert r.returncode != 0
+
+
+def test_roofline_byte_figures():
+    """The per-flop byte figures bench.py reports, from the plan and the workload.
+
+    At 8192^3 the kernel delivers every cluster tile its 256 A rows and 256 B
+    rows of 128 bytes per k-block: 1024 tiles x 128 k-blocks x 512 rows x 128 B
+    = 2^33 bytes into shared memory.  A full Nsight Compute capture of that
+    launch counted 8,589,937,024 bytes arriving from L2
+    (l1tex__m_xbar2l1tex_read_bytes.sum), the same figure within 2.5 KB."""
+    import bench
+    import dense_fp16_gemm_gb300 as g
+    from dense_fp16_gemm_gb300 import inputs
+    w = inputs.WORKLOADS["gemm_8192"]
+    pl = g.plan(w.M, w.N, w.K, num_sms=152, max_clusters=76)
+    assert bench.l2_to_sm_bytes(pl) == 2 ** 33
+    assert abs(bench.l2_to_sm_bytes(pl) - 8_589_937_024) < 2600
+    assert w.flops == 2 * 8192 ** 3
+    assert w.compulsory_bytes == 3 * 8192 * 8192 * 2          # A and B read, C written, fp16
+    # two pairs per cluster: each pair receives the tile's A rows (multicast), plus 512 B rows
+    r = inputs.WORKLOADS["ragged_4000x3000x5000"]
+    pr = g.plan(r.M, r.N, r.K, num_sms=152, max_clusters=36)
+    assert pr["cluster_pairs"] == 2
+    assert bench.l2_to_sm_bytes(pr) == pr["num_tiles"] * pr["k_blocks"] * 128 * (2 * 256 + 512)
