@@ -15,7 +15,12 @@ Printed: one JSON line with the throughput (TFLOP/s = 2·M·N·K / time), the
 roofline fraction of the GEMM kernel against the measured dense 16-bit tensor
 peak, an end-to-end figure through the same C ABI from pinned host memory, the
 clocks seen during the timed region, and the CPU oracle timed on a bounded
-sample of the same workload.
+sample of the same workload.  Beside the headline, on rank 0: every other
+workload (256³, 4096³, the ragged shape with float and integer inputs, the MLP
+shape) timed the same way through the C ABI, each with cuBLAS beside it and its
+own clock record ("workloads"), and a sustained window of back-to-back 8192³
+launches lasting seconds, long enough for the board's power cap to set the
+clock ("sustained").
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -49,7 +54,11 @@ METRIC = "fp16 NT GEMM TFLOP/s and % of GB300 dense fp16 tensor peak"
 UNIT = "TFLOP/s"
 KERNEL_SOURCES = ["dense_fp16_gemm_gb300/csrc/gemm_f16_nt.cu", "dense_fp16_gemm_gb300/csrc/ptx.cuh",
                   "dense_fp16_gemm_gb300/csrc/sched.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_f16_nt_8192_traffic.md")
+# DRAM bytes per launch from an Nsight Compute capture, written by
+# `bench.py --record-traffic`; used only while the kernel sources hash the same
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+SIDE_WORKLOADS = ["gemm_256", "gemm_4096", "ragged_4000x3000x5000", "ragged_int_4000x3000x5000",
+                  "mlp_up_16384x14336x4096"]
 FALLBACK_PEAK_TFLOPS = 1900.0   # one earlier GB300 bf16 burst measurement
 L2_BYTES = 129 * 10**6
 SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -122,25 +131,58 @@ def kernel_source_hash() -> str:
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source and this workload; else None."""
+    """(DRAM bytes per launch, record) from the machine-readable record of an
+    Nsight Compute capture of this workload, if that capture was taken on the
+    current kernel sources; else (None, None).  The figure is recorded, not
+    measured by this run, and the JSON line says so."""
     try:
-        text = open(TRAFFIC_FILE).read()
-    except OSError:
-        return None
-    fields = {}
-    for line in text.splitlines():
-        if line.startswith("- ") and ":" in line:
-            k, v = line[2:].split(":", 1)
-            fields[k.strip()] = v.strip().strip("`")
-    if fields.get("kernel_source_sha256_16") != kernel_source_hash():
-        return None
-    if fields.get("workload") != workload:
-        return None
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None, None
+    if not rec or rec.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None, None
     try:
-        return int(fields["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+        return int(rec["dram_bytes_per_launch"]), rec
+    except (KeyError, ValueError, TypeError):
+        return None, None
+
+
+def record_traffic(rep_path: str, workload: str, command: str):
+    """Read dram__bytes_{read,write}.sum of the GEMM launches in an Nsight
+    Compute report (ncu -i … --page raw --csv) and store their mean per launch
+    for `workload` in the traffic record, keyed by the kernel-source hash."""
+    import csv
+    import io
+    out = subprocess.run(["ncu", "-i", rep_path, "--page", "raw", "--csv"], capture_output=True, text=True,
+                         check=True).stdout
+    rows = list(csv.reader(io.StringIO(out)))
+    head = rows[0]
+    col = {n: i for i, n in enumerate(head)}
+    units = rows[1]
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    per = []
+    for r in rows[2:]:
+        if "gemm_f16_nt_kernel" not in r[col["Kernel Name"]]:
+            continue
+        b = 0.0
+        for m in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            b += float(r[col[m]].replace(",", "")) * scale[units[col[m]]]
+        per.append(b)
+    if not per:
+        raise SystemExit(f"no gemm_f16_nt_kernel launch in {rep_path}")
+    try:
+        with open(TRAFFIC_FILE) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        data = {}
+    data[workload] = {"dram_bytes_per_launch": int(round(sum(per) / len(per))), "launches": len(per),
+                      "kernel_source_sha256_16": kernel_source_hash(), "command": command,
+                      "metrics": "dram__bytes_read.sum + dram__bytes_write.sum"}
+    with open(TRAFFIC_FILE, "w") as f:
+        json.dump(data, f, indent=1, sort_keys=True)
+        f.write("\n")
+    print(json.dumps(data[workload]))
 
 
 class ClockSampler:
@@ -182,20 +224,31 @@ class ClockSampler:
         except OSError:
             return None
 
-    def _poll(self, period):
+    def _take(self):
+        """One NVML sample (clock, max clock, power, reason bits), timestamped."""
         import ctypes
         lib, h = self._nvml
         mhz, mx, mw = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint()
         bits = ctypes.c_ulonglong()
         get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
             getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        t = time.time()
+        if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0 and \
+                lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            pw = mw.value / 1e3 if lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) == 0 else 0.0
+            rb = bits.value if get_reasons(h, ctypes.byref(bits)) == 0 else 0
+            self.samples.append((t, float(mhz.value), float(mx.value), pw, int(rb)))
+
+    def sample_now(self):
+        """Take a sample from the calling thread: called while launches the host
+        has already enqueued keep the GPU busy, so that even a timed region of a
+        few milliseconds holds at least one sample."""
+        if self._nvml is not None:
+            self._take()
+
+    def _poll(self, period):
         while not self._stop.is_set():
-            t = time.time()
-            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0 and \
-                    lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
-                pw = mw.value / 1e3 if lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) == 0 else 0.0
-                rb = bits.value if get_reasons(h, ctypes.byref(bits)) == 0 else 0
-                self.samples.append((t, float(mhz.value), float(mx.value), pw, int(rb)))
+            self._take()
             time.sleep(period)
 
     def _start_smi(self, idx):
@@ -209,6 +262,10 @@ class ClockSampler:
 
     def window(self, t0: float, t1: float):
         self.windows.append((t0, t1))
+
+    def summary_for(self, t0: float, t1: float):
+        """Clock summary of the samples inside one wall window (after stop())."""
+        return self.summary([(t0, t1)])
 
     def stop(self):
         self._stop.set()
@@ -238,8 +295,9 @@ class ClockSampler:
             os.unlink(self._f.name)
         return self.summary()
 
-    def summary(self):
-        inside = [s for s in self.samples if any(a <= s[0] <= b for a, b in self.windows)]
+    def summary(self, windows=None):
+        windows = self.windows if windows is None else windows
+        inside = [s for s in self.samples if any(a <= s[0] <= b for a, b in windows)]
         if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
                     "source": "nvml" if self._nvml else "nvidia-smi"}
@@ -369,6 +427,136 @@ def cublas_context(A_d, B_d, steps: int, stream, flush=None):
         m.allow_fp16_reduced_precision_reduction, m.allow_bf16_reduced_precision_reduction = prev
 
 
+def time_steps(step, steps: int, stream, flush=None, sampler=None):
+    """Run `steps` calls of `step` on `stream`, timed with CUDA events on it.
+    Back to back (flush None): returns (mean ms per launch from the events
+    around the whole region, wall window).  With an L2 flush buffer: each
+    launch is preceded by the flush and bracketed by its own events; returns
+    the mean of those per-launch times."""
+    import torch
+    torch.cuda.synchronize()
+    w0 = time.time()
+    if flush is None:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            step()
+        b.record(stream)
+        if sampler is not None:
+            sampler.sample_now()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / steps
+    else:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            step()
+            b.record(stream)
+        if sampler is not None:
+            sampler.sample_now()
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    return ms, (w0, time.time())
+
+
+def cublas_step(A_d, B_d, out):
+    import torch
+
+    def step():
+        torch.matmul(A_d, B_d.t(), out=out)
+    return step
+
+
+def fp32_accumulate_only():
+    """Context manager: cuBLAS through torch.matmul keeps fp32 accumulation."""
+    import contextlib
+
+    import torch
+
+    @contextlib.contextmanager
+    def cm():
+        m = torch.backends.cuda.matmul
+        prev = (m.allow_fp16_reduced_precision_reduction, m.allow_bf16_reduced_precision_reduction)
+        m.allow_fp16_reduced_precision_reduction = False
+        m.allow_bf16_reduced_precision_reduction = False
+        try:
+            yield
+        finally:
+            m.allow_fp16_reduced_precision_reduction, m.allow_bf16_reduced_precision_reduction = prev
+    return cm()
+
+
+def measure_workload(lib, name: str, device, stream, steps: int, warmup: int, cooldown: float, peaks,
+                     sampler=None):
+    """One workload through the C ABI entry point gemm_f16_nt, timed like the
+    headline (L2 flushed between launches when its operands fit in L2), with
+    torch.matmul (cuBLAS) timed the same way on the same operands beside it.
+    Returns the record and the wall windows of the two timed regions."""
+    import torch
+
+    import dense_fp16_gemm_gb300 as g
+    w = inputs.WORKLOADS[name]
+    A, B = inputs.operands(w)
+    Ad, Bd = torch.from_numpy(A).to(device), torch.from_numpy(B).to(device)
+    Cd = torch.full((w.M, w.N), float("nan"), dtype=torch.float16, device=device)
+    handle = stream.cuda_stream
+
+    def step():
+        st = lib.gemm_f16_nt(w.M, w.N, w.K, Ad.data_ptr(), w.K, Bd.data_ptr(), w.K, Cd.data_ptr(), w.N, handle)
+        if st != 0:
+            raise g.GemmError(st, "gemm_f16_nt")
+    flushed = w.compulsory_bytes < 2 * L2_BYTES
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=device) if flushed else None
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    if g.device_status(stream) != 0 or torch.isnan(Cd).any().item():
+        raise SystemExit(f"bench.py: {name}: watchdog word set or C unwritten after warm-up")
+    time.sleep(cooldown)
+    ms, win = time_steps(step, steps, stream, flush, sampler)
+    if g.device_status(stream) != 0:
+        raise SystemExit(f"bench.py: {name}: watchdog word set during the timed region")
+    out = torch.empty_like(Cd)
+    with fp32_accumulate_only():
+        cb = cublas_step(Ad, Bd, out)
+        for _ in range(warmup):
+            cb()
+        time.sleep(cooldown)
+        ms_cb, win_cb = time_steps(cb, steps, stream, flush, sampler)
+    pl = g.launch_plan(w.M, w.N, w.K, stream=stream, lib=lib)
+    peak, peak_sus = peaks
+    tf = w.flops / (ms * 1e-3) / 1e12
+    tf_cb = w.flops / (ms_cb * 1e-3) / 1e12
+    rec = {"M": w.M, "N": w.N, "K": w.K, "inputs": f"A {w.dist_a}, B {w.dist_b}, seeds {w.seed_a},{w.seed_b}",
+           "steps": steps, "us_per_launch": round(ms * 1e3, 2), "tflops": round(tf, 2),
+           "frac_of_burst_peak": round(tf / peak, 4),
+           "frac_of_sustained_peak": round(tf / peak_sus, 4) if peak_sus else None,
+           "l2": "flushed between launches (per-launch events)" if flushed
+                 else "operands larger than L2, launches back to back",
+           "plan": {k: pl[k] for k in ("cluster_pairs", "clusters", "num_tiles", "sk_tiles", "tail_split")},
+           "cublas_tflops": round(tf_cb, 2), "ours_over_cublas": round(tf / tf_cb, 4)}
+    del Ad, Bd, Cd, out, flush
+    torch.cuda.empty_cache()
+    return rec, win, win_cb
+
+
+def measure_sustained(step, cb_step, flops: float, ms_hint: float, seconds: float, stream, cooldown: float):
+    """Back-to-back launches for `seconds` (ours, then cuBLAS after a
+    cooldown): long enough for the board's power limit to set the clock."""
+    n = max(10, int(seconds / (ms_hint * 1e-3)))
+    time.sleep(cooldown)
+    ms, win = time_steps(step, n, stream)
+    with fp32_accumulate_only():
+        time.sleep(cooldown)
+        ms_cb, win_cb = time_steps(cb_step, n, stream)
+    tf, tf_cb = flops / (ms * 1e-3) / 1e12, flops / (ms_cb * 1e-3) / 1e12
+    return {"launches": n, "seconds": round(ms * n / 1e3, 3), "us_per_launch": round(ms * 1e3, 2),
+            "tflops": round(tf, 2), "cublas_tflops": round(tf_cb, 2),
+            "ours_over_cublas": round(tf / tf_cb, 4)}, win, win_cb
+
+
 def run_e2e(args, w, A, B, Ad, Bd, Cd, tdt, entry, device, dist, bf16):
     """Pipelined end-to-end steps; returns (max time over ranks, total flops, steps)."""
     import torch
@@ -458,7 +646,12 @@ def run_ours(args, w):
     Cd = torch.full((w.M, w.N), float("nan"), dtype=tdt, device=device)
     stream = torch.cuda.current_stream(device)
     handle = stream.cuda_stream
-    lib = g.library()
+    if args.library == "mcast":
+        if world > 1:
+            raise SystemExit("bench.py: the multicast build is for single-GPU runs only (--gpus 1)")
+        lib = g.library_mcast()
+    else:
+        lib = g.library()
     acc16 = args.accumulate == "f16"
     if acc16:   # the fp16-accumulation variant, through the options entry point
         acc_opts = g.Options(accumulate=1)
@@ -488,7 +681,7 @@ def run_ours(args, w):
     if w.compulsory_bytes < 2 * L2_BYTES or args.flush_l2:
         flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=device)
     sampler = ClockSampler(local) if rank == 0 else None
-    times, launch_ms = [], []
+    times, launch_ms, head_windows = [], [], []
     for rep in range(args.repeat):
         if rep and args.cooldown > 0:
             time.sleep(args.cooldown)
@@ -511,17 +704,19 @@ def run_ours(args, w):
             else:
                 step()
         t_end.record(stream)
+        if sampler:
+            sampler.sample_now()       # the enqueued launches are still running
         torch.cuda.synchronize(device)
         w1 = time.time()
         barrier(dist, device)
         if sampler:
             sampler.window(w0, w1)
+        head_windows.append((w0, w1))
         times.append(t_start.elapsed_time(t_end) / 1e3)
         if flush is not None:
             launch_ms.extend(a.elapsed_time(b) for a, b in evs)
         else:   # back to back: the region is the launches
             launch_ms.extend([times[-1] * 1e3 / args.steps] * args.steps)
-    clocks = sampler.stop() if sampler else None
     if g.device_status(stream) != 0:
         raise SystemExit("bench.py: watchdog word set during the timed region")
 
@@ -552,17 +747,53 @@ def run_ours(args, w):
                    "note": "same operands, same stream, fp32 accumulation; run as a library, "
                            "context only (not the target, not part of the value)"}
 
+    peaks = (peak, peak_sustained)
+    windows = {}
+    extras = rank == 0 and world == 1 and w.name == "gemm_8192" and not bf16 and not acc16 \
+        and args.library == "default"
+    # Every other workload, timed the same way through the C ABI, each with
+    # cuBLAS beside it and its own clock record.
+    side = {}
+    if extras and not args.no_workloads:
+        for name in SIDE_WORKLOADS:
+            rec, win, win_cb = measure_workload(lib, name, device, stream, args.workload_steps, args.warmup,
+                                                args.cooldown, peaks, sampler)
+            side[name] = rec
+            windows[name] = (win, win_cb)
+    # A sustained window: seconds of back-to-back launches at the headline
+    # shape, long enough for the board's power limit to settle the clock.
+    sustained = None
+    if extras and args.sustained_seconds > 0:
+        out = torch.empty_like(Cd)
+        sustained, win, win_cb = measure_sustained(step, cublas_step(Ad, Bd, out), w.flops, mean_launch_s * 1e3,
+                                                   args.sustained_seconds, stream, args.cooldown)
+        if g.device_status(stream) != 0:
+            raise SystemExit("bench.py: watchdog word set during the sustained window")
+        sustained["frac_of_burst_peak"] = round(sustained["tflops"] / peak, 4)
+        sustained["frac_of_sustained_peak"] = round(sustained["tflops"] / peak_sustained, 4) if peak_sustained else None
+        sustained["gpu_launches"] = sustained["launches"]
+        windows["sustained"] = (win, win_cb)
+        del out
+
+    clocks = None
+    if sampler:
+        sampler.stop()
+        clocks = sampler.summary(head_windows)
+        for name, rec in side.items():
+            rec["clocks"] = sampler.summary([windows[name][0]])
+            rec["cublas_clocks"] = sampler.summary([windows[name][1]])
+        if sustained is not None:
+            sustained["clocks"] = sampler.summary([windows["sustained"][0]])
+            sustained["cublas_clocks"] = sampler.summary([windows["sustained"][1]])
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle_sample(w, A, B, args.cpu_seconds, acc16, bf16)
 
     if rank == 0:
-        traffic = recorded_traffic(w.name)
-        lim = g.device_limits()
+        traffic, traffic_rec = recorded_traffic(w.name) if not bf16 and not acc16 else (None, None)
         popts = g.Options(accumulate=1 if acc16 else 0)
-        pl = g.plan(w.M, w.N, w.K, num_sms=lim["sms"], options=popts)
-        pl = g.plan(w.M, w.N, w.K, num_sms=lim["sms"], options=popts,
-                    max_clusters=lim["resident_pair_pairs"] if pl["cluster_pairs"] == 2 else lim["resident_pairs"])
+        pl = g.launch_plan(w.M, w.N, w.K, stream=stream, options=popts, lib=lib)
         kernel_desc = (f"gemm_f16_nt_kernel<KCfg<{pl['cta_group']},256,{pl['stages']},{pl['cluster_pairs']},"
                        f"{int(bf16)},{int(acc16)}>>: "
                        f"{pl['clusters']} clusters x {pl['grid_ctas'] // pl['clusters']} CTAs, "
@@ -578,6 +809,9 @@ def run_ours(args, w):
             "pct_of_peak": round(100.0 * achieved / peak, 2),
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                          "unit": UNIT, "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "traffic_source": (f"recorded by an Nsight Compute capture of this kernel source "
+                                            f"({traffic_rec['command']}), not measured by this run"
+                                            if traffic_rec else None),
                          "peak_source": f"{peak_src} bf16 dense burst (fp16 runs at the bf16 rate)",
                          "frac_of_sustained": round(achieved / peak_sustained, 4) if peak_sustained else None,
                          "kernel": kernel_desc,
@@ -593,6 +827,8 @@ def run_ours(args, w):
             "clocks": clocks,
             "timing": {"repeats": args.repeat, "cooldown_s": args.cooldown,
                        "per_repeat_ms_per_step": [round(t / args.steps * 1e3, 4) for t in times]},
+            "sustained": sustained,
+            "workloads": side or None,
             "cpu_baseline": cpu,
             "context": context,
         }
@@ -665,6 +901,19 @@ def main(argv=None):
                     help="flush L2 between steps even for operands larger than 2x L2")
     ap.add_argument("--no-cublas", action="store_true",
                     help="skip the torch.matmul (cuBLAS) context measurement")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads' records (headline run only)")
+    ap.add_argument("--workload-steps", type=int, default=30,
+                    help="timed launches per other workload (the pages time 30 iterations)")
+    ap.add_argument("--sustained-seconds", type=float, default=2.5,
+                    help="length of the sustained back-to-back window at 8192^3 (0: skip)")
+    ap.add_argument("--library", choices=["default", "mcast"], default="default",
+                    help="mcast: the single-GPU multicast build (refused with --gpus > 1)")
+    ap.add_argument("--record-command", default="",
+                    help="with --record-traffic: the command line the capture ran")
+    ap.add_argument("--record-traffic", metavar="NCU_REP",
+                    help="store the DRAM bytes per launch of the GEMM launches in an Nsight Compute "
+                         "report for --workload in the traffic record, then exit")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -674,6 +923,11 @@ def main(argv=None):
     if args.gpus != world and world > 1:
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
     w = inputs.WORKLOADS[args.workload]
+    if args.record_traffic:
+        record_traffic(args.record_traffic, w.name, args.record_command or "")
+        return
+    if args.library == "mcast" and (world > 1 or args.gpus > 1):
+        ap.error("--library mcast is for single-GPU runs only")
     if args.impl == "reference":
         run_reference(args, w)
     else:

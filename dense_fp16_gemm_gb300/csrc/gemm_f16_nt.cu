@@ -15,10 +15,11 @@
 // A and one half of the B tile, and the pair's single MMA reads both halves, so
 // the shared operand crosses L2 once per pair.
 //
-// Variants, all in this one kernel template (KCfg): a cluster of two pairs that
-// share A by TMA multicast; one CTA per tile (cta_group::1); bf16 operands and
-// result; an fp16 accumulator; A and/or B stored M/N-contiguous (MN-major
-// operands).  The work schedule (see "work schedule") mixes whole tiles, a
+// Variants, all in this one kernel template (KCfg): one CTA per tile
+// (cta_group::1); bf16 operands and result; an fp16 accumulator; A and/or B
+// stored M/N-contiguous (MN-major operands); and, only in the separately built
+// single-GPU library (mcast/gemm_f16_nt_mcast.cu, which includes this file), a
+// cluster of two pairs that share A by TMA multicast.  The work schedule (see "work schedule") mixes whole tiles, a
 // stream-K split of the last wave in k, and column slices of small problems'
 // tiles.  Launches use programmatic dependent launch: a CTA sets up, then
 // waits for the previous kernel on the stream before touching global memory.
@@ -33,10 +34,12 @@
 // accumulator lives in TMEM instead of registers, so V6's register
 // reallocation (§The Register Budget Problem) has no counterpart here.
 //
-// Every wait on an mbarrier is bounded by a watchdog (default 1 s): on expiry
-// the CTA sets a flag that ends every role's loop, records the expired wait in a
-// device word, waits (bounded) for its own copies and MMAs in flight, releases
-// its tensor memory and exits.
+// Every wait on an mbarrier or a flag is bounded by a watchdog: a wait for one
+// pipeline stage by the base limit (default 1 s), a wait that can span a whole
+// work item's main loop by the base limit plus a fixed allowance per k-block of
+// a tile.  On expiry the CTA sets a flag that ends every role's loop, records
+// the expired wait in a device word, waits (bounded) for its own copies and MMAs
+// in flight, releases its tensor memory and exits.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -54,7 +57,22 @@
 
 #define G16_EXPORT extern "C" __attribute__((visibility("default")))
 
+// 1 when this file is compiled into the single-GPU multicast library (whose
+// translation unit defines it and provides McastA first); 0 in the default
+// library, which has no multicast load.
+#ifndef G16_MCAST_LIB
+#define G16_MCAST_LIB 0
+#endif
+
 namespace g16 {
+
+#if !G16_MCAST_LIB
+// The default library has no loader for clusters of two pairs.
+template <int CP>
+struct McastA {
+    static constexpr bool kAvailable = false;
+};
+#endif
 
 constexpr int kBlockM = 128;   // accumulator rows per CTA = TMEM lanes
 constexpr int kBlockK = 64;    // k per stage: 64 fp16 = one 128-byte swizzle row
@@ -66,6 +84,10 @@ constexpr int kOutBufBytes = 32 * kEpiCols * 2;    // one warp's 32×64 fp16 sta
 constexpr int kOutBufs = 2;                        // double-buffered per warp
 constexpr int kDefaultSwizzle = 8;
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;
+// Allowance per k-block of a tile for the waits that can span a work item's
+// whole main loop (a k-block takes about 0.27 us at full clock; 8 us leaves a
+// margin of about 30x for low clocks and contention).
+constexpr uint64_t kItemWaitNsPerKb = 8000ull;
 
 // watchdog word layout: bit 0 = a wait expired, bit 7+s = wait site s expired
 enum : uint32_t {
@@ -139,7 +161,8 @@ struct Params {
     int32_t N8;        // N rounded down to a multiple of 8 (16 bytes)
     uint16_t* C;       // for the last N - N8 columns, written with plain stores
     int64_t ldc;
-    uint64_t timeout_ns;
+    uint64_t timeout_ns;       // limit of a wait for one pipeline stage
+    uint64_t item_timeout_ns;  // limit of a wait that can span a work item's main loop
     uint32_t* watchdog;
     int32_t inject_stall;
     uint32_t a_mn;     // 1: A stored [K, M] (M contiguous) — MN-major in shared memory
@@ -269,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
     constexpr int NCTA = Cfg::kCtas;
     constexpr int BN = Cfg::kBN;
     constexpr int S = Cfg::kStages;
+    static_assert(CP == 1 || McastA<CP>::kAvailable, "two pairs per cluster need the multicast library's loader");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -335,6 +359,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
     w.ctas = NCTA;
     w.rank = rank;
     w.word = p.watchdog;
+    // Waits that can legitimately last a whole work item: the epilogue's wait
+    // for a finished accumulator, an owner's wait for its partners' partial
+    // tiles, the MMA issuer's wait for a drained accumulator and, behind it, the
+    // producer's wait for a free stage.  Only the MMA issuer's wait for a filled
+    // stage (which depends on nothing but the copies in flight) keeps the base
+    // limit.
+    Watch wi = w;
+    wi.limit_ns = p.item_timeout_ns;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -366,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                 const bool down = it.kind == kItemPartialOut;
                 for (uint32_t i = it.kb0; i < it.kb1; ++i) {
                     const uint32_t kb = down ? it.kb1 - 1u - (i - it.kb0) : i;
-                    if (!wait(empty0 + 8 * stage, phase ^ 1u, w, kSiteProducerEmpty)) {
+                    if (!wait(empty0 + 8 * stage, phase ^ 1u, wi, kSiteProducerEmpty)) {
                         ok = false;
                         break;
                     }
@@ -379,13 +411,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                     const uint32_t b_dst = sB + stage * Cfg::kBBytes;
                     if constexpr (CP == 2) {
                         // Both pairs need the same A rows: this CTA loads half of them
-                        // into the same-rank CTA of both pairs (TMA multicast).
+                        // into the same-rank CTA of both pairs (TMA multicast; the
+                        // loader exists only in the single-GPU multicast library).
                         const int32_t r0 = m0 + int32_t(pair * (kBlockM / 2));
                         const uint16_t mask = uint16_t((1u << prank) | (1u << (prank + 2u)));
                         if (p.a_mn)
-                            ptx::tma_load_2d_pair_mcast(a_dst + pair * kMnBoxBytes, &p.tmA, r0, k0, bar, mask);
+                            McastA<CP>::load(a_dst + pair * kMnBoxBytes, &p.tmA, r0, k0, bar, mask);
                         else
-                            ptx::tma_load_2d_pair_mcast(a_dst + pair * (Cfg::kABytes / 2), &p.tmA, k0, r0, bar, mask);
+                            McastA<CP>::load(a_dst + pair * (Cfg::kABytes / 2), &p.tmA, k0, r0, bar, mask);
                     } else if (p.a_mn) {
                         for (int j = 0; j < kBlockM / 64; ++j) {
                             if constexpr (CG == 2)
@@ -461,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                 work_init(work, p, cluster, nclusters);
                 uint32_t item_no = 0;
                 while (ok && work_next(work, p, it)) {
-                    if (!wait(acce0 + 8 * acc, acc_phase ^ 1u, w, kSiteMmaAccFree)) break;
+                    if (!wait(acce0 + 8 * acc, acc_phase ^ 1u, wi, kSiteMmaAccFree)) break;
                     ptx::tc_fence_after();
                     uint64_t* tr = (p.trace && item_no < p.trace_items)
                                        ? p.trace + (size_t(cluster) * p.trace_items + item_no) * 8 : nullptr;
@@ -569,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                                ? p.trace + (size_t(cluster) * p.trace_items + item_no) * 8 : nullptr;
             ++item_no;
             uint32_t ok = 0;
-            if (lane == 0) ok = wait(accf0 + 8 * acc, acc_phase, w, kSiteEpiAccFull) ? 1u : 0u;
+            if (lane == 0) ok = wait(accf0 + 8 * acc, acc_phase, wi, kSiteEpiAccFull) ? 1u : 0u;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             ptx::tc_fence_after();
@@ -582,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                 if (lane == 0)
                     for (uint32_t i = 0; i < npart && okf; ++i)
                         okf = wait_flag(p.flags + (size_t(cluster + 1 + i) * NCTA + rank) * kEpiWarps + q,
-                                        p.launch_id, w, kSiteStreamK) ? 1u : 0u;
+                                        p.launch_id, wi, kSiteStreamK) ? 1u : 0u;
                 okf = __shfl_sync(0xffffffffu, okf, 0);
                 if (!okf) break;
                 __threadfence();
@@ -727,14 +760,16 @@ __global__ void zero_fill_kernel(uint16_t* C, int64_t M, int64_t N, int64_t ldc)
 // ---------------------------------------------------------------------------
 
 using Cfg2 = KCfg<2, 256, 6>;      // CTA pair, 256×256 tile, 6-stage ring
-using Cfg2x2 = KCfg<2, 256, 6, 2>; // two CTA pairs per cluster sharing A: 256×512 cluster tile
 using Cfg1 = KCfg<1, 256, 4>;      // single CTA, 128×256 tile, 4-stage ring
-using Cfg2Bf = KCfg<2, 256, 6, 1, true>;    // the same three with bf16 operands and result
-using Cfg2x2Bf = KCfg<2, 256, 6, 2, true>;
+using Cfg2Bf = KCfg<2, 256, 6, 1, true>;    // the same with bf16 operands and result
 using Cfg1Bf = KCfg<1, 256, 4, 1, true>;
 using Cfg2A16 = KCfg<2, 256, 6, 1, false, true>;   // the fp16 ones with an fp16 accumulator
-using Cfg2x2A16 = KCfg<2, 256, 6, 2, false, true>;
 using Cfg1A16 = KCfg<1, 256, 4, 1, false, true>;
+#if G16_MCAST_LIB
+using Cfg2x2 = KCfg<2, 256, 6, 2>; // two CTA pairs per cluster sharing A: 256×512 cluster tile
+using Cfg2x2Bf = KCfg<2, 256, 6, 2, true>;
+using Cfg2x2A16 = KCfg<2, 256, 6, 2, false, true>;
+#endif
 
 template <class Cfg>
 bool allow_smem() {
@@ -747,16 +782,32 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// A stream-K workspace reserved at a device's set-up.  A launch that uses it
+// makes its stream wait for the slot's previous user (`done`), so launches on
+// unordered streams that land on the same slot run one after the other; the
+// mutex keeps host threads from interleaving wait, launch and record.
+struct WorkspaceSlot {
+    void* ptr = nullptr;
+    cudaEvent_t done = nullptr;
+    std::mutex mu;
+};
+constexpr int kMaxWorkspaceSlots = 8;
+constexpr int kDefaultWorkspaceSlots = 4;
+
 struct DeviceState {
     bool ready = false;
     gemm_status_t status = GEMM_OK;
     int sms = 0;
     int max_clusters2 = 0;   // resident CTA pairs for Cfg2
-    int max_clusters4 = 0;   // resident clusters of two pairs for Cfg2x2
+    int max_clusters4 = 0;   // resident clusters of two pairs for Cfg2x2 (0 without it)
     int max_ctas1 = 0;       // resident CTAs for Cfg1
+    bool single_gpu = false; // the process sees exactly one CUDA device
     uint32_t* watchdog = nullptr;
-    bool pool_ready = false;
-    cudaMemPool_t pool = nullptr;   // private stream-ordered pool for stream-K workspaces
+    bool ws_ready = false;
+    int ws_slots = 0;        // workspace slots reserved (0: stream-K unavailable)
+    int64_t ws_bytes = 0;    // bytes per slot
+    WorkspaceSlot slot[kMaxWorkspaceSlots];
+    std::atomic<uint32_t> next_slot{0};
 };
 
 constexpr int kMaxDevices = 64;
@@ -794,12 +845,23 @@ gemm_status_t setup_device(int dev, DeviceState& st) {
         }
         g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
-    if (!allow_smem<Cfg2>() || !allow_smem<Cfg2x2>() || !allow_smem<Cfg1>() ||
-        !allow_smem<Cfg2Bf>() || !allow_smem<Cfg2x2Bf>() || !allow_smem<Cfg1Bf>() ||
-        !allow_smem<Cfg2A16>() || !allow_smem<Cfg2x2A16>() || !allow_smem<Cfg1A16>()) {
+    if (!allow_smem<Cfg2>() || !allow_smem<Cfg1>() || !allow_smem<Cfg2Bf>() || !allow_smem<Cfg1Bf>() ||
+        !allow_smem<Cfg2A16>() || !allow_smem<Cfg1A16>()) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
+#if G16_MCAST_LIB
+    if (!allow_smem<Cfg2x2>() || !allow_smem<Cfg2x2Bf>() || !allow_smem<Cfg2x2A16>()) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+#endif
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    st.single_gpu = ndev == 1;
     // How many clusters can be resident at once (cluster placement within the
     // GPCs may leave some SMs out: on a 152-SM GB300, 76 pairs but only 36
     // clusters of four).
@@ -823,7 +885,11 @@ gemm_status_t setup_device(int dev, DeviceState& st) {
         return n < sms / ctas ? n : sms / ctas;
     };
     st.max_clusters2 = resident_clusters(gemm_f16_nt_kernel<Cfg2>, 2, Cfg2::kSmemBytes);
+#if G16_MCAST_LIB
     st.max_clusters4 = resident_clusters(gemm_f16_nt_kernel<Cfg2x2>, 4, Cfg2x2::kSmemBytes);
+#else
+    st.max_clusters4 = 0;
+#endif
     {
         int per_sm = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_f16_nt_kernel<Cfg1>, kThreads,
@@ -844,25 +910,69 @@ gemm_status_t setup_device(int dev, DeviceState& st) {
     return GEMM_OK;
 }
 
-// Workspaces come from a pool of this library's own, on the caller's stream,
-// and stay cached in it between calls.
-void setup_pool(int dev, DeviceState& st) {
-    cudaMemPoolProps props = {};
-    props.allocType = cudaMemAllocationTypePinned;
-    props.location.type = cudaMemLocationTypeDevice;
-    props.location.id = dev;
-    if (cudaMemPoolCreate(&st.pool, &props) != cudaSuccess) {
-        cudaGetLastError();
-        st.pool = nullptr;
-    } else {
-        uint64_t keep = UINT64_MAX;
-        cudaMemPoolSetAttribute(st.pool, cudaMemPoolAttrReleaseThreshold, &keep);
-    }
+// Stream-K workspace: flags first ([cluster][rank][warp] uint64, 256-byte
+// aligned), then the fp32 partial tiles ([cluster][rank][256/4][128] float4),
+// one 128×256 partial per CTA of the cluster.
+constexpr int kCtaTileN = 256;
+int64_t flags_bytes(int ctas, int64_t clusters) {
+    return (clusters * ctas * kEpiWarps * 8 + 255) / 256 * 256;
+}
+int64_t workspace_bytes(int ctas, int64_t clusters) {
+    return flags_bytes(ctas, clusters) + clusters * ctas * int64_t(kBlockM) * kCtaTileN * 4;
 }
 
-// The current device's state after its one-time set-up; `with_pool` also
-// creates the workspace pool (the static-scratch entry point never needs it).
-gemm_status_t device_state(DeviceState** out, int* dev_out, bool with_pool) {
+// Workspace slots to reserve: GEMM_F16_NT_WORKSPACE_SLOTS (0..8) if set to a
+// number, else 4.
+int workspace_slots_setting() {
+    const char* e = getenv("GEMM_F16_NT_WORKSPACE_SLOTS");
+    if (!e || !*e) return kDefaultWorkspaceSlots;
+    char* end = nullptr;
+    const long v = strtol(e, &end, 10);
+    if (end == e || *end != '\0' || v < 0) return kDefaultWorkspaceSlots;
+    return v > kMaxWorkspaceSlots ? kMaxWorkspaceSlots : int(v);
+}
+
+// Reserve the stream-K workspace slots, each large enough for any launch on
+// this device.  If the memory cannot be had, no slot is kept and every call
+// is planned without the split (reported in the plan's split_k_off).
+void setup_workspace(DeviceState& st) {
+    int64_t need = workspace_bytes(2, st.max_clusters2);
+    if (workspace_bytes(1, st.max_ctas1) > need) need = workspace_bytes(1, st.max_ctas1);
+    if (workspace_bytes(4, st.max_clusters4) > need) need = workspace_bytes(4, st.max_clusters4);
+    const int want = workspace_slots_setting();
+    int got = 0;
+    for (; got < want; ++got) {
+        WorkspaceSlot& sl = st.slot[got];
+        if (cudaMalloc(&sl.ptr, size_t(need)) != cudaSuccess) {
+            cudaGetLastError();
+            sl.ptr = nullptr;
+            break;
+        }
+        if (cudaEventCreateWithFlags(&sl.done, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(sl.ptr);
+            sl.ptr = nullptr;
+            sl.done = nullptr;
+            break;
+        }
+    }
+    if (got < want) {   // all or nothing: a partial reservation hides a memory shortage
+        for (int i = 0; i < got; ++i) {
+            cudaEventDestroy(st.slot[i].done);
+            cudaFree(st.slot[i].ptr);
+            st.slot[i].ptr = nullptr;
+            st.slot[i].done = nullptr;
+        }
+        got = 0;
+    }
+    st.ws_slots = got;
+    st.ws_bytes = got ? need : 0;
+}
+
+// The current device's state after its one-time set-up; `with_workspace` also
+// reserves the stream-K workspace slots (the static-scratch entry point never
+// needs them).
+gemm_status_t device_state(DeviceState** out, int* dev_out, bool with_workspace) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         cudaGetLastError();
@@ -875,16 +985,16 @@ gemm_status_t device_state(DeviceState** out, int* dev_out, bool with_pool) {
         st.ready = true;
     }
     if (st.status != GEMM_OK) return st.status;
-    if (with_pool && !st.pool_ready) {
-        setup_pool(dev, st);
-        st.pool_ready = true;
+    if (with_workspace && !st.ws_ready) {
+        setup_workspace(st);
+        st.ws_ready = true;
     }
     *out = &st;
     if (dev_out) *dev_out = dev;
     return GEMM_OK;
 }
 
-gemm_status_t current_device(DeviceState** out) { return device_state(out, nullptr, true); }
+gemm_status_t current_device(DeviceState** out, int* dev = nullptr) { return device_state(out, dev, true); }
 
 gemm_status_t check_args(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
                          const uint16_t* B, int64_t ldb, const uint16_t* C, int64_t ldc,
@@ -906,26 +1016,40 @@ gemm_status_t check_args(int64_t M, int64_t N, int64_t K, const uint16_t* A, int
     return GEMM_OK;
 }
 
-// Stream-K workspace: flags first ([cluster][rank][warp] uint64, 256-byte
-// aligned), then the fp32 partial tiles ([cluster][rank][256/4][128] float4),
-// one 128×256 partial per CTA of the cluster.
-constexpr int kCtaTileN = 256;
-int64_t flags_bytes(int ctas, int64_t clusters) {
-    return (clusters * ctas * kEpiWarps * 8 + 255) / 256 * 256;
-}
-int64_t workspace_bytes(int ctas, int64_t clusters) {
-    return flags_bytes(ctas, clusters) + clusters * ctas * int64_t(kBlockM) * kCtaTileN * 4;
-}
-
-// Default CTA pairs per cluster.  Two pairs that share A through multicast pay
-// off when a row pitch of A or B is not a multiple of 128 bytes: every 128-byte
-// row slice of a tile then spans two L2 lines, L2 traffic becomes the limit,
-// and halving A's share outweighs the SMs that clusters of four leave idle.
-// They need N wide enough for both pairs' tiles.
+// Default CTA pairs per cluster.  In the multicast library, two pairs that
+// share A pay off when a row pitch of A or B is not a multiple of 128 bytes:
+// every 128-byte row slice of a tile then spans two L2 lines, L2 traffic
+// becomes the limit, and halving A's share outweighs the SMs that clusters of
+// four leave idle.  They need N wide enough for both pairs' tiles.  The
+// default library has one pair per cluster only.
 int auto_cluster_pairs(int cg, int64_t N, int64_t lda, int64_t ldb) {
-    if (cg != 2 || N <= kCtaTileN) return 1;
+    if (!G16_MCAST_LIB || cg != 2 || N <= kCtaTileN) return 1;
     return (lda % 64 != 0 || ldb % 64 != 0) ? 2 : 1;
 }
+
+#if G16_MCAST_LIB
+// The multicast library's rule: its tensor maps may cover only this GPU's own
+// memory, in a process that sees one GPU.  A and B (first and last element)
+// must be device memory of the current device.
+gemm_status_t check_local_operands(const DeviceState& st, int dev, int64_t M, int64_t N, int64_t K,
+                                   const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                                   bool a_mn, bool b_mn) {
+    if (!st.single_gpu) return GEMM_ERR_NOT_LOCAL;
+    if (K == 0 || M == 0 || N == 0) return GEMM_OK;   // no operand is read
+    const int64_t a_rows = a_mn ? K : M, a_cols = a_mn ? M : K;
+    const int64_t b_rows = b_mn ? K : N, b_cols = b_mn ? N : K;
+    const void* ends[4] = {A, A + (a_rows - 1) * lda + (a_cols - 1), B, B + (b_rows - 1) * ldb + (b_cols - 1)};
+    for (const void* q : ends) {
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, q) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_NOT_LOCAL;
+        }
+        if (at.type != cudaMemoryTypeDevice || at.device != dev) return GEMM_ERR_NOT_LOCAL;
+    }
+    return GEMM_OK;
+}
+#endif
 
 // The options with every "auto" (zero) CTA-group and cluster choice resolved.
 gemm_f16_nt_options_t resolve_options(const gemm_f16_nt_options_t* o, int64_t N, int64_t lda, int64_t ldb) {
@@ -951,7 +1075,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
     const int cp = (o && o->cluster_pairs) ? o->cluster_pairs : 1;
     const int acc = o ? o->accumulate : 0;
     if ((cg != 1 && cg != 2) || sw < 1 || sw > 64 || (o && o->max_clusters < 0) || sched < 0 ||
-        sched > 3 || cp < 1 || cp > 2 || (cp == 2 && cg != 2) || acc < 0 || acc > 1)
+        sched > 3 || cp < 1 || cp > 2 || (cp == 2 && (cg != 2 || !G16_MCAST_LIB)) || acc < 0 || acc > 1)
         return GEMM_ERR_INVALID_VALUE;
     memset(pl, 0, sizeof(*pl));
     pl->cta_group = cg;
@@ -1104,6 +1228,7 @@ gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t
     p.M = int32_t(M);
     p.N = int32_t(N);
     p.timeout_ns = (o && o->timeout_ns) ? o->timeout_ns : kDefaultTimeoutNs;
+    p.item_timeout_ns = p.timeout_ns + uint64_t(pl.k_blocks) * kItemWaitNsPerKb;
     p.watchdog = watchdog;
     p.inject_stall = o ? o->inject_stall : 0;
     p.a_mn = a_mn ? 1u : 0u;
@@ -1149,76 +1274,142 @@ gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t
     return GEMM_OK;
 }
 
-gemm_status_t run(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B,
-                  int64_t ldb, uint16_t* C, int64_t ldc, void* stream_v, const gemm_f16_nt_options_t* o,
-                  bool bf16 = false) {
-    if (o && (o->a_layout < 0 || o->a_layout > 1 || o->b_layout < 0 || o->b_layout > 1 ||
-              o->accumulate < 0 || o->accumulate > 1 || (bf16 && o->accumulate != 0)))
+// Why a call ran without the stream-K split that its shape would take
+// (gemm_f16_nt_plan_t.split_k_off).
+enum : int32_t { kSplitOn = 0, kSplitOffCapture = 1, kSplitOffNoWorkspace = 2 };
+
+gemm_status_t check_options(const gemm_f16_nt_options_t* o, bool bf16) {
+    if (!o) return GEMM_OK;
+    if (o->a_layout < 0 || o->a_layout > 1 || o->b_layout < 0 || o->b_layout > 1 || o->accumulate < 0 ||
+        o->accumulate > 1 || (bf16 && o->accumulate != 0))
         return GEMM_ERR_INVALID_VALUE;
-    gemm_status_t s = check_args(M, N, K, A, lda, B, ldb, C, ldc, o && o->a_layout == 1, o && o->b_layout == 1);
-    if (s != GEMM_OK) return s;
-    if (o && ((o->cta_group != 0 && o->cta_group != 1 && o->cta_group != 2) || o->swizzle < 0 ||
-              o->swizzle > 64 || o->max_clusters < 0 || o->schedule < 0 || o->schedule > 3 ||
-              o->cluster_pairs < 0 || o->cluster_pairs > 2 || (o->cluster_pairs == 2 && o->cta_group == 1) ||
-              o->trace_items < 0 || (o->trace && (reinterpret_cast<uintptr_t>(o->trace) & 7))))
+    if ((o->cta_group != 0 && o->cta_group != 1 && o->cta_group != 2) || o->swizzle < 0 || o->swizzle > 64 ||
+        o->max_clusters < 0 || o->schedule < 0 || o->schedule > 3 || o->cluster_pairs < 0 ||
+        o->cluster_pairs > (G16_MCAST_LIB ? 2 : 1) || (o->cluster_pairs == 2 && o->cta_group == 1) ||
+        o->trace_items < 0 || (o->trace && (reinterpret_cast<uintptr_t>(o->trace) & 7)))
         return GEMM_ERR_INVALID_VALUE;
-    if (M == 0 || N == 0) return GEMM_OK;
-    DeviceState* st = nullptr;
-    if ((s = current_device(&st)) != GEMM_OK) return s;
-    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
-    if (K == 0) {
-        const int64_t total = M * N;
-        int64_t blocks = cdiv(total, 256);
-        if (blocks > int64_t(st->sms) * 8) blocks = int64_t(st->sms) * 8;
-        zero_fill_kernel<<<dim3(uint32_t(blocks)), dim3(256), 0, stream>>>(C, M, N, ldc);
-        if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
-        return GEMM_OK;
-    }
-    const gemm_f16_nt_options_t ro = resolve_options(o, N, lda, ldb);
-    const int cg = ro.cta_group, cp = ro.cluster_pairs;
-    // A captured launch is replayed with the parameters it was captured with.
-    // The stream-K split tags its completion flags with a per-launch id, which
-    // a replay would repeat (an owner could then take a partner's partial from
-    // an earlier replay), so a call made under stream capture runs without it.
+    return GEMM_OK;
+}
+
+// The plan a call on `stream` gets on this device.  A captured launch is
+// replayed with the parameters it was captured with; the stream-K split tags
+// its completion flags with a per-launch id, which a replay would repeat (an
+// owner could then take a partner's partial from an earlier replay), so a call
+// made under stream capture runs without it.  Without reserved workspace the
+// split is off too.  `split_k_off` records either reason when the shape would
+// have split.
+gemm_status_t plan_call(const DeviceState& st, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
+                        const gemm_f16_nt_options_t& ro, bool have_workspace, gemm_f16_nt_plan_t* pl) {
     cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(stream, &capture) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
-    const bool allow_split_k = capture == cudaStreamCaptureStatusNone;
+    const int32_t off = capture != cudaStreamCaptureStatusNone ? kSplitOffCapture
+                        : !have_workspace                      ? kSplitOffNoWorkspace
+                                                               : kSplitOn;
+    const int resident = resident_clusters_for(st, ro);
+    gemm_status_t s = make_plan(M, N, K, st.sms, resident, &ro, pl, off == kSplitOn);
+    if (s != GEMM_OK || off == kSplitOn) return s;
+    gemm_f16_nt_plan_t would;
+    if ((s = make_plan(M, N, K, st.sms, resident, &ro, &would, true)) != GEMM_OK) return s;
+    if (would.sk_tiles > 0) pl->split_k_off = off;
+    return GEMM_OK;
+}
+
+template <class C2, class C2x2, class C1>
+gemm_status_t launch_cfg(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t K, const uint16_t* A,
+                         int64_t lda, const uint16_t* B, int64_t ldb, uint16_t* C, int64_t ldc,
+                         cudaStream_t stream, const gemm_f16_nt_options_t* o, uint32_t* watchdog, void* ws) {
+    if (pl.cta_group == 1) return launch<C1>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, o, watchdog, ws);
+    if constexpr (!std::is_void<C2x2>::value)
+        if (pl.cluster_pairs == 2) return launch<C2x2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, o, watchdog, ws);
+    return launch<C2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, o, watchdog, ws);
+}
+
+#if G16_MCAST_LIB
+using Cfg2x2_ = Cfg2x2;
+using Cfg2x2Bf_ = Cfg2x2Bf;
+using Cfg2x2A16_ = Cfg2x2A16;
+#else
+using Cfg2x2_ = void;
+using Cfg2x2Bf_ = void;
+using Cfg2x2A16_ = void;
+#endif
+
+gemm_status_t launch_any(bool bf16, const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t K,
+                         const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb, uint16_t* C, int64_t ldc,
+                         cudaStream_t stream, const gemm_f16_nt_options_t* ro, uint32_t* watchdog, void* ws) {
+    if (bf16)
+        return launch_cfg<Cfg2Bf, Cfg2x2Bf_, Cfg1Bf>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, ro, watchdog, ws);
+    if (ro->accumulate == 1)
+        return launch_cfg<Cfg2A16, Cfg2x2A16_, Cfg1A16>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, ro, watchdog, ws);
+    return launch_cfg<Cfg2, Cfg2x2_, Cfg1>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, ro, watchdog, ws);
+}
+
+gemm_status_t zero_fill(const DeviceState& st, int64_t M, int64_t N, uint16_t* C, int64_t ldc,
+                        cudaStream_t stream) {
+    const int64_t total = M * N;
+    int64_t blocks = cdiv(total, 256);
+    if (blocks > int64_t(st.sms) * 8) blocks = int64_t(st.sms) * 8;
+    zero_fill_kernel<<<dim3(uint32_t(blocks)), dim3(256), 0, stream>>>(C, M, N, ldc);
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+}
+
+gemm_status_t run(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B,
+                  int64_t ldb, uint16_t* C, int64_t ldc, void* stream_v, const gemm_f16_nt_options_t* o,
+                  bool bf16 = false) {
+    gemm_status_t s = check_options(o, bf16);
+    if (s != GEMM_OK) return s;
+    const bool a_mn = o && o->a_layout == 1, b_mn = o && o->b_layout == 1;
+    if ((s = check_args(M, N, K, A, lda, B, ldb, C, ldc, a_mn, b_mn)) != GEMM_OK) return s;
+    if (M == 0 || N == 0) return GEMM_OK;
+    DeviceState* st = nullptr;
+    int dev = -1;
+    if ((s = current_device(&st, &dev)) != GEMM_OK) return s;
+#if G16_MCAST_LIB
+    if ((s = check_local_operands(*st, dev, M, N, K, A, lda, B, ldb, a_mn, b_mn)) != GEMM_OK) return s;
+#endif
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    if (K == 0) return zero_fill(*st, M, N, C, ldc, stream);
+    const gemm_f16_nt_options_t ro = resolve_options(o, N, lda, ldb);
     gemm_f16_nt_plan_t pl;
-    const int resident = resident_clusters_for(*st, ro);
-    if ((s = make_plan(M, N, K, st->sms, resident, &ro, &pl, allow_split_k)) != GEMM_OK) return s;
-    void* ws = nullptr;
-    if (pl.sk_tiles > 0) {
-        // The workspace is taken from the library's pool on the caller's stream
-        // and handed back on it right after the launch (stream-ordered reuse).
-        if (!st->pool || cudaMallocFromPoolAsync(&ws, size_t(pl.workspace_bytes), st->pool, stream) != cudaSuccess) {
-            cudaGetLastError();
-            ws = nullptr;
-            gemm_f16_nt_options_t dp = ro;
-            dp.schedule = 1;   // no workspace: whole tiles only
-            if ((s = make_plan(M, N, K, st->sms, resident, &dp, &pl)) != GEMM_OK) return s;
-        }
-    }
-    if (bf16) {
-        if (cg == 1) s = launch<Cfg1Bf>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
-        else if (cp == 2) s = launch<Cfg2x2Bf>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
-        else s = launch<Cfg2Bf>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
-    } else if (ro.accumulate == 1) {
-        if (cg == 1) s = launch<Cfg1A16>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
-        else if (cp == 2) s = launch<Cfg2x2A16>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
-        else s = launch<Cfg2A16>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
-    } else {
-        if (cg == 1) s = launch<Cfg1>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
-        else if (cp == 2) s = launch<Cfg2x2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
-        else s = launch<Cfg2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
-    }
-    if (ws && cudaFreeAsync(ws, stream) != cudaSuccess) {
+    if ((s = plan_call(*st, M, N, K, stream, ro, st->ws_slots > 0, &pl)) != GEMM_OK) return s;
+    if (pl.sk_tiles == 0)
+        return launch_any(bf16, pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, nullptr);
+    if (pl.workspace_bytes > st->ws_bytes) return GEMM_ERR_LAUNCH;   // every slot fits any plan of this device
+    // A reserved workspace slot, taken round-robin.  The stream first waits for
+    // the slot's previous launch (a no-op if it has finished or ran on this
+    // stream), so launches on unordered streams never share a slot at the same time.
+    WorkspaceSlot& sl = st->slot[st->next_slot.fetch_add(1) % uint32_t(st->ws_slots)];
+    std::lock_guard<std::mutex> lock(sl.mu);
+    if (cudaStreamWaitEvent(stream, sl.done, 0) != cudaSuccess) {
         cudaGetLastError();
-        if (s == GEMM_OK) s = GEMM_ERR_LAUNCH;
+        return GEMM_ERR_LAUNCH;
     }
-    return s;
+    if ((s = launch_any(bf16, pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, sl.ptr)) != GEMM_OK)
+        return s;
+    if (cudaEventRecord(sl.done, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    return GEMM_OK;
+}
+
+// The plan gemm_f16_nt(_ex) would launch for these arguments on the current
+// device and `stream` (its stream-capture state included).
+gemm_status_t launch_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, void* stream_v,
+                          const gemm_f16_nt_options_t* o, gemm_f16_nt_plan_t* pl) {
+    if (!pl) return GEMM_ERR_INVALID_VALUE;
+    gemm_status_t s = check_options(o, false);
+    if (s != GEMM_OK) return s;
+    const int64_t lim = int64_t(1) << 31;
+    if (M < 0 || N < 0 || K < 0 || M >= lim || N >= lim || K >= lim || lda < 0 || ldb < 0)
+        return GEMM_ERR_INVALID_VALUE;
+    DeviceState* st = nullptr;
+    if ((s = current_device(&st)) != GEMM_OK) return s;
+    const gemm_f16_nt_options_t ro = resolve_options(o, N, lda, ldb);
+    return plan_call(*st, M, N, K, static_cast<cudaStream_t>(stream_v), ro, st->ws_slots > 0, pl);
 }
 
 // ---------------------------------------------------------------------------
@@ -1266,18 +1457,17 @@ gemm_status_t run_noalloc(int64_t M, int64_t N, int64_t K, const uint16_t* A, in
     DeviceState* st = nullptr;
     int dev = -1;
     if ((s = device_state(&st, &dev, false)) != GEMM_OK) return s;
+#if G16_MCAST_LIB
+    if ((s = check_local_operands(*st, dev, M, N, K, A, lda, B, ldb, false, false)) != GEMM_OK) return s;
+#endif
     cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
-    if (K == 0) {
-        const int64_t total = M * N;
-        int64_t blocks = cdiv(total, 256);
-        if (blocks > int64_t(st->sms) * 8) blocks = int64_t(st->sms) * 8;
-        zero_fill_kernel<<<dim3(uint32_t(blocks)), dim3(256), 0, stream>>>(C, M, N, ldc);
-        if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
-        return GEMM_OK;
-    }
+    if (K == 0) return zero_fill(*st, M, N, C, ldc, stream);
     const gemm_f16_nt_options_t ro = resolve_options(nullptr, N, lda, ldb);
     gemm_f16_nt_plan_t pl;
-    if ((s = make_plan(M, N, K, st->sms, resident_clusters_for(*st, ro), &ro, &pl)) != GEMM_OK) return s;
+    // As in gemm_f16_nt, a call made under stream capture is planned without
+    // the stream-K split: a replay would repeat the launch id that tags the
+    // split's completion flags in the shared scratch.
+    if ((s = plan_call(*st, M, N, K, stream, ro, true, &pl)) != GEMM_OK) return s;
     void* ws = nullptr;
     if (pl.sk_tiles > 0) {
         if (uint64_t(pl.workspace_bytes) > kStaticScratchBytes) return GEMM_ERR_SCRATCH_LIMIT;
@@ -1286,9 +1476,7 @@ gemm_status_t run_noalloc(int64_t M, int64_t N, int64_t K, const uint16_t* A, in
     // Nothing in the scratch has to start at zero: each launch's completion
     // flags carry that launch's own 64-bit id, so values left by an earlier
     // call never match, and every partial tile is written before it is read.
-    if (ro.cluster_pairs == 2)
-        return launch<Cfg2x2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
-    return launch<Cfg2>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
+    return launch_any(false, pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, ws);
 }
 
 }  // namespace g16
@@ -1357,7 +1545,28 @@ G16_EXPORT gemm_status_t gemm_f16_nt_device_limits(int32_t* sms, int32_t* reside
     return GEMM_OK;
 }
 
-G16_EXPORT const char* gemm_f16_nt_status_string(int32_t status) {
+G16_EXPORT gemm_status_t gemm_f16_nt_debug_status(void* stream) {
+    return gemm_f16_nt_device_status(stream, nullptr);
+}
+
+G16_EXPORT gemm_status_t gemm_f16_nt_device_workspace(int32_t* slots, int64_t* bytes_per_slot) {
+    g16::DeviceState* st = nullptr;
+    gemm_status_t s = g16::current_device(&st);
+    if (s != GEMM_OK) return s;
+    if (slots) *slots = st->ws_slots;
+    if (bytes_per_slot) *bytes_per_slot = st->ws_bytes;
+    return GEMM_OK;
+}
+
+G16_EXPORT int32_t gemm_f16_nt_multicast_available(void) { return G16_MCAST_LIB ? 1 : 0; }
+
+G16_EXPORT gemm_status_t gemm_f16_nt_launch_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                                 void* stream, const gemm_f16_nt_options_t* opts,
+                                                 gemm_f16_nt_plan_t* plan) {
+    return g16::launch_plan(M, N, K, lda, ldb, stream, opts, plan);
+}
+
+G16_EXPORT const char* gemm_f16_nt_status_string(gemm_status_t status) {
     switch (status) {
         case GEMM_OK: return "GEMM_OK";
         case GEMM_ERR_INVALID_VALUE: return "GEMM_ERR_INVALID_VALUE: size or leading dimension out of range, or NULL pointer";
@@ -1368,6 +1577,9 @@ G16_EXPORT const char* gemm_f16_nt_status_string(int32_t status) {
         case GEMM_ERR_SCRATCH_LIMIT:
             return "GEMM_ERR_SCRATCH_LIMIT: the problem's stream-K scratch exceeds the 20 MiB static array "
                    "of gemm_f16_nt_noalloc; use gemm_f16_nt";
+        case GEMM_ERR_NOT_LOCAL:
+            return "GEMM_ERR_NOT_LOCAL: the multicast library takes only operands in device memory of the "
+                   "current device, in a process that sees one GPU";
         default: return "unknown gemm_status_t";
     }
 }

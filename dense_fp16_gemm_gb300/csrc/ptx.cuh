@@ -143,18 +143,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
         :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
-// The CTA-pair form with multicast: the data lands at the same offset in the
-// shared memory of every CTA in `cta_mask`, and each destination's completion
-// bytes go to the barrier at `bar`'s offset in the leader CTA of that
-// destination's pair.
-__device__ __forceinline__ void tma_load_2d_pair_mcast(uint32_t dst, const void* tmap, int32_t x,
-                                                       int32_t y, uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;"
-        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
-        : "memory");
-}
 // An L2 cache policy that keeps lines resident in preference to others.
 __device__ __forceinline__ uint64_t policy_evict_last() {
     uint64_t p;

@@ -122,3 +122,16 @@ def draw_bf16(shape, dist: tuple, seed: int, ld: int | None = None) -> np.ndarra
 def operands(w: Workload):
     """(A [M,K], B [N,K]) for a workload, contiguous float16."""
     return draw((w.M, w.K), w.dist_a, w.seed_a), draw((w.N, w.K), w.dist_b, w.seed_b)
+
+
+def draw_device_ints(shape, lo: int, hi: int, seed: int, device):
+    """A float16 torch tensor of `shape` on `device`, integers uniform on
+    {lo..hi} from torch's own generator for that device seeded with `seed`.
+
+    For operands too large to draw on the host (tens of GB); reproducible for a
+    given seed, device type and torch version.  Rows can be copied to the host
+    for the oracle."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    return torch.randint(lo, hi + 1, tuple(shape), generator=gen, device=device, dtype=torch.float16)

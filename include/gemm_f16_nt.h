@@ -20,6 +20,13 @@
  *
  * Threading: every entry point may be called from any host thread.  Each GEMM
  * call is asynchronous on the given stream.
+ *
+ * Two builds share this header.  libgemm_f16_nt.so is the library; it issues
+ * no multicast copy and may be loaded by each of several processes on several
+ * GPUs.  libgemm_f16_nt_mcast.so, built only on request, is the same library
+ * plus clusters of two CTA pairs that share A by TMA multicast (cluster_pairs
+ * below); it is for single-GPU processes and refuses any other use
+ * (GEMM_ERR_NOT_LOCAL).
  */
 #ifndef GEMM_F16_NT_H_
 #define GEMM_F16_NT_H_
@@ -37,7 +44,9 @@ typedef enum {
     GEMM_ERR_UNSUPPORTED_DEVICE = 3, /* no CUDA device, or the current device is not compute capability 10.3 */
     GEMM_ERR_LAUNCH = 4,             /* the CUDA runtime or driver refused a call (set-up or launch) */
     GEMM_ERR_TIMEOUT = 5,            /* the device watchdog word is set (see gemm_f16_nt_device_status) */
-    GEMM_ERR_SCRATCH_LIMIT = 6       /* gemm_f16_nt_noalloc: the scratch needed exceeds its static array */
+    GEMM_ERR_SCRATCH_LIMIT = 6,      /* gemm_f16_nt_noalloc: the scratch needed exceeds its static array */
+    GEMM_ERR_NOT_LOCAL = 7           /* multicast library only: an operand is not device memory of the
+                                        current device, or the process sees more than one GPU */
 } gemm_status_t;
 
 /*
@@ -63,12 +72,21 @@ typedef enum {
  * C must not overlap A or B (not checked).
  *
  * Ownership: the caller owns A, B and C and keeps them alive until the work on
- * `stream` completes.  The library keeps no pointer after the call returns.
- * The first call on a device performs one-time set-up on that device (device
- * query, kernel attributes, the watchdog word's address, a private memory
- * pool); later calls do none.  Shapes whose last wave of output tiles would
- * leave enough SMs idle use a stream-K schedule (see `schedule` below) whose
- * workspace is taken from that pool on `stream` and handed back on it.
+ * `stream` completes.  The library keeps no pointer after the call returns,
+ * and allocates nothing per call.  The first call on a device performs
+ * one-time set-up on that device: device query, kernel attributes, the
+ * watchdog word's address, and the reservation (cudaMalloc) of the stream-K
+ * workspace, GEMM_F16_NT_WORKSPACE_SLOTS slots (environment variable, 0..8,
+ * default 4) of about 20 MB each on a 152-SM GPU, kept until the process exits
+ * (gemm_f16_nt_device_workspace reports them).  Shapes whose last wave of
+ * output tiles would leave enough SMs idle use a stream-K schedule (see
+ * `schedule` below) that takes one slot, round-robin.  Before such a launch
+ * the call makes `stream` wait for the previous launch that used the same slot
+ * (cudaStreamWaitEvent on an event the call records after each launch), so
+ * calls on unordered streams never use one slot at the same time: up to that
+ * many stream-K calls run concurrently, and more are ordered.  If the
+ * reservation fails, or the environment variable is 0, every call is planned
+ * without the split; gemm_f16_nt_launch_plan reports it (split_k_off = 2).
  *
  * Ordering: the kernel is launched with programmatic stream serialization, so
  * its CTAs may start their set-up (shared memory, barriers, tensor memory)
@@ -80,10 +98,11 @@ typedef enum {
  * Stream capture: a call made while `stream` is being captured into a CUDA
  * graph is planned without the stream-K split (schedule 2 included), because
  * a replay repeats the launch's parameters and the split's completion flags
- * are tagged per launch.  The captured kernel then touches only A, B, C, the
- * watchdog word and (if requested) the trace buffer, so the graph can be
- * replayed any number of times.  Make the first call on a device outside any
- * capture: it sets the device up (kernel attributes, the memory pool).
+ * are tagged per launch (split_k_off = 1 in gemm_f16_nt_launch_plan).  The
+ * captured kernel then touches only A, B, C, the watchdog word and (if
+ * requested) the trace buffer, so the graph can be replayed any number of
+ * times.  Make the first call on a device outside any capture: it sets the
+ * device up (kernel attributes, the workspace reservation).
  *
  * Errors: invalid arguments are reported before anything is enqueued, and C is
  * left unchanged.  The call returns after enqueueing; a fault during execution
@@ -104,11 +123,12 @@ gemm_status_t gemm_f16_nt(int64_t M, int64_t N, int64_t K,
  * No counterpart in the tutorial pages: this is an interface choice of the
  * library, not part of the method.
  *
- * Who needs it: gemm_f16_nt takes the stream-K workspace (up to about 20 MB)
- * from a memory pool of its own.  Some callers cannot let a library allocate:
- * processes whose device memory is reserved up front by their own allocator,
- * so that an extra allocation can fail or fragment it, and latency-critical
- * loops that cannot afford an allocation's cost or implicit synchronisation.
+ * Who needs it: gemm_f16_nt reserves its stream-K workspace (four slots of
+ * about 20 MB) with cudaMalloc on its first call on a device.  Some callers
+ * cannot let a library allocate at all, not even once: processes whose device
+ * memory is reserved up front by their own allocator, so that an extra
+ * allocation can fail or fragment it, and latency-critical loops whose first
+ * call must not pay an allocation's cost or implicit synchronisation.
  * This entry point computes the same product with the same kernel and the same
  * schedule, and takes no memory at all during the call: its scratch is a
  * fixed array of 20 MiB (20,971,520 bytes) compiled into the library, which
@@ -128,6 +148,8 @@ gemm_status_t gemm_f16_nt(int64_t M, int64_t N, int64_t K,
  *   - A problem whose stream-K scratch would exceed the array (possible only
  *     on GPUs with more than 152 SMs) is rejected with GEMM_ERR_SCRATCH_LIMIT
  *     before anything is enqueued.
+ *   - Like gemm_f16_nt, a call made while `stream` is capturing is planned
+ *     without the stream-K split, so it does not use the array.
  */
 gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
                                   const uint16_t *A, int64_t lda,
@@ -150,8 +172,14 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  *                 (see gemm_f16_nt_tile_coord).  Range 1..64; default 8.
  *   max_clusters  upper bound on the persistent grid, in CTA pairs (or CTAs
  *                 for cta_group 1); 0 = as many as can be resident.
- *   timeout_ns    watchdog limit for any single pipeline wait, in ns
- *                 (default 1 s).
+ *   timeout_ns    watchdog limit, in ns, for a wait on one pipeline stage
+ *                 (default 1 s).  Waits that can last a whole work item (the
+ *                 epilogue's wait for a finished accumulator, a stream-K
+ *                 owner's wait for its partners' partial tiles, the MMA
+ *                 issuer's wait for a drained accumulator and the producer's
+ *                 wait for a free stage behind it) get timeout_ns plus 8 us
+ *                 per 64-wide k-block of K, so that deep-K problems finish:
+ *                 K = 2^30 allows each of them about 134 s.
  *   inject_stall  test hook: if nonzero the TMA producers issue nothing, so
  *                 every consumer wait runs into the watchdog; the kernel then
  *                 sets the watchdog word, releases its tensor memory and
@@ -188,10 +216,10 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  *                 when 2R <= clusters.  Only with one CTA pair per cluster and
  *                 B stored [N, K].
  *                 A stream-K launch needs a workspace (gemm_f16_nt_plan's
- *                 workspace_bytes); the call takes it from a memory pool
- *                 private to this library on `stream` (cudaMallocFromPoolAsync)
- *                 and returns it on the same stream after the launch.  If the
- *                 pool cannot supply it the call runs whole tiles only.
+ *                 workspace_bytes): one of the slots reserved at the device's
+ *                 set-up (see Ownership above).  Without slots, or under
+ *                 stream capture, the call is planned as with schedule 0 but
+ *                 with no stream-K split (plan field split_k_off).
  *   trace, trace_items
  *                 debugging aid: if `trace` is a device pointer to
  *                 clusters × trace_items × 8 uint64 (zeroed by the caller), the
@@ -204,15 +232,17 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  *                 (stamps from the leader CTA's MMA thread and one of its
  *                 epilogue warps), j=7 total ns the MMA thread waited for
  *                 filled pipeline stages during the item.
- *   cluster_pairs 1: a cluster is one CTA pair; 2: a cluster is two CTA
- *                 pairs side by side in N (a 256×512 tile) that share their A
- *                 rows: each CTA loads half of its A tile and TMA multicasts it
- *                 to the same-rank CTA of the other pair, which halves A's
- *                 L2 → SM traffic.  Clusters of four CTAs fit on fewer SMs (144
- *                 of 152 on a GB300).  Needs cta_group 2.  Default (0): 2 when
- *                 lda or ldb is not a multiple of 64 elements (128 bytes: each
- *                 128-byte row slice of a tile then spans two L2 lines and L2
- *                 traffic is the limit) and N > 256, else 1.
+ *   cluster_pairs 1: a cluster is one CTA pair; 2 (multicast library only;
+ *                 GEMM_ERR_INVALID_VALUE in libgemm_f16_nt.so): a cluster is
+ *                 two CTA pairs side by side in N (a 256×512 tile) that share
+ *                 their A rows: each CTA loads half of its A tile and TMA
+ *                 multicasts it to the same-rank CTA of the other pair, which
+ *                 halves A's L2 → SM traffic.  Clusters of four CTAs fit on
+ *                 fewer SMs (144 of 152 on a GB300).  Needs cta_group 2.
+ *                 Default (0): 1 in libgemm_f16_nt.so; in the multicast
+ *                 library 2 when lda or ldb is not a multiple of 64 elements
+ *                 (128 bytes: each 128-byte row slice of a tile then spans two
+ *                 L2 lines and L2 traffic is the limit) and N > 256, else 1.
  *   a_layout      0 (default): A is stored [M, K], element (m, k) at
  *                 A[m*lda + k]; 1: A is stored [K, M] (M contiguous), element
  *                 (m, k) at A[k*lda + m], lda >= M.
@@ -303,18 +333,31 @@ gemm_status_t gemm_bf16_nt_ex(int64_t M, int64_t N, int64_t K,
  */
 gemm_status_t gemm_f16_nt_device_status(void *stream, uint32_t *flags);
 
+/* gemm_f16_nt_device_status(stream, NULL): GEMM_OK if no wait expired since
+ * the word was last read, GEMM_ERR_TIMEOUT if one did (the word is cleared). */
+gemm_status_t gemm_f16_nt_debug_status(void *stream);
+
+/* The stream-K workspace reserved on the current device at its set-up: the
+ * number of slots (0: the split is off for every call) and the bytes of each.
+ * Either pointer may be NULL. */
+gemm_status_t gemm_f16_nt_device_workspace(int32_t *slots, int64_t *bytes_per_slot);
+
+/* 1 in the multicast library (libgemm_f16_nt_mcast.so), 0 in libgemm_f16_nt.so. */
+int32_t gemm_f16_nt_multicast_available(void);
+
 /*
  * What the one-time set-up found on the current device: its SM count and how
  * many clusters of the GEMM kernel can be resident at once (the persistent
  * grid sizes): CTA pairs (cta_group 2), single CTAs (cta_group 1), and
- * clusters of two pairs (cluster_pairs 2).  Any pointer may be NULL.
+ * clusters of two pairs (cluster_pairs 2; 0 in libgemm_f16_nt.so, which has
+ * no such configuration).  Any pointer may be NULL.
  * GEMM_ERR_UNSUPPORTED_DEVICE without a usable device.
  */
 gemm_status_t gemm_f16_nt_device_limits(int32_t *sms, int32_t *resident_pairs,
                                         int32_t *resident_ctas, int32_t *resident_pair_pairs);
 
 /* A static, human-readable name for a gemm_status_t value. */
-const char *gemm_f16_nt_status_string(int32_t status);
+const char *gemm_f16_nt_status_string(gemm_status_t status);
 
 /* ---- host-only helpers (no CUDA call; used by the scheduler and its tests) ---- */
 
@@ -345,12 +388,27 @@ typedef struct {
     int64_t workspace_bytes; /* device workspace a stream-K launch needs (0 if none) */
     int32_t tail_tiles;    /* the last tail_tiles tiles are each split in N (N-split) ... */
     int32_t tail_split;    /* ... into tail_split narrower tiles (1 = no split) */
+    int32_t split_k_off;   /* gemm_f16_nt_launch_plan only: 0, or why the shape's stream-K
+                              split is not taken: 1 the stream is capturing, 2 no workspace
+                              was reserved on the device */
 } gemm_f16_nt_plan_t;
 
 gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms,
                                int32_t max_clusters,
                                const gemm_f16_nt_options_t *opts,
                                gemm_f16_nt_plan_t *plan);
+
+/*
+ * The plan gemm_f16_nt_ex(M, N, K, A, lda, B, ldb, …, stream, opts) would
+ * launch on the current device right now: the device's SM count and resident
+ * clusters, the automatic choices for these leading dimensions, and the
+ * split's availability (stream capture, reserved workspace; see split_k_off).
+ * Performs the device's one-time set-up if it has not happened yet.  Errors
+ * as gemm_f16_nt_plan, plus GEMM_ERR_UNSUPPORTED_DEVICE and GEMM_ERR_LAUNCH.
+ */
+gemm_status_t gemm_f16_nt_launch_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                      void *stream, const gemm_f16_nt_options_t *opts,
+                                      gemm_f16_nt_plan_t *plan);
 
 /*
  * One work item of the persistent schedule (gemm_f16_nt_schedule).

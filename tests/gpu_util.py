@@ -30,3 +30,10 @@ def empty_out(M: int, N: int, ld: int | None = None, extra_rows: int = 0, fill=f
         ld += (-ld) % 8
     buf = torch.full((M + extra_rows, ld), fill, dtype=torch.float16, device="cuda:0")
     return buf[:M, :N], buf
+
+
+def lib_for(cluster_pairs: int):
+    """The library that runs a cluster_pairs choice: two CTA pairs per cluster
+    (A shared by TMA multicast) exist only in the single-GPU multicast build."""
+    import dense_fp16_gemm_gb300 as g
+    return g.library_mcast() if cluster_pairs == 2 else g.library()

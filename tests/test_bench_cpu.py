@@ -106,6 +106,25 @@ def test_roofline_byte_figures():
     assert w.compulsory_bytes == 3 * 8192 * 8192 * 2          # A and B read, C written, fp16
     # two pairs per cluster: each pair receives the tile's A rows (multicast), plus 512 B rows
     r = inputs.WORKLOADS["ragged_4000x3000x5000"]
-    pr = g.plan(r.M, r.N, r.K, num_sms=152, max_clusters=36)
+    pr = g.plan(r.M, r.N, r.K, num_sms=152, max_clusters=36, lib=g.library_mcast())
     assert pr["cluster_pairs"] == 2
     assert bench.l2_to_sm_bytes(pr) == pr["num_tiles"] * pr["k_blocks"] * 128 * (2 * 256 + 512)
+
+
+def test_traffic_record_used_only_for_the_same_kernel_source(tmp_path, monkeypatch):
+    """The roofline's DRAM figure comes from a machine-readable record of an
+    Nsight Compute capture, and only while the kernel sources hash the same."""
+    import json
+
+    import bench
+    path = tmp_path / "dram_traffic.json"
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(path))
+    assert bench.recorded_traffic("gemm_8192") == (None, None)
+    rec = {"dram_bytes_per_launch": 1_100_000_000, "kernel_source_sha256_16": bench.kernel_source_hash(),
+           "command": "ncu …", "launches": 1}
+    path.write_text(json.dumps({"gemm_8192": rec}))
+    assert bench.recorded_traffic("gemm_8192")[0] == 1_100_000_000
+    assert bench.recorded_traffic("gemm_4096") == (None, None)
+    rec["kernel_source_sha256_16"] = "0" * 16
+    path.write_text(json.dumps({"gemm_8192": rec}))
+    assert bench.recorded_traffic("gemm_8192") == (None, None)

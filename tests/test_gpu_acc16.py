@@ -22,7 +22,7 @@ import pytest
 
 import oracle
 from dense_fp16_gemm_gb300 import inputs
-from tests.gpu_util import empty_out, to_device, to_host
+from tests.gpu_util import empty_out, lib_for, to_device, to_host
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -41,7 +41,8 @@ def _needs_gpu():
 def run(A, B, **kw):
     M, N = A.shape[0], B.shape[0]
     Cd, Cbuf = empty_out(M, N)
-    g.gemm_f16_nt(to_device(A), to_device(B), Cd, options=g.Options(accumulate=1, **kw))
+    g.gemm_f16_nt(to_device(A), to_device(B), Cd, options=g.Options(accumulate=1, **kw),
+                  lib=lib_for(kw.get("cluster_pairs", 0)))
     torch.cuda.synchronize()
     assert np.isnan(to_host(Cbuf)[:M, N:].astype(np.float32)).all(), "padding columns of C were written"
     return to_host(Cd)

@@ -8,6 +8,7 @@ import pytest
 
 import oracle
 from dense_fp16_gemm_gb300 import inputs
+from tests.gpu_util import lib_for
 from tests.tolerance import bf16_to_f64, check_bitexact, check_close, ulp_bf16
 
 torch = pytest.importorskip("torch")
@@ -44,7 +45,8 @@ def host_bits(t) -> np.ndarray:
 def run(A, B, ldc=None, options=None):
     M, N = A.shape[0], B.shape[0]
     Cbuf = dev_bf16(np.full((M, N), NAN_BF16, dtype=np.uint16), ldc)
-    g.gemm_bf16_nt(dev_bf16(A), dev_bf16(B), Cbuf, options=options)
+    g.gemm_bf16_nt(dev_bf16(A), dev_bf16(B), Cbuf, options=options,
+                   lib=lib_for(options.cluster_pairs if options is not None else 0))
     torch.cuda.synchronize()
     return host_bits(Cbuf)
 

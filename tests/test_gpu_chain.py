@@ -16,6 +16,7 @@ import numpy as np
 import pytest
 
 from dense_fp16_gemm_gb300 import inputs
+from tests.gpu_util import lib_for
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -57,7 +58,7 @@ def test_chained_permutations_are_exact(M, KN, schedule, pairs, bf16):
     o = g.Options(schedule=schedule, cluster_pairs=pairs)
     torch.cuda.synchronize()
     for t in range(steps):
-        fn(X[t % 2], P, X[(t + 1) % 2], options=o)
+        fn(X[t % 2], P, X[(t + 1) % 2], options=o, lib=lib_for(pairs))
     torch.cuda.synchronize()
     idx = np.arange(KN)
     for _ in range(steps):

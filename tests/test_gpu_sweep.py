@@ -18,6 +18,7 @@ import pytest
 
 import oracle
 from dense_fp16_gemm_gb300 import inputs
+from tests.gpu_util import lib_for
 from tests.tolerance import bf16_to_f64, check_bitexact, check_close, ulp_bf16
 
 torch = pytest.importorskip("torch")
@@ -89,7 +90,7 @@ def test_random_configuration(c):
     o = g.Options(cta_group=c["cg"], cluster_pairs=c["cp"], schedule=c["schedule"],
                   a_layout=c["a_layout"], b_layout=c["b_layout"], accumulate=int(c["acc16"]))
     g.gemm_f16_nt_ptr(M, N, K, Ad.data_ptr(), lda, Bd.data_ptr(), ldb, Cd.data_ptr(), ldc,
-                      torch.cuda.current_stream().cuda_stream, o, bf16=dt == "bf16")
+                      torch.cuda.current_stream().cuda_stream, o, bf16=dt == "bf16", lib=lib_for(c["cp"]))
     torch.cuda.synchronize()
     out = Cd.cpu().numpy().view(np.uint16)
     assert np.all(out[:M, N:] == NAN[dt]), "padding columns of C were written"

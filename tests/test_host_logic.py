@@ -186,41 +186,52 @@ def test_plan_n_split():
     assert (p["tail_tiles"], p["tail_split"]) == (12, 4)
     assert g.plan(256 * 15, 256 * 10, 4096, options=g.Options(schedule=3))["tail_split"] == 1   # R = 74
     # not with two pairs per cluster, one CTA, B stored [K, N], or another forced schedule
-    for o in (g.Options(cluster_pairs=2), g.Options(cta_group=1), g.Options(b_layout=1),
-              g.Options(schedule=1), g.Options(schedule=2)):
+    mc = g.library_mcast()
+    assert g.plan(256, 256, 256, options=g.Options(cluster_pairs=2), lib=mc)["tail_split"] == 1
+    for o in (g.Options(cta_group=1), g.Options(b_layout=1), g.Options(schedule=1), g.Options(schedule=2)):
         assert g.plan(256, 256, 256, options=o)["tail_split"] == 1
     # the fp16 accumulator may use it (each output's sum is unchanged)
     assert g.plan(256, 256, 256, options=g.Options(accumulate=1))["tail_split"] == 4
 
 
 def test_plan_two_pairs_per_cluster():
+    # only the single-GPU multicast build has two pairs per cluster
     o = g.Options(cluster_pairs=2)
-    p = g.plan(8192, 8192, 8192, num_sms=152, max_clusters=36, options=o)
+    with pytest.raises(g.GemmError):
+        g.plan(8192, 8192, 8192, num_sms=152, max_clusters=36, options=o)
+    mc = g.library_mcast()
+    assert (mc.gemm_f16_nt_multicast_available(), g.library().gemm_f16_nt_multicast_available()) == (1, 0)
+    p = g.plan(8192, 8192, 8192, num_sms=152, max_clusters=36, options=o, lib=mc)
     assert (p["cluster_pairs"], p["tile_m"], p["tile_n"]) == (2, 256, 512)
     assert (p["m_tiles"], p["n_tiles"], p["num_tiles"]) == (32, 16, 512)
     assert (p["clusters"], p["grid_ctas"]) == (36, 144)
     assert p["sk_tiles"] == 0                           # auto: two pairs keep whole tiles
     o = g.Options(cluster_pairs=2, schedule=2)
-    p = g.plan(8192, 8192, 8192, num_sms=152, max_clusters=36, options=o)
+    p = g.plan(8192, 8192, 8192, num_sms=152, max_clusters=36, options=o, lib=mc)
     assert p["sk_tiles"] == 512 % 36 + 36               # forced: last wave 8/36 + one wave
     assert p["workspace_bytes"] == 36 * 4 * 4 * 8 + 36 * 4 * 128 * 256 * 4
-    p = g.plan(4000, 3000, 5000, num_sms=152, max_clusters=36, options=o)
+    p = g.plan(4000, 3000, 5000, num_sms=152, max_clusters=36, options=o, lib=mc)
     assert (p["m_tiles"], p["n_tiles"]) == (16, 6)
-    with pytest.raises(g.GemmError):
-        g.plan(256, 256, 256, options=g.Options(cluster_pairs=2, cta_group=1))
-    with pytest.raises(g.GemmError):
-        g.plan(256, 256, 256, options=g.Options(cluster_pairs=3))
+    # K = 5000: 10,000-byte rows are not 128-byte multiples, so the multicast
+    # build's default shares A between two pairs (256 x 512 cluster tiles);
+    # the default build keeps one pair
+    p = g.plan(4000, 3000, 5000, lib=mc)
+    assert (p["cluster_pairs"], p["m_tiles"], p["n_tiles"]) == (2, 16, 6)
+    assert g.plan(8192, 8192, 8192, lib=mc)["cluster_pairs"] == 1
+    assert g.plan(4000, 256, 5000, lib=mc)["cluster_pairs"] == 1      # too narrow for two pairs
+    for lib in (mc, g.library()):
+        with pytest.raises(g.GemmError):
+            g.plan(256, 256, 256, options=g.Options(cluster_pairs=2, cta_group=1), lib=lib)
+        with pytest.raises(g.GemmError):
+            g.plan(256, 256, 256, options=g.Options(cluster_pairs=3), lib=lib)
 
 
 def test_plan_edges_and_options():
     p = g.plan(4000, 3000, 5000, options=g.Options(cluster_pairs=1))
     assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (16, 12, 79)
-    # K = 5000: 10,000-byte rows are not 128-byte multiples, so by default two
-    # pairs share A through multicast (256 x 512 cluster tiles)
+    # the default build has one pair per cluster for every pitch
     p = g.plan(4000, 3000, 5000)
-    assert (p["cluster_pairs"], p["m_tiles"], p["n_tiles"]) == (2, 16, 6)
-    assert g.plan(8192, 8192, 8192)["cluster_pairs"] == 1
-    assert g.plan(4000, 256, 5000)["cluster_pairs"] == 1      # too narrow for two pairs
+    assert (p["cluster_pairs"], p["m_tiles"], p["n_tiles"]) == (1, 16, 12)
     p = g.plan(100, 100, 8)                        # one pair tile, rank-1 rows all out of range,
     # cut into four 64-column slices (the last two lie wholly past N and store nothing)
     assert (p["num_tiles"], p["clusters"], p["grid_ctas"], p["tail_split"]) == (1, 4, 8, 4)
@@ -308,3 +319,16 @@ def test_without_a_gpu_valid_calls_report_no_device():
         pytest.skip("a GPU is present; this case is for GPU-less hosts")
     assert call(128, 128, 64) == 3
     assert g.library().gemm_f16_nt_device_status(None, None) == 3
+
+
+def test_noalloc_scratch_limit_condition():
+    """gemm_f16_nt_noalloc keeps its stream-K scratch in a fixed 20 MiB array and
+    rejects (GEMM_ERR_SCRATCH_LIMIT) a plan whose workspace exceeds it.  On a
+    152-SM GB300 no plan does; on a GPU with more SMs the same shape would."""
+    limit = 20 << 20
+    for sms in (148, 152):
+        for shape in ((4096, 4096, 4096), (6144, 4096, 4096), (1024, 1024, 8192), (256, 256, 1 << 20)):
+            for o in (g.Options(), g.Options(schedule=2), g.Options(cta_group=1, schedule=2)):
+                assert g.plan(*shape, num_sms=sms, options=o)["workspace_bytes"] <= limit
+    big = g.plan(4096, 4096, 4096, num_sms=176, options=g.Options(schedule=2))
+    assert big["workspace_bytes"] > limit

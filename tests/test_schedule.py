@@ -32,7 +32,8 @@ CASES = [
     (1024, 1024, 8192, {}, 64),                       # 16 tiles cut in k
     (1024, 1024, 1024, {}, 76),
     (4096, 4096, 1024, {}, 76),                       # shallow last wave: N-split
-    (4000, 3000, 5000, {}, 36),                       # two pairs per cluster
+    (4000, 3000, 5000, {"_lib": "mcast"}, 36),        # two pairs per cluster (multicast build's default)
+    (4000, 3000, 5000, {}, 76),                       # one pair: the default build
     (4000, 3000, 5000, {"schedule": 2, "cluster_pairs": 1}, 76),
     (300, 520, 328, {"schedule": 2}, 76),
     (1300, 1000, 320, {"schedule": 3, "cluster_pairs": 1}, 76),
@@ -64,9 +65,16 @@ CASES = CASES + _random_cases()
 
 
 def _all_items(M, N, K, opts, max_clusters):
+    """The plan and every cluster's items.  Two pairs per cluster exist only in
+    the multicast build, whose schedule code is the same source; it is asked
+    for them explicitly (cluster_pairs 2) or by "_lib"."""
+    opts = dict(opts)
+    lib = opts.pop("_lib", None)
+    lib = g.library_mcast() if (lib == "mcast" or opts.get("cluster_pairs") == 2) else g.library()
     o = g.Options(**opts)
-    pl = g.plan(M, N, K, max_clusters=max_clusters, options=o)
-    items = [g.schedule(M, N, K, c, max_clusters=max_clusters, options=o) for c in range(pl["clusters"])]
+    pl = g.plan(M, N, K, max_clusters=max_clusters, options=o, lib=lib)
+    items = [g.schedule(M, N, K, c, max_clusters=max_clusters, options=o, lib=lib)
+             for c in range(pl["clusters"])]
     return pl, items
 
 
