@@ -69,7 +69,8 @@ class Plan(ctypes.Structure):
                 ("smem_bytes", ctypes.c_int32), ("tmem_cols", ctypes.c_int32),
                 ("sk_tiles", ctypes.c_int32), ("cluster_pairs", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("tail_tiles", ctypes.c_int32),
-                ("tail_split", ctypes.c_int32), ("split_k_off", ctypes.c_int32)]
+                ("tail_split", ctypes.c_int32), ("split_k_off", ctypes.c_int32),
+                ("split_pieces", ctypes.c_int32)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -79,7 +80,8 @@ class Item(ctypes.Structure):
     """gemm_f16_nt_item_t: one work item of a persistent cluster."""
     _fields_ = [("tile", ctypes.c_int32), ("m_tile", ctypes.c_int32), ("n_tile", ctypes.c_int32),
                 ("kb0", ctypes.c_int32), ("kb1", ctypes.c_int32), ("kind", ctypes.c_int32),
-                ("part", ctypes.c_int32), ("parts", ctypes.c_int32), ("partners", ctypes.c_int32)]
+                ("part", ctypes.c_int32), ("parts", ctypes.c_int32), ("partners", ctypes.c_int32),
+                ("piece", ctypes.c_int32), ("pieces", ctypes.c_int32)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -144,6 +144,7 @@ struct Ctl {
     uint64_t acc_full[2];       // accumulator ready for the epilogue
     uint64_t acc_empty[2];      // accumulator drained               — leader CTA's copy is used
     uint64_t mma_done;          // all MMAs retired (teardown)
+    uint64_t xfer[kEpiWarps];   // split pieces: partial slices landed in an epilogue warp's scratch
     uint32_t tmem_base;
     uint32_t abort_flag;
 };
@@ -177,6 +178,7 @@ struct Params {
     // tiles of BN/tail_split columns (tail_first = num_tiles: no split)
     uint32_t tail_first;
     uint32_t tail_split;
+    uint32_t split_pieces; // > 1: each cluster runs one split piece of tile cluster / split_pieces
     uint64_t* trace;       // optional per-item timestamps (debugging)
     uint32_t trace_items;
 };
@@ -327,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
             ptx::mbar_init(acce0 + 8 * b, kEpiWarps * CG);     // every epilogue warp of the pair
         }
         ptx::mbar_init(mma_done, 1);
+        for (int e = 0; e < kEpiWarps; ++e) ptx::mbar_init(ptx::smem_u32(&ctl->xfer[e]), 1);
         ctl->abort_flag = 0u;
         ptx::fence_mbarrier_init();
     }
@@ -583,9 +586,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
         // A partial tile in workspace slot `slot` is stored as float4 groups of
         // columns, row innermost: [col/4][128 rows], so that the 32 lanes of a
         // warp (32 consecutive rows) touch 512 contiguous bytes per access.
+        // Layout [slot][cta rank][epilogue warp][BN/4 column groups][32 rows]:
+        // a warp's partial rows are contiguous, 8 KB per 64 columns, and the 32
+        // lanes (rows) of one float4 column group touch 512 contiguous bytes.
         auto partial_f4 = [&](uint32_t slot, uint32_t col4) {
             return reinterpret_cast<float4*>(p.partials) +
-                   ((size_t(slot) * NCTA + rank) * (BN / 4) + col4) * kBlockM + q * 32u + lane;
+                   (((size_t(slot) * NCTA + rank) * kEpiWarps + q) * (BN / 4) + col4) * 32u + lane;
         };
         uint32_t acc = 0, acc_phase = 0, ob = 0;
         Work work;
@@ -607,6 +613,161 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
             if (!ok) break;
             ptx::tc_fence_after();
             if (tr) tr[4] = ptx::globaltimer();
+            if constexpr (!Cfg::kA16) {
+                if (it.kind == kItemSplitPiece) {
+                    // One of `np` split pieces of the tile, all running at once on
+                    // clusters first .. first+np-1.  The tile's BN columns are cut
+                    // into np contiguous slices, piece i owning slice i.  The
+                    // pieces exchange partials through the workspace with bulk
+                    // copies, staged in this warp's share of the ring (idle now:
+                    // a split piece is its cluster's only item, and its last
+                    // stage was consumed before the accumulator was ready):
+                    //  1. the fp32 partials of the slices other pieces own are
+                    //     written to scratch and stored to this cluster's slot;
+                    //  2. once they are complete, a release flag publishes them;
+                    //  3. after the same warp of every other piece has published,
+                    //     their partials of this piece's slice are loaded back
+                    //     together, summed with its own in piece order (k order)
+                    //     and stored to C.
+                    const uint32_t np = it.pieces, pc = it.piece, first = cluster - pc;
+                    const uint32_t tacc = tmem_base + lane_off + acc * uint32_t(BN);
+                    const uint32_t own0 = pc * (BN / 32) / np, own1 = (pc + 1) * (BN / 32) / np;  // 32-col slices
+                    constexpr uint32_t kScratch = Cfg::kRingBytes / kEpiWarps;
+                    static_assert(kScratch >= 7 * 4096 && kScratch >= (BN / 32) * 4096, "split-piece scratch");
+                    const uint32_t scr = sA + q * kScratch;    // ring is [sA, sA + kRingBytes)
+                    // 1. partial slices for the other pieces, 4 KB each: [8 column groups][32 rows] float4
+                    uint32_t nst = 0;
+#pragma unroll 1
+                    for (uint32_t c = 0; c < uint32_t(BN / 64); ++c) {
+                        const bool own_lo = 2 * c >= own0 && 2 * c < own1;
+                        const bool own_hi = 2 * c + 1 >= own0 && 2 * c + 1 < own1;
+                        if (own_lo && own_hi) continue;
+                        uint32_t lo[32], hi[32];
+                        ptx::tmem_ld_32x32b_x32(tacc + 64 * c, lo);
+                        ptx::tmem_ld_32x32b_x32(tacc + 64 * c + 32, hi);
+                        ptx::tmem_wait_ld();
+                        ptx::reg_fence(lo);
+                        ptx::reg_fence(hi);
+                        const uint32_t blk = scr + 8192u * c;    // scratch mirrors the slot's layout
+                        if (!own_lo)
+#pragma unroll
+                            for (int k = 0; k < 8; ++k)
+                                ptx::st_shared_v4(blk + (uint32_t(k) * 32u + lane) * 16u, lo[4 * k], lo[4 * k + 1],
+                                                  lo[4 * k + 2], lo[4 * k + 3]);
+                        if (!own_hi)
+#pragma unroll
+                            for (int k = 0; k < 8; ++k)
+                                ptx::st_shared_v4(blk + 4096u + (uint32_t(k) * 32u + lane) * 16u, hi[4 * k],
+                                                  hi[4 * k + 1], hi[4 * k + 2], hi[4 * k + 3]);
+                        nst += (own_lo ? 0u : 1u) + (own_hi ? 0u : 1u);
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        for (uint32_t j = 0; j < uint32_t(BN / 32); ++j)
+                            if (j < own0 || j >= own1)
+                                ptx::bulk_store(partial_f4(cluster, 8 * j) - lane, scr + 4096u * j, 4096u);
+                        ptx::bulk_commit_group();
+                        ptx::bulk_wait_group_all();          // the partials are in global memory
+                        ptx::fence_proxy_async_global();
+                        __threadfence();
+                        ptx::st_release_u64(p.flags + (size_t(cluster) * NCTA + rank) * kEpiWarps + q, p.launch_id);
+                    }
+                    // 2-3. wait for the other pieces, then load their partials of this slice
+                    uint32_t okf = 1;
+                    if (lane == 0) {
+                        for (uint32_t i = 0; i < np && okf; ++i)
+                            if (i != pc)
+                                okf = wait_flag(p.flags + (size_t(first + i) * NCTA + rank) * kEpiWarps + q,
+                                                p.launch_id, wi, kSiteStreamK) ? 1u : 0u;
+                        if (okf) {
+                            ptx::fence_proxy_async_global();
+                            const uint32_t nown = own1 - own0;
+                            const uint32_t xb = ptx::smem_u32(&ctl->xfer[q]);
+                            ptx::mbar_arrive_expect_tx(xb, (np - 1) * nown * 4096u);
+                            for (uint32_t i = 0, slot = 0; i < np; ++i) {
+                                if (i == pc) continue;
+                                for (uint32_t jj = 0; jj < nown; ++jj)
+                                    ptx::bulk_load(scr + (slot * nown + jj) * 4096u,
+                                                   partial_f4(first + i, 8 * (own0 + jj)) - lane, 4096u, xb);
+                                ++slot;
+                            }
+                        }
+                    }
+                    okf = __shfl_sync(0xffffffffu, okf, 0);
+                    (void)nst;
+                    if (!okf) break;
+                    // every lane observes the loads' completion (each reads the scratch)
+                    if (!wait(ptx::smem_u32(&ctl->xfer[q]), 0, wi, kSiteStreamK)) break;
+                    const int32_t r = row0 + int32_t(lane);
+                    const uint32_t nown = own1 - own0;
+#pragma unroll 1
+                    for (uint32_t jj = 0; jj < nown; ++jj) {
+                        const uint32_t j = own0 + jj;
+                        uint32_t v[32];
+                        ptx::tmem_ld_32x32b_x32(tacc + 32 * j, v);
+                        ptx::tmem_wait_ld();
+                        ptx::reg_fence(v);
+                        float sum[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) sum[e] = 0.0f;
+                        for (uint32_t i = 0, slot = 0; i < np; ++i) {
+                            if (i == pc) {
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) sum[e] += __uint_as_float(v[e]);
+                                continue;
+                            }
+                            const uint32_t blk = scr + (slot * nown + jj) * 4096u;
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                float4 t;
+                                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                             : "=f"(t.x), "=f"(t.y), "=f"(t.z), "=f"(t.w)
+                                             : "r"(blk + (uint32_t(k) * 32u + lane) * 16u) : "memory");
+                                sum[4 * k] += t.x;
+                                sum[4 * k + 1] += t.y;
+                                sum[4 * k + 2] += t.z;
+                                sum[4 * k + 3] += t.w;
+                            }
+                            ++slot;
+                        }
+                        uint32_t h[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            h[e] = Cfg::kBF ? ptx::pack_bf16x2_rn(__float_as_uint(sum[2 * e]), __float_as_uint(sum[2 * e + 1]))
+                                            : ptx::pack_f16x2_rn(__float_as_uint(sum[2 * e]), __float_as_uint(sum[2 * e + 1]));
+                        // 32 columns of this lane's row, in 16-byte pieces where all 8 fit in N
+                        if (r < p.M) {
+                            uint16_t* crow = p.C + int64_t(r) * p.ldc;
+#pragma unroll
+                            for (int g8 = 0; g8 < 4; ++g8) {
+                                const int32_t n = col0 + int32_t(j) * 32 + g8 * 8;
+                                if (n + 8 <= p.N) {
+                                    *reinterpret_cast<uint4*>(crow + n) =
+                                        make_uint4(h[4 * g8], h[4 * g8 + 1], h[4 * g8 + 2], h[4 * g8 + 3]);
+                                } else {
+                                    for (int e = 0; e < 8 && n + e < p.N; ++e)
+                                        crow[n + e] = uint16_t(h[4 * g8 + e / 2] >> (16 * (e & 1)));
+                                }
+                            }
+                        }
+                    }
+                    // The last read of this accumulator is done: hand it back.
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (CG == 2) ptx::mbar_arrive_cluster(acce_tgt + 8 * acc);
+                        else ptx::mbar_arrive(acce0 + 8 * acc);
+                    }
+                    if (tr) {
+                        tr[5] = ptx::globaltimer();
+                        tr[6] = tr[5];
+                    }
+                    acc ^= 1u;
+                    if (acc == 0) acc_phase ^= 1u;
+                    continue;
+                }
+            }
             // An owner adds the partials of the clusters that took the rest of its tile.
             uint32_t npart = 0;
             if (it.kind == kItemOwner) {
@@ -644,12 +805,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                     float4* dst = partial_f4(cluster, uint32_t(c * kEpiCols / 4));
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        __stcg(dst + size_t(j) * kBlockM,
+                        __stcg(dst + size_t(j) * 32u,
                                make_float4(__uint_as_float(lo[4 * j]), __uint_as_float(lo[4 * j + 1]),
                                            __uint_as_float(lo[4 * j + 2]), __uint_as_float(lo[4 * j + 3])));
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        __stcg(dst + size_t(8 + j) * kBlockM,
+                        __stcg(dst + size_t(8 + j) * 32u,
                                make_float4(__uint_as_float(hi[4 * j]), __uint_as_float(hi[4 * j + 1]),
                                            __uint_as_float(hi[4 * j + 2]), __uint_as_float(hi[4 * j + 3])));
                     continue;
@@ -658,7 +819,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                     const float4* src = partial_f4(cluster + 1 + i, uint32_t(c * kEpiCols / 4));
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const float4 v = __ldcg(src + size_t(j) * kBlockM);
+                        const float4 v = __ldcg(src + size_t(j) * 32u);
                         lo[4 * j] = __float_as_uint(__uint_as_float(lo[4 * j]) + v.x);
                         lo[4 * j + 1] = __float_as_uint(__uint_as_float(lo[4 * j + 1]) + v.y);
                         lo[4 * j + 2] = __float_as_uint(__uint_as_float(lo[4 * j + 2]) + v.z);
@@ -666,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                     }
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const float4 v = __ldcg(src + size_t(8 + j) * kBlockM);
+                        const float4 v = __ldcg(src + size_t(8 + j) * 32u);
                         hi[4 * j] = __float_as_uint(__uint_as_float(hi[4 * j]) + v.x);
                         hi[4 * j + 1] = __float_as_uint(__uint_as_float(hi[4 * j + 1]) + v.y);
                         hi[4 * j + 2] = __float_as_uint(__uint_as_float(hi[4 * j + 2]) + v.z);
@@ -818,8 +979,9 @@ std::atomic<uint64_t> g_launch_seq{0};
 
 constexpr int kMinSplitKb = 8;   // smallest stream-K share worth its fix-up, in k-blocks
 constexpr int kTailSplitGainKb = 32;    // k-blocks a split of the last wave must save each cluster
-constexpr int kSmallSplitGainKb = 64;   // the same with fewer tiles than clusters ...
-constexpr int kMaxPiecesPerTile = 4;    // ... and the pieces it may cut one tile into
+constexpr int kMaxSplitPieces = 8;      // split pieces per tile with fewer tiles than clusters ...
+constexpr int kMinPieceKb = 2;          // ... each at least this many k-blocks long,
+constexpr int kSplitPiecesMinKb = 48;   // ... taken by default from this k depth (k-blocks)
 constexpr int kTailSplitIdlePct = 8;    // idle tile slots (%) above which the last wave may be split
 constexpr int kSplitTailMaxKb = 32;     // deepest k for which the default N-splits a last wave
 
@@ -1075,7 +1237,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
     const int cp = (o && o->cluster_pairs) ? o->cluster_pairs : 1;
     const int acc = o ? o->accumulate : 0;
     if ((cg != 1 && cg != 2) || sw < 1 || sw > 64 || (o && o->max_clusters < 0) || sched < 0 ||
-        sched > 3 || cp < 1 || cp > 2 || (cp == 2 && (cg != 2 || !G16_MCAST_LIB)) || acc < 0 || acc > 1)
+        sched > 4 || cp < 1 || cp > 2 || (cp == 2 && (cg != 2 || !G16_MCAST_LIB)) || acc < 0 || acc > 1)
         return GEMM_ERR_INVALID_VALUE;
     memset(pl, 0, sizeof(*pl));
     pl->cta_group = cg;
@@ -1109,10 +1271,11 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
     // k-blocks.  Measured on GB300: 4096^3 (16 % idle) gains 5.6 %,
     // 4096x11008x4096 (9.5 %) 3 %; 6144^3 (5.3 %) ties; 8192^3 (3.8 % idle,
     // power-capped) loses 1.4 % when split.  1 = whole tiles only; 2 = stream-K
-    // whenever it can; 3 = N-split whenever it can.
+    // whenever it can; 3 = N-split whenever it can; 4 = split pieces whenever
+    // they can run.
     const int64_t kb = pl->k_blocks;
     int64_t clusters = tiles < resident ? tiles : resident;
-    int64_t sk_tiles = 0, tail_tiles = 0, tail_split = 1;
+    int64_t sk_tiles = 0, tail_tiles = 0, tail_split = 1, split_pieces = 1;
     // An fp16 accumulator never splits in k: that would add fp32 partials of
     // fp16 accumulators, a different rounding sequence.
     if (allow_split_k && tiles > 0 && kb > 0 && sched != 1 && sched != 3 && acc == 0) {
@@ -1131,25 +1294,36 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
                                kb >= kMinSplitKb && deep && tiles >= 2 * resident;
             if (sched == 2 || worth) sk_tiles = rem + resident;
             if (sk_tiles > tiles) sk_tiles = tiles;
-        } else {
-            // Fewer tiles than clusters: spreading them over g clusters saves each
-            // cluster kb·(1 - tiles/g) k-blocks but costs the fix-up, in which a
-            // tile's owner adds its partners' partials one after another.  So a
-            // tile is cut into at most kMaxPiecesPerTile pieces, and only for deep
-            // k.  Measured with L2 flushed: 1024^3 (16 tiles of 16 k-blocks over
-            // 32 clusters) 22.3 us split against 16.8 us whole; 2048^3 31.7
-            // against 21.3; one 256x256x4096 tile over 8 clusters 32.5 against
-            // 29.2, over 64 clusters 134 us; 512x4096x4096 (37 k-blocks spared)
-            // 35.4 against 29.0, while 1024x1024x8192 (96 spared) 35.5 against
-            // 45.3.
-            int64_t g = tiles * kb / kMinSplitKb;      // clusters that still get kMinSplitKb each
-            if (sched != 2 && g > kMaxPiecesPerTile * tiles) g = kMaxPiecesPerTile * tiles;
-            if (sched == 2) g = tiles * kb;            // forced: up to one k-block each
+        } else if (sched == 2) {
+            // Forced stream-K with fewer tiles than clusters (tests): all the
+            // tiles' k-blocks spread evenly, owners adding their partners'
+            // partials one after another.
+            int64_t g = tiles * kb;                    // up to one k-block each
             if (g > resident) g = resident;
-            const bool worth = sched == 2 || kb * (g - tiles) >= kSmallSplitGainKb * g;
-            if (g > tiles && worth) {
+            if (g > tiles) {
                 clusters = g;
                 sk_tiles = tiles;
+            }
+        } else if (cp == 1) {
+            // Fewer tiles than clusters: cut every tile along k into s equal
+            // split pieces on s clusters, s = 2, 4 or 8 (the largest with
+            // tiles·s <= clusters and at least kMinPieceKb k-blocks a piece).
+            // The pieces reduce each other's partials in parallel (each owns
+            // s-th of the columns), so the fix-up costs one partial round trip
+            // through L2 per piece; with (s-1) partial tiles written per tile
+            // it is bound by the L2's aggregate write rate (about 5 TB/s
+            // measured).  Measured with L2 flushed, default against N-split:
+            // 256x256x8192 23.0 us (8 pieces) against 42.6, 1024x1024x8192 29.1
+            // (4) against 44.6, 1024x1024x4096 23.0 against 27.1, 512x4096x4096
+            // 27.1 (2) against 28.2; but at k = 1024 and 2048 the N-split wins
+            // (1024^3 14.8 against 19.0, 768x768x2048 18.0 against 20.0).  So
+            // the default takes it from kSplitPiecesMinKb k-blocks.
+            const int64_t min_kb = sched == 4 ? 1 : kMinPieceKb;   // forced: pieces of one k-block allowed
+            int64_t sp = 1;
+            while (sp < kMaxSplitPieces && tiles * sp * 2 <= resident && kb >= sp * 2 * min_kb) sp *= 2;
+            if (sp > 1 && (sched == 4 || kb >= kSplitPiecesMinKb)) {
+                split_pieces = sp;
+                clusters = tiles * sp;
             }
         }
     }
@@ -1166,7 +1340,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
     // last wave measured 693.8 against 688.8 us.  One pair per cluster and B
     // stored [N, K] only.
     const bool can_split = cg == 2 && cp == 1 && !(o && o->b_layout == 1);
-    if (sk_tiles == 0 && tiles > 0 && kb > 0 && can_split &&
+    if (sk_tiles == 0 && split_pieces == 1 && tiles > 0 && kb > 0 && can_split &&
         ((sched == 0 && (tiles < resident || kb <= kSplitTailMaxKb)) || sched == 3)) {
         const int64_t R = tiles % resident;          // all tiles when tiles < resident
         int64_t s = 1;
@@ -1180,9 +1354,10 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
     pl->clusters = int32_t(clusters);
     pl->grid_ctas = int32_t(clusters * cg * cp);
     pl->sk_tiles = int32_t(sk_tiles);
-    pl->workspace_bytes = sk_tiles > 0 ? workspace_bytes(cg * cp, clusters) : 0;
+    pl->workspace_bytes = (sk_tiles > 0 || split_pieces > 1) ? workspace_bytes(cg * cp, clusters) : 0;
     pl->tail_tiles = int32_t(tail_tiles);
     pl->tail_split = int32_t(tail_split);
+    pl->split_pieces = int32_t(split_pieces);
     return GEMM_OK;
 }
 
@@ -1233,7 +1408,7 @@ gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t
     p.inject_stall = o ? o->inject_stall : 0;
     p.a_mn = a_mn ? 1u : 0u;
     p.b_mn = b_mn ? 1u : 0u;
-    if (pl.sk_tiles > 0) {
+    if (pl.workspace_bytes > 0) {
         uint8_t* ws = static_cast<uint8_t*>(workspace);
         p.flags = reinterpret_cast<uint64_t*>(ws);
         p.partials = reinterpret_cast<float*>(ws + flags_bytes(Cfg::kCtas, pl.clusters));
@@ -1284,7 +1459,7 @@ gemm_status_t check_options(const gemm_f16_nt_options_t* o, bool bf16) {
         o->accumulate > 1 || (bf16 && o->accumulate != 0))
         return GEMM_ERR_INVALID_VALUE;
     if ((o->cta_group != 0 && o->cta_group != 1 && o->cta_group != 2) || o->swizzle < 0 || o->swizzle > 64 ||
-        o->max_clusters < 0 || o->schedule < 0 || o->schedule > 3 || o->cluster_pairs < 0 ||
+        o->max_clusters < 0 || o->schedule < 0 || o->schedule > 4 || o->cluster_pairs < 0 ||
         o->cluster_pairs > (G16_MCAST_LIB ? 2 : 1) || (o->cluster_pairs == 2 && o->cta_group == 1) ||
         o->trace_items < 0 || (o->trace && (reinterpret_cast<uintptr_t>(o->trace) & 7)))
         return GEMM_ERR_INVALID_VALUE;
@@ -1313,7 +1488,7 @@ gemm_status_t plan_call(const DeviceState& st, int64_t M, int64_t N, int64_t K, 
     if (s != GEMM_OK || off == kSplitOn) return s;
     gemm_f16_nt_plan_t would;
     if ((s = make_plan(M, N, K, st.sms, resident, &ro, &would, true)) != GEMM_OK) return s;
-    if (would.sk_tiles > 0) pl->split_k_off = off;
+    if (would.sk_tiles > 0 || would.split_pieces > 1) pl->split_k_off = off;
     return GEMM_OK;
 }
 
@@ -1375,7 +1550,7 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t ld
     const gemm_f16_nt_options_t ro = resolve_options(o, N, lda, ldb);
     gemm_f16_nt_plan_t pl;
     if ((s = plan_call(*st, M, N, K, stream, ro, st->ws_slots > 0, &pl)) != GEMM_OK) return s;
-    if (pl.sk_tiles == 0)
+    if (pl.workspace_bytes == 0)
         return launch_any(bf16, pl, M, N, K, A, lda, B, ldb, C, ldc, stream, &ro, st->watchdog, nullptr);
     if (pl.workspace_bytes > st->ws_bytes) return GEMM_ERR_LAUNCH;   // every slot fits any plan of this device
     // A reserved workspace slot, taken round-robin.  The stream first waits for
@@ -1469,7 +1644,7 @@ gemm_status_t run_noalloc(int64_t M, int64_t N, int64_t K, const uint16_t* A, in
     // split's completion flags in the shared scratch.
     if ((s = plan_call(*st, M, N, K, stream, ro, true, &pl)) != GEMM_OK) return s;
     void* ws = nullptr;
-    if (pl.sk_tiles > 0) {
+    if (pl.workspace_bytes > 0) {
         if (uint64_t(pl.workspace_bytes) > kStaticScratchBytes) return GEMM_ERR_SCRATCH_LIMIT;
         if ((s = static_scratch(dev, &ws)) != GEMM_OK) return s;
     }
@@ -1622,7 +1797,7 @@ G16_EXPORT gemm_status_t gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, i
     struct {
         uint32_t num_tiles, num_kb, sk_tiles;
         uint64_t sk_units;
-        uint32_t tail_first, tail_split;
+        uint32_t tail_first, tail_split, split_pieces;
     } sp;
     g16::set_schedule(sp, pl);
     const g16::Raster r = g16::make_raster(uint32_t(pl.m_tiles), uint32_t(pl.n_tiles), uint32_t(pl.swizzle));
@@ -1645,6 +1820,8 @@ G16_EXPORT gemm_status_t gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, i
             o.part = int32_t(it.part);
             o.parts = int32_t(it.parts);
             o.partners = it.kind == g16::kItemOwner ? int32_t(g16::owner_partners(sp, it.tile, c, G)) : 0;
+            o.piece = int32_t(it.piece);
+            o.pieces = int32_t(it.pieces);
         }
         ++n;
     }

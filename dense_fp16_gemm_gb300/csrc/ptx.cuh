@@ -183,6 +183,23 @@ __device__ __forceinline__ void bulk_wait_group_read() {
 __device__ __forceinline__ void bulk_wait_group_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Non-tensor bulk copies (contiguous bytes, 16-byte aligned, size a multiple
+// of 16).  Shared -> global, tracked by the bulk async-group of this thread:
+__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(reinterpret_cast<uint64_t>(gdst)), "r"(ssrc), "r"(bytes) : "memory");
+}
+// Global -> this CTA's shared memory, completion bytes on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t sdst, const void* gsrc, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(sdst), "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(bar) : "memory");
+}
+// Order global-memory accesses of the async proxy (bulk copies) with those of
+// the generic proxy (ordinary loads and stores, flags).
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) reads of them.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -90,13 +90,14 @@ G16_HD void raster_coord(const Raster& r, uint32_t t, uint32_t& m_tile, uint32_t
 }
 
 // Kinds of work item (see work_next)
-enum : uint32_t { kItemWhole = 0, kItemPartialOut = 1, kItemOwner = 2 };
+enum : uint32_t { kItemWhole = 0, kItemPartialOut = 1, kItemOwner = 2, kItemSplitPiece = 3 };
 
 // ---------------------------------------------------------------------------
 // work schedule
 // ---------------------------------------------------------------------------
 // The functions below take the launch's parameters as any struct P with the
-// fields num_tiles, num_kb, sk_tiles, sk_units, tail_first and tail_split, so
+// fields num_tiles, num_kb, sk_tiles, sk_units, tail_first, tail_split and
+// split_pieces, so
 // that the host tests enumerate exactly the items the kernel runs.
 //
 // The tiles [0, sk_tiles) form the stream-K part: their sk_tiles * num_kb
@@ -114,6 +115,15 @@ enum : uint32_t { kItemWhole = 0, kItemPartialOut = 1, kItemOwner = 2 };
 // Owner pieces come at the end of a cluster's range and partial pieces at the
 // start, so an owner seldom waits.
 //
+// Split pieces (split_pieces = s > 1, only when every cluster runs exactly one
+// item): tile c / s is cut along k into s pieces of equal length, piece c % s
+// on cluster c.  The pieces of a tile are symmetric: the tile's columns are cut
+// into s contiguous slices, piece i owning slice i; each piece writes the fp32
+// partial of the slices it does not own, publishes a flag, waits for the other
+// pieces' flags, and reduces its own slice, adding the s partials in piece
+// order, which is k order.  So the fix-up is spread over all s clusters
+// instead of falling on one owner.
+//
 // After the whole tiles come the N-split items: the last tiles of the raster,
 // [tail_first, num_tiles), each cut into tail_split column slices of
 // BN/tail_split, dealt round-robin like the whole tiles.  No cluster depends
@@ -126,6 +136,7 @@ struct Item {
     uint32_t kb0, kb1;   // k-block range [kb0, kb1)
     uint32_t kind;
     uint32_t part, parts;   // column slice `part` of `parts` (1 = the whole tile)
+    uint32_t piece, pieces; // split piece `piece` of `pieces` (1 = not split)
 };
 
 struct Work {
@@ -147,10 +158,31 @@ G16_HD void work_init(Work& s, const P& p, uint32_t c, uint32_t G) {
     s.t = p.sk_tiles + c;
     s.q = c;
     s.G = G;
+    if (p.split_pieces > 1) {   // one split piece per cluster, nothing else
+        s.u = s.u_end = 0;
+        s.t = c;                 // reused: this cluster's piece index in the launch
+        s.q = 1;                 // 1 while the piece is still to be returned
+    }
 }
 
 template <class P>
 G16_HD bool work_next(Work& s, const P& p, Item& it) {
+    it.piece = 0;
+    it.pieces = 1;
+    if (p.split_pieces > 1) {
+        if (!s.q) return false;
+        s.q = 0;
+        const uint32_t np = p.split_pieces, piece = s.t % np;
+        it.tile = s.t / np;
+        it.kb0 = uint32_t(uint64_t(p.num_kb) * piece / np);
+        it.kb1 = uint32_t(uint64_t(p.num_kb) * (piece + 1) / np);
+        it.kind = kItemSplitPiece;
+        it.part = 0;
+        it.parts = 1;
+        it.piece = piece;
+        it.pieces = np;
+        return true;
+    }
     if (s.u < s.u_end) {
         const uint32_t t = uint32_t(s.u / p.num_kb);
         const uint32_t kb0 = uint32_t(s.u - uint64_t(t) * p.num_kb);
@@ -206,6 +238,7 @@ inline void set_schedule(P& p, const PlanT& pl) {
     p.sk_units = uint64_t(pl.sk_tiles) * uint64_t(pl.k_blocks);
     p.tail_split = uint32_t(pl.tail_split > 1 ? pl.tail_split : 1);
     p.tail_first = uint32_t(pl.num_tiles - (pl.tail_split > 1 ? pl.tail_tiles : 0));
+    p.split_pieces = uint32_t(pl.split_pieces > 1 ? pl.split_pieces : 1);
 }
 
 }  // namespace g16

@@ -190,15 +190,24 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  *                 cluster), the k-block work of the last wave plus one full
  *                 wave is split evenly across all clusters (stream-K), with
  *                 fp32 partial tiles summed by each tile's first piece in a
- *                 fixed order (results are reproducible run to run).  With
- *                 fewer tiles than clusters the tiles are split in k the same
- *                 way only for deep k: at most 4 pieces a tile, and only when
- *                 that spares each cluster at least 64 k-blocks (otherwise the
- *                 N-split below applies).  The last-wave split, too, needs deep
- *                 k (at least 32 k-blocks spared a cluster) and at least one
- *                 full wave of whole tiles beside it;
- *                 1: whole tiles only; 2: stream-K whenever possible (tests);
- *                 3: N-split whenever possible (tests).
+ *                 fixed order (results are reproducible run to run).  The
+ *                 last-wave split needs deep k (at least 32 k-blocks spared a
+ *                 cluster) and at least one full wave of whole tiles beside it.
+ *                 With fewer tiles than clusters and k of at least 48 k-blocks
+ *                 (64 k each), every tile is cut along k into s = 2, 4 or 8
+ *                 equal split pieces (the largest with tiles·s <= clusters, at
+ *                 least 2 k-blocks a piece) on their own clusters; the tile's
+ *                 columns are cut into s slices, and each piece writes the
+ *                 fp32 partials of the other pieces' slices, then sums the s
+ *                 partials of its own slice in piece (k) order and stores it.
+ *                 With fewer tiles than clusters and shallower k, the N-split
+ *                 below applies;
+ *                 1: whole tiles only; 2: stream-K whenever possible (tests;
+ *                 with fewer tiles than clusters, all their k-blocks spread
+ *                 over the clusters, owners adding their partners'
+ *                 partials); 3: N-split whenever possible (tests); 4: split
+ *                 pieces whenever there is room for two a tile (tests; pieces
+ *                 of one k-block allowed).
  *                 N-split: when the stream-K rule does not split the problem
  *                 and either there are fewer tiles than clusters or k is
  *                 shallow (at most 32 k-blocks), the R tiles of the last wave
@@ -213,13 +222,15 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  *                 mainly shortens each cluster's epilogue: it is for small,
  *                 latency-bound problems.
  *                 With 3 the last R tiles of any problem are cut the same way
- *                 when 2R <= clusters.  Only with one CTA pair per cluster and
- *                 B stored [N, K].
- *                 A stream-K launch needs a workspace (gemm_f16_nt_plan's
- *                 workspace_bytes): one of the slots reserved at the device's
- *                 set-up (see Ownership above).  Without slots, or under
- *                 stream capture, the call is planned as with schedule 0 but
- *                 with no stream-K split (plan field split_k_off).
+ *                 when 2R <= clusters.  N-split and split pieces need one CTA
+ *                 pair per cluster; the N-split also B stored [N, K].  An fp16
+ *                 accumulator never splits in k.
+ *                 A stream-K or split-piece launch needs a workspace
+ *                 (gemm_f16_nt_plan's workspace_bytes): one of the slots
+ *                 reserved at the device's set-up (see Ownership above).
+ *                 Without slots, or under stream capture, the call is planned
+ *                 as with schedule 0 but with no split in k, neither stream-K
+ *                 nor split pieces (plan field split_k_off).
  *   trace, trace_items
  *                 debugging aid: if `trace` is a device pointer to
  *                 clusters × trace_items × 8 uint64 (zeroed by the caller), the
@@ -391,6 +402,9 @@ typedef struct {
     int32_t split_k_off;   /* gemm_f16_nt_launch_plan only: 0, or why the shape's stream-K
                               split is not taken: 1 the stream is capturing, 2 no workspace
                               was reserved on the device */
+    int32_t split_pieces;  /* > 1: every tile is cut along k into split_pieces equal pieces,
+                              one per cluster, which reduce each other's fp32 partials
+                              (clusters = num_tiles · split_pieces); 1 = not used */
 } gemm_f16_nt_plan_t;
 
 gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms,
@@ -422,11 +436,16 @@ typedef struct {
                            start at k-block 0 (written as an fp32 partial tile
                            to the cluster's workspace slot); 2: stream-K piece
                            from k-block 0 that ends early (the tile's owner:
-                           adds the partners' partials and stores C)          */
+                           adds the partners' partials and stores C); 3: one
+                           of split_pieces equal pieces of the tile (writes the
+                           partial of the column slices it does not own, adds
+                           the others' partials of the slices it owns)        */
     int32_t part;       /* column slice `part` of `parts` (N-split);          */
     int32_t parts;      /*   parts = 1: the whole tile width                  */
     int32_t partners;   /* kind 2: the number of following clusters whose
                            partial pieces it adds, in cluster order; else 0   */
+    int32_t piece;      /* kind 3 (split piece): its index in the tile's      */
+    int32_t pieces;     /*   pieces, 0 <= piece < pieces; else 0 and 1        */
 } gemm_f16_nt_item_t;
 
 /*

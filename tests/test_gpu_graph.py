@@ -35,7 +35,8 @@ def _operands(M, N, K, seed):
 @pytest.mark.parametrize("M,N,K", [(1024, 1024, 8192), (256, 256, 8192)])
 def test_captured_gemm_replays_with_new_inputs(M, N, K):
     lim = g.device_limits()
-    assert g.plan(M, N, K, num_sms=lim["sms"], max_clusters=lim["resident_pairs"])["sk_tiles"] > 0
+    pl = g.plan(M, N, K, num_sms=lim["sms"], max_clusters=lim["resident_pairs"])
+    assert pl["sk_tiles"] > 0 or pl["split_pieces"] > 1     # split in k when called directly
     A0, B0 = _operands(M, N, K, 700)
     As = torch.from_numpy(A0).cuda()
     Bs = torch.from_numpy(B0).cuda()

@@ -371,3 +371,38 @@ def test_layout_pitch_rule():
         g.gemm_f16_nt_ptr(256, 512, 64, A.data_ptr(), 128, B.data_ptr(), 64, C.data_ptr(), 512, 0,
                           g.Options(a_layout=1))
     assert e.value.status == 1
+
+
+# ---------------------------------------------------------------------------
+# split pieces: every tile cut along k into s pieces that reduce each other
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("shape,max_clusters,pieces", [
+    ((1024, 1024, 1024), 0, 4),     # 16 tiles of 16 k-blocks over 64 pairs
+    ((1024, 1024, 1024), 32, 2),    # the same over 32 pairs
+    ((256, 256, 8192), 0, 8),       # one tile, 8 pieces of 16 k-blocks
+    ((300, 520, 328), 0, 4),        # 6 ragged tiles of 6 k-blocks: uneven pieces (1 or 2 k-blocks)
+    ((513, 1100, 2000), 0, 4),      # N % 8 != 0: the last 32-column slice stored element-wise
+    ((1, 1, 100), 0, 2),            # 2 k-blocks, one valid row and column
+])
+def test_split_pieces(shape, max_clusters, pieces):
+    M, N, K = shape
+    A = inputs.draw((M, K), inputs.U, 801 + M)
+    B = inputs.draw((N, K), inputs.U, 802 + N)
+    o = g.Options(max_clusters=max_clusters, schedule=4)
+    pl = g.plan(M, N, K, options=o)
+    assert pl["split_pieces"] == pieces and pl["sk_tiles"] == 0
+    C1 = run(A, B, options=o)
+    check_close(C1, oracle.gemm_f16_nt(A, B), K, f"split pieces {shape}")
+    C2 = run(A, B, options=o)                      # the pieces are summed in a fixed order
+    assert np.array_equal(C1.view(np.uint16), C2.view(np.uint16))
+
+
+@pytest.mark.parametrize("cg", [2, 1])
+def test_split_pieces_integers_bit_exact(cg):
+    M, N, K = 700, 900, 3000
+    A = inputs.draw((M, K), inputs.I2, 803)
+    B = inputs.draw((N, K), inputs.I2, 804)
+    o = g.Options(cta_group=cg, schedule=4)
+    assert g.plan(M, N, K, options=o)["split_pieces"] > 1
+    check_bitexact(run(A, B, options=o), oracle.gemm_f16_nt(A, B), f"split pieces int cg{cg}")

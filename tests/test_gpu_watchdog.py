@@ -47,24 +47,27 @@ def test_stalled_pipeline_reports_timeout_then_recovers(cg, cp):
 
 
 def test_deep_k_finishes_inside_the_item_scaled_limit():
-    """K = 2^30 with M = N = 8: one 256x256 tile of 2^24 k-blocks, split in k into
-    four pieces of about 4.2 M k-blocks (about 1.1 s each).  The epilogue's wait
-    for its accumulator and the owner's wait for its partners' partial tiles last
-    a whole piece, longer than the 1 s base limit; their limit grows with the
-    tile's k-blocks, so the kernel finishes with the watchdog word at 0.  Inputs
-    in {-1, 0, 1}: every partial sum is an integer far below 2^24, so the result
-    is exact and must equal the oracle bit for bit at the sampled points."""
+    """K = 2^30 with M = N = 8, whole tiles: one 256x256 tile of 2^24 k-blocks on
+    one CTA pair, about 4.5 s of tensor work.  The epilogue's wait for the
+    accumulator, the MMA issuer's wait for a drained one and the producer's
+    waits behind it last the whole item, far beyond the 1 s base limit; their
+    limit grows with the tile's k-blocks, so the kernel finishes with the
+    watchdog word at 0.  Inputs in {-1, 0, 1}: every partial sum is an integer
+    far below 2^24, so the result is exact and must equal the oracle bit for bit
+    at the sampled points."""
     M, N, K = 8, 8, 1 << 30
     dev = torch.device("cuda:0")
     free = torch.cuda.mem_get_info(dev)[0]
     if free < 40 * 2**30:
         pytest.skip("needs 32 GiB of free device memory for the operands")
-    pl = g.launch_plan(M, N, K)
-    assert (pl["num_tiles"], pl["k_blocks"], pl["sk_tiles"], pl["clusters"]) == (1, 1 << 24, 1, 4)
+    whole = g.Options(schedule=1)
+    pl = g.launch_plan(M, N, K, options=whole)
+    assert (pl["num_tiles"], pl["k_blocks"], pl["sk_tiles"], pl["split_pieces"], pl["clusters"]) == \
+        (1, 1 << 24, 0, 1, 1)
     Ad = inputs.draw_device_ints((M, K), -1, 1, 2001, dev)
     Bd = inputs.draw_device_ints((N, K), -1, 1, 2002, dev)
     Cd, _ = empty_out(M, N)
-    g.gemm_f16_nt(Ad, Bd, Cd)
+    g.gemm_f16_nt(Ad, Bd, Cd, options=whole)
     assert g.device_status() == 0, "a wait ran into the watchdog"
     C = to_host(Cd)
     rows, cols = np.array([0, 7]), np.array([0, 5])

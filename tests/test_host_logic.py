@@ -130,8 +130,8 @@ def test_plan_stream_k_schedule():
     # wave of whole tiles left; shallow last waves take the N-split instead
     assert g.plan(6144, 4096, 4096, num_sms=152)["sk_tiles"] == 4 + 76
     assert g.plan(4096, 11008, 4096, num_sms=152)["sk_tiles"] == 4 + 76   # 9.5 % of slots idle
-    p = g.plan(512, 4096, 4096, num_sms=152)              # 32 tiles: only 37 k-blocks spared
-    assert (p["sk_tiles"], p["tail_split"]) == (0, 2)
+    p = g.plan(512, 4096, 4096, num_sms=152)              # 32 tiles of 64 k-blocks: two split pieces each
+    assert (p["sk_tiles"], p["tail_split"], p["split_pieces"], p["clusters"]) == (0, 1, 2, 64)
     p = g.plan(4096, 4096, 1024, num_sms=152)             # 16 k-blocks
     assert (p["sk_tiles"], p["tail_split"], p["tail_tiles"]) == (0, 2, 28)
     p = g.plan(3584, 2304, 2048, num_sms=152)             # 32 k-blocks, 126 tiles
@@ -149,23 +149,30 @@ def test_plan_stream_k_schedule():
     assert (p["sk_tiles"], p["tail_split"]) == (0, 1)
     p = g.plan(256 * 15, 256 * 10, 4096, num_sms=152)     # 150 tiles: last wave 74/76 full
     assert (p["sk_tiles"], p["tail_split"]) == (0, 1)
-    # fewer tiles than pairs: split in k only for deep k, at most 4 pieces a tile,
-    # and only if each cluster is spared >= 32 k-blocks
+    # fewer tiles than pairs and deep k (>= 48 k-blocks): every tile cut into
+    # s = 2, 4 or 8 split pieces, the largest with tiles * s <= pairs
     one = g.Options(cluster_pairs=1)
-    p = g.plan(1024, 1024, 8192, options=one)             # 16 tiles x 128 k-blocks
-    assert (p["sk_tiles"], p["clusters"], p["tail_split"]) == (16, 64, 1)
-    p = g.plan(256, 256, 8192, options=one)               # 1 tile x 128 k-blocks: 4 pieces
-    assert (p["sk_tiles"], p["clusters"]) == (1, 4)
-    p = g.plan(1024, 1024, 1024, options=one)             # 16 x 16 k-blocks: not worth it
-    assert (p["sk_tiles"], p["tail_split"]) == (0, 4)
-    p = g.plan(2048, 2048, 2048, options=one)             # 64 x 32 k-blocks: not worth it
-    assert (p["sk_tiles"], p["clusters"]) == (0, 64)
-    p = g.plan(1000, 700, 1000, options=one)              # 12 x 16 k-blocks: N-split instead
-    assert (p["sk_tiles"], p["clusters"], p["tail_split"]) == (0, 48, 4)
+    p = g.plan(1024, 1024, 8192, options=one)             # 16 tiles x 128 k-blocks: 4 pieces
+    assert (p["sk_tiles"], p["split_pieces"], p["clusters"], p["tail_split"]) == (0, 4, 64, 1)
+    assert p["workspace_bytes"] == 64 * 2 * 4 * 8 + 64 * 2 * 128 * 256 * 4
+    p = g.plan(256, 256, 8192, options=one)               # 1 tile x 128 k-blocks: 8 pieces
+    assert (p["split_pieces"], p["clusters"]) == (8, 8)
+    p = g.plan(1024, 1024, 1024, options=one)             # 16 x 16 k-blocks: too shallow, N-split
+    assert (p["split_pieces"], p["tail_split"], p["clusters"]) == (1, 4, 64)
+    p = g.plan(2048, 2048, 2048, options=one)             # 64 tiles: no room for 2 pieces each
+    assert (p["split_pieces"], p["clusters"]) == (1, 64)
+    p = g.plan(1000, 700, 1000, options=one)              # 12 x 16 k-blocks: N-split
+    assert (p["split_pieces"], p["clusters"], p["tail_split"]) == (1, 48, 4)
+    # forced (schedule 4): from one k-block a piece; never for an fp16 accumulator
+    p = g.plan(300, 520, 328, options=g.Options(schedule=4))
+    assert (p["split_pieces"], p["clusters"]) == (4, 24)
+    assert g.plan(256, 256, 8192, options=g.Options(schedule=4, accumulate=1))["split_pieces"] == 1
+    assert g.plan(256, 256, 8192, options=g.Options(schedule=1))["split_pieces"] == 1
+    # the owner-based stream-K split over all tiles stays available when forced
     p = g.plan(256, 256, 4096, options=g.Options(schedule=2))   # forced: one k-block per pair
-    assert (p["sk_tiles"], p["clusters"]) == (1, 64)
+    assert (p["sk_tiles"], p["clusters"], p["split_pieces"]) == (1, 64, 1)
     with pytest.raises(g.GemmError):
-        g.plan(256, 256, 256, options=g.Options(schedule=4))
+        g.plan(256, 256, 256, options=g.Options(schedule=5))
 
 
 def test_plan_n_split():

@@ -17,7 +17,7 @@ import pytest
 
 import dense_fp16_gemm_gb300 as g
 
-WHOLE, PARTIAL, OWNER = 0, 1, 2
+WHOLE, PARTIAL, OWNER, SPLIT = 0, 1, 2, 3
 
 CASES = [
     # M, N, K, options, max_clusters
@@ -42,6 +42,10 @@ CASES = [
     (1, 1, 1, {}, 76),
     (70000, 300, 64, {}, 76),
     (256, 512, 1 << 20, {}, 76),
+    (1024, 1024, 8192, {}, 76),                       # split pieces: 16 tiles x 4
+    (256, 256, 8192, {}, 76),                         # one tile in 8 pieces
+    (300, 520, 328, {"schedule": 4}, 76),             # forced: pieces of 1 or 2 k-blocks
+    (700, 900, 1000, {"cta_group": 1, "schedule": 4}, 152),
 ]
 
 
@@ -53,7 +57,7 @@ def _random_cases(n=60, seed=20261203):
     out = []
     for _ in range(n):
         cg = 1 if rng.random() < 0.25 else 2
-        opts = {"cta_group": cg, "schedule": int(rng.choice([0, 0, 1, 2, 3]))}
+        opts = {"cta_group": cg, "schedule": int(rng.choice([0, 0, 1, 2, 3, 4]))}
         if cg == 2:
             opts["cluster_pairs"] = int(rng.choice([0, 1, 2]))
         mc = int(rng.choice([0, 0, 7, 36, 64, 76, 152]))
@@ -86,6 +90,7 @@ def check_coverage(pl, items):
     for c, its in enumerate(items):
         for it in its:
             assert it["parts"] in (1, pl["tail_split"]), it
+            assert (it["kind"] == SPLIT) == (pl["split_pieces"] > 1), it
             if it["parts"] > 1:
                 sliced += 1
                 assert it["tile"] >= pl["num_tiles"] - pl["tail_tiles"], it
@@ -99,9 +104,27 @@ def check_coverage(pl, items):
     assert sliced == (pl["tail_tiles"] * pl["tail_split"] if pl["tail_split"] > 1 else 0)
 
 
+def check_split_pieces(pl, items):
+    """Split pieces: each cluster runs exactly one piece; cluster c holds piece
+    c % s of tile c // s; a tile's pieces cover its k-blocks in order, with
+    lengths differing by at most one."""
+    s, kb = pl["split_pieces"], pl["k_blocks"]
+    assert pl["clusters"] == pl["num_tiles"] * s and pl["sk_tiles"] == 0 and pl["tail_split"] == 1
+    for c, its in enumerate(items):
+        assert len(its) == 1, (c, its)
+        it = its[0]
+        assert (it["kind"], it["tile"], it["piece"], it["pieces"], it["parts"]) == (SPLIT, c // s, c % s, s, 1)
+        assert it["kb0"] == kb * (c % s) // s and it["kb1"] == kb * (c % s + 1) // s
+    lens = [its[0]["kb1"] - its[0]["kb0"] for its in items]
+    assert max(lens) - min(lens) <= 1 and min(lens) >= 1
+
+
 def check_partials_and_owners(pl, items):
     """One partial piece per cluster at most, as its first item; owners add exactly
     the partial pieces of their tile, held by the next clusters, contiguous in k."""
+    if pl["split_pieces"] > 1:
+        check_split_pieces(pl, items)
+        return
     kb = pl["k_blocks"]
     partial_of = {}                                   # tile -> [(cluster, kb0, kb1)]
     for c, its in enumerate(items):

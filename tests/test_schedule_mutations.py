@@ -29,14 +29,15 @@ _HARNESS = r"""
 #include "sched.cuh"
 
 namespace {
-struct Sp { uint32_t num_tiles, num_kb, sk_tiles; uint64_t sk_units; uint32_t tail_first, tail_split; };
-struct Pl { int64_t num_tiles; int32_t k_blocks, sk_tiles, tail_split, tail_tiles; };
+struct Sp { uint32_t num_tiles, num_kb, sk_tiles; uint64_t sk_units; uint32_t tail_first, tail_split, split_pieces; };
+struct Pl { int64_t num_tiles; int32_t k_blocks, sk_tiles, tail_split, tail_tiles, split_pieces; };
 }
 
 extern "C" int32_t sched_items(int64_t num_tiles, int32_t k_blocks, int32_t sk_tiles, int32_t tail_split,
-                               int32_t tail_tiles, int32_t m_tiles, int32_t n_tiles, int32_t swizzle,
-                               int32_t clusters, int32_t cluster, int32_t* out, int32_t max_items) {
-    Pl pl{num_tiles, k_blocks, sk_tiles, tail_split, tail_tiles};
+                               int32_t tail_tiles, int32_t split_pieces, int32_t m_tiles, int32_t n_tiles,
+                               int32_t swizzle, int32_t clusters, int32_t cluster, int32_t* out,
+                               int32_t max_items) {
+    Pl pl{num_tiles, k_blocks, sk_tiles, tail_split, tail_tiles, split_pieces};
     Sp sp;
     g16::set_schedule(sp, pl);
     const g16::Raster r = g16::make_raster(uint32_t(m_tiles), uint32_t(n_tiles), uint32_t(swizzle));
@@ -48,12 +49,13 @@ extern "C" int32_t sched_items(int64_t num_tiles, int32_t k_blocks, int32_t sk_t
         if (n < max_items) {
             uint32_t mt, nt;
             g16::raster_coord(r, it.tile, mt, nt);
-            int32_t* o = out + 9 * n;
+            int32_t* o = out + 11 * n;
             o[0] = int32_t(it.tile); o[1] = int32_t(mt); o[2] = int32_t(nt);
             o[3] = int32_t(it.kb0); o[4] = int32_t(it.kb1); o[5] = int32_t(it.kind);
             o[6] = int32_t(it.part); o[7] = int32_t(it.parts);
             o[8] = it.kind == g16::kItemOwner
                        ? int32_t(g16::owner_partners(sp, it.tile, uint32_t(cluster), uint32_t(clusters))) : 0;
+            o[9] = int32_t(it.piece); o[10] = int32_t(it.pieces);
         }
         ++n;
     }
@@ -61,7 +63,7 @@ extern "C" int32_t sched_items(int64_t num_tiles, int32_t k_blocks, int32_t sk_t
 }
 """
 
-_FIELDS = ("tile", "m_tile", "n_tile", "kb0", "kb1", "kind", "part", "parts", "partners")
+_FIELDS = ("tile", "m_tile", "n_tile", "kb0", "kb1", "kind", "part", "parts", "partners", "piece", "pieces")
 
 # M, N, K, options, max_clusters: stream-K (last wave, forced, few tiles with
 # middle pieces), N-split (small problem, forced tail), two pairs, cta_group 1
@@ -77,6 +79,8 @@ CASES = [
     (1300, 1000, 320, {"schedule": 3, "cluster_pairs": 1}, 76),
     (700, 900, 1000, {"cta_group": 1, "schedule": 2}, 152),
     (6000, 7000, 3000, {}, 76),
+    (300, 520, 328, {"schedule": 4}, 76),             # split pieces of 1 or 2 k-blocks
+    (256, 256, 8192, {"schedule": 4}, 76),            # one tile in 8 pieces
 ]
 
 MUTATIONS = {
@@ -95,6 +99,11 @@ MUTATIONS = {
                                   "m_tile = (g & 1u) ? mm : r.m_tiles - 1u - mm;"),
     "narrow_last_group_ignored": ("const FastDiv& w = (first_n + r.swizzle <= r.n_tiles) ? r.full : r.last;",
                                   "const FastDiv& w = r.full;"),
+    "split_piece_ranges_rounded": ("it.kb0 = uint32_t(uint64_t(p.num_kb) * piece / np);",
+                                   "it.kb0 = p.num_kb / np * piece;"),
+    "split_piece_tile_from_remainder": ("it.tile = s.t / np;", "it.tile = s.t % np;"),
+    "split_piece_index_from_quotient": ("const uint32_t np = p.split_pieces, piece = s.t % np;",
+                                        "const uint32_t np = p.split_pieces, piece = s.t / np;"),
     "piece_kinds_swapped": (
         "it.kind = kb0 > 0 ? kItemPartialOut : (kb1 < p.num_kb ? kItemOwner : kItemWhole);",
         "it.kind = kb1 < p.num_kb ? kItemPartialOut : (kb0 > 0 ? kItemOwner : kItemWhole);"),
@@ -119,20 +128,20 @@ def _build(tmp, source):
                     os.path.join(d, "harness.cpp")], check=True, capture_output=True)
     lib = ctypes.CDLL(out)
     lib.sched_items.restype = ctypes.c_int32
-    lib.sched_items.argtypes = [ctypes.c_int64] + [ctypes.c_int32] * 9 + [ctypes.POINTER(ctypes.c_int32),
-                                                                           ctypes.c_int32]
+    lib.sched_items.argtypes = [ctypes.c_int64] + [ctypes.c_int32] * 10 + [ctypes.POINTER(ctypes.c_int32),
+                                                                            ctypes.c_int32]
     return lib
 
 
 def _items(lib, pl):
     args = (pl["num_tiles"], pl["k_blocks"], pl["sk_tiles"], pl["tail_split"], pl["tail_tiles"],
-            pl["m_tiles"], pl["n_tiles"], pl["swizzle"], pl["clusters"])
+            pl["split_pieces"], pl["m_tiles"], pl["n_tiles"], pl["swizzle"], pl["clusters"])
     out = []
     for c in range(pl["clusters"]):
         n = lib.sched_items(*args, c, None, 0)
-        buf = (ctypes.c_int32 * (9 * max(n, 1)))()
+        buf = (ctypes.c_int32 * (11 * max(n, 1)))()
         lib.sched_items(*args, c, buf, n)
-        out.append([dict(zip(_FIELDS, buf[9 * i:9 * i + 9])) for i in range(n)])
+        out.append([dict(zip(_FIELDS, buf[11 * i:11 * i + 11])) for i in range(n)])
     return out
 
 

@@ -34,7 +34,7 @@ def _call(fn, A, B, C, stream):
 
 
 @pytest.mark.parametrize("M,N,K,uses_scratch,ints", [
-    (1024, 1024, 8192, True, False),     # 16 pair tiles split in k over 64 pairs
+    (1024, 1024, 8192, True, False),     # 16 pair tiles, each in 4 split pieces over 64 pairs
     (6144, 4096, 4096, True, False),     # 384 tiles: last wave 4/76 full, deep k: stream-K part
     (1024, 1024, 8192, True, True),      # integers: exact, whatever the summation order
     (300, 520, 328, False, False),       # whole tiles, no scratch needed
@@ -44,7 +44,7 @@ def test_noalloc_matches_oracle_and_gemm_f16_nt_on_two_calls(M, N, K, uses_scrat
         pytest.skip("no CUDA device")
     lib = g.library()
     pl = g.launch_plan(M, N, K)
-    assert (pl["sk_tiles"] > 0) == uses_scratch
+    assert (pl["workspace_bytes"] > 0) == uses_scratch
     dist = inputs.I2 if ints else inputs.U
     A = inputs.draw((M, K), dist, 301 + M)
     B = inputs.draw((N, K), dist, 302 + N)
@@ -77,7 +77,7 @@ def test_noalloc_call_under_capture_replays_with_new_inputs():
         pytest.skip("no CUDA device")
     lib = g.library()
     M, N, K = 1024, 1024, 8192                    # split in k when called directly
-    assert g.launch_plan(M, N, K)["sk_tiles"] > 0
+    assert g.launch_plan(M, N, K)["workspace_bytes"] > 0
     Ad = torch.empty((M, K), dtype=torch.float16, device="cuda")
     Bd = torch.empty((N, K), dtype=torch.float16, device="cuda")
     C = torch.empty((M, N), dtype=torch.float16, device="cuda")
