@@ -576,7 +576,8 @@ def run_e2e(args, w, A, B, Ad, Bd, Cd, tdt, entry, device, dist, bf16):
     handle = s_mm.cuda_stream
 
     def gemm(j):
-        st = entry(w.M, w.N, w.K, dA[j].data_ptr(), w.K, dB[j].data_ptr(), w.K, dC[j].data_ptr(), w.N, handle)
+        st = entry(w.M, w.N, w.K, dA[j].data_ptr(), dA[j].stride(0), dB[j].data_ptr(), dB[j].stride(0),
+                   dC[j].data_ptr(), w.N, handle)
         if st != 0:
             raise RuntimeError(f"GEMM call failed with status {st}")
 
@@ -643,6 +644,14 @@ def run_ours(args, w):
         A, B = inputs.operands(w)
         Ad = torch.from_numpy(A).to(device)
         Bd = torch.from_numpy(B).to(device)
+    if args.ld:   # operands placed with a row pitch of args.ld elements
+        if args.ld < w.K or args.ld % 8:
+            raise SystemExit("bench.py: --ld must be at least K and a multiple of 8")
+        Ap = torch.zeros((w.M, args.ld), dtype=tdt, device=device)
+        Bp = torch.zeros((w.N, args.ld), dtype=tdt, device=device)
+        Ap[:, :w.K] = Ad
+        Bp[:, :w.K] = Bd
+        Ad, Bd = Ap[:, :w.K], Bp[:, :w.K]
     Cd = torch.full((w.M, w.N), float("nan"), dtype=tdt, device=device)
     stream = torch.cuda.current_stream(device)
     handle = stream.cuda_stream
@@ -662,7 +671,7 @@ def run_ours(args, w):
         entry = lib.gemm_bf16_nt if bf16 else lib.gemm_f16_nt
 
     def step():
-        st = entry(w.M, w.N, w.K, Ad.data_ptr(), w.K, Bd.data_ptr(), w.K, Cd.data_ptr(), w.N, handle)
+        st = entry(w.M, w.N, w.K, Ad.data_ptr(), Ad.stride(0), Bd.data_ptr(), Bd.stride(0), Cd.data_ptr(), w.N, handle)
         if st != 0:
             raise g.GemmError(st, "gemm_bf16_nt" if bf16 else "gemm_f16_nt")
 
@@ -805,7 +814,8 @@ def run_ours(args, w):
             "ms_per_step": round(t_max / args.steps * 1e3, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if bf16 else "f16",
-            "data": "synthetic", "config": workload_config(w, flush is not None, args.accumulate),
+            "data": "synthetic", "config": {**workload_config(w, flush is not None, args.accumulate),
+                                            **({"lda_ldb": args.ld} if args.ld else {})},
             "pct_of_peak": round(100.0 * achieved / peak, 2),
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                          "unit": UNIT, "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -890,6 +900,12 @@ def main(argv=None):
     ap.add_argument("--dtype", choices=["f16", "bf16"], default="f16",
                     help="operand/result type: f16 (the method's) or the bf16 variant")
     ap.add_argument("--workload", default="gemm_8192", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--ld", type=int, default=0,
+                    help="row pitch of A and B in elements (default K); e.g. a 128-byte-aligned pitch "
+                         "for a K whose rows are not")
+    ap.add_argument("--shape", metavar="MxNxK",
+                    help="time this shape instead of a named workload (inputs uniform in [-1, 1], "
+                         "seeds 101 and 102); for profiling other shapes")
     ap.add_argument("--accumulate", choices=["f32", "f16"], default="f32",
                     help="accumulator type: f32 (the method) or the fp16-accumulation variant")
     ap.add_argument("--repeat", type=int, default=1,
@@ -923,6 +939,12 @@ def main(argv=None):
     if args.gpus != world and world > 1:
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
     w = inputs.WORKLOADS[args.workload]
+    if args.shape:
+        try:
+            M, N, K = (int(x) for x in args.shape.lower().split("x"))
+        except ValueError:
+            ap.error("--shape wants MxNxK")
+        w = inputs.Workload(f"shape_{M}x{N}x{K}", M, N, K, inputs.U, inputs.U, 101, 102)
     if args.record_traffic:
         record_traffic(args.record_traffic, w.name, args.record_command or "")
         return
