@@ -557,6 +557,31 @@ def measure_sustained(step, cb_step, flops: float, ms_hint: float, seconds: floa
             "ours_over_cublas": round(tf / tf_cb, 4)}, win, win_cb
 
 
+def fresh_process_headlines(args):
+    """Run the headline alone in `args.fresh_processes` new processes (one after
+    another, each idling `args.cooldown` s before its timed region) and return
+    their values and median: the timing protocol the Tilus pages describe
+    (median of three fresh processes, a cooldown before each measurement)."""
+    cmd = [sys.executable, os.path.abspath(__file__), "--steps", str(args.steps), "--warmup", str(args.warmup),
+           "--no-workloads", "--sustained-seconds", "0", "--no-cpu-baseline", "--no-cublas",
+           "--cooldown", str(args.cooldown), "--cooldown-first", "--fresh-processes", "0",
+           "--workload", args.workload, "--dtype", args.dtype, "--accumulate", args.accumulate]
+    if args.shape:
+        cmd += ["--shape", args.shape]
+    if args.ld:
+        cmd += ["--ld", str(args.ld)]
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    values = []
+    for _ in range(args.fresh_processes):
+        out = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
+        if out.returncode != 0:
+            raise SystemExit("bench.py: a fresh-process headline failed:\n" + out.stderr[-2000:])
+        values.append(json.loads(out.stdout.strip().splitlines()[-1])["value"])
+    return {"values": values, "median": statistics.median(values), "unit": UNIT,
+            "protocol": f"{len(values)} fresh processes, {args.cooldown} s idle before each timed region "
+                        f"of {args.steps} launches"}
+
+
 def run_e2e(args, w, A, B, Ad, Bd, Cd, tdt, entry, device, dist, bf16):
     """Pipelined end-to-end steps; returns (max time over ranks, total flops, steps)."""
     import torch
@@ -692,7 +717,7 @@ def run_ours(args, w):
     sampler = ClockSampler(local) if rank == 0 else None
     times, launch_ms, head_windows = [], [], []
     for rep in range(args.repeat):
-        if rep and args.cooldown > 0:
+        if (rep or args.cooldown_first) and args.cooldown > 0:
             time.sleep(args.cooldown)
         # per-launch events only around flushed launches: between back-to-back
         # launches they would stop the next GEMM's set-up overlapping this one's tail
@@ -795,6 +820,12 @@ def run_ours(args, w):
             sustained["clocks"] = sampler.summary([windows["sustained"][0]])
             sustained["cublas_clocks"] = sampler.summary([windows["sustained"][1]])
 
+    # The pages' protocol, on request: the headline measured again in fresh
+    # processes, each after a cooldown, and the median reported beside it.
+    fresh = None
+    if rank == 0 and world == 1 and args.fresh_processes > 0:
+        fresh = fresh_process_headlines(args)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle_sample(w, A, B, args.cpu_seconds, acc16, bf16)
@@ -838,6 +869,7 @@ def run_ours(args, w):
             "timing": {"repeats": args.repeat, "cooldown_s": args.cooldown,
                        "per_repeat_ms_per_step": [round(t / args.steps * 1e3, 4) for t in times]},
             "sustained": sustained,
+            "fresh_processes": fresh,
             "workloads": side or None,
             "cpu_baseline": cpu,
             "context": context,
@@ -911,6 +943,11 @@ def main(argv=None):
     ap.add_argument("--repeat", type=int, default=1,
                     help="timed regions of K steps per process (the median is reported)")
     ap.add_argument("--cooldown", type=float, default=1.0, help="seconds of idle before each repeat")
+    ap.add_argument("--fresh-processes", type=int, default=0,
+                    help="also time the headline in this many fresh processes (with --cooldown before each) "
+                         "and report their median, the pages' protocol (e.g. 3 with --cooldown 3)")
+    ap.add_argument("--cooldown-first", action="store_true",
+                    help="also idle --cooldown seconds between the warm-up and the first timed region")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--flush-l2", action="store_true",
