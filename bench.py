@@ -432,7 +432,8 @@ def time_steps(step, steps: int, stream, flush=None, sampler=None):
     Back to back (flush None): returns (mean ms per launch from the events
     around the whole region, wall window).  With an L2 flush buffer: each
     launch is preceded by the flush and bracketed by its own events; returns
-    the mean of those per-launch times."""
+    the median of those per-launch times (robust to the odd delayed launch at
+    the few-microsecond scale of small problems)."""
     import torch
     torch.cuda.synchronize()
     w0 = time.time()
@@ -457,7 +458,7 @@ def time_steps(step, steps: int, stream, flush=None, sampler=None):
         if sampler is not None:
             sampler.sample_now()
         torch.cuda.synchronize()
-        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        ms = statistics.median(a.elapsed_time(b) for a, b in evs)
     return ms, (w0, time.time())
 
 
@@ -515,6 +516,8 @@ def measure_workload(lib, name: str, device, stream, steps: int, warmup: int, co
     if g.device_status(stream) != 0 or torch.isnan(Cd).any().item():
         raise SystemExit(f"bench.py: {name}: watchdog word set or C unwritten after warm-up")
     time.sleep(cooldown)
+    if flushed and w.flops < 1e9:   # a few microseconds a launch: more samples for the median
+        steps = max(steps, 200)
     ms, win = time_steps(step, steps, stream, flush, sampler)
     if g.device_status(stream) != 0:
         raise SystemExit(f"bench.py: {name}: watchdog word set during the timed region")

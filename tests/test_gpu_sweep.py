@@ -29,25 +29,27 @@ import dense_fp16_gemm_gb300 as g  # noqa: E402
 NAN = {"f16": 0x7E00, "bf16": 0x7FC0}
 
 
-def _configs(n=48, seed=20261202):
+def _configs(n=48, seed=20261202, schedules=(0, 0, 1, 2, 3), mn_max=2600, k_min=1):
     rng = np.random.default_rng(seed)
-    size = lambda: int(np.clip(np.round(np.exp(rng.uniform(0.0, np.log(2600.0)))), 1, 2600))
+    size = lambda hi=2600: int(np.clip(np.round(np.exp(rng.uniform(0.0, np.log(float(hi))))), 1, hi))
     out = []
     for i in range(n):
         dtype = "bf16" if rng.random() < 0.3 else "f16"
         cg = 1 if rng.random() < 0.25 else 2
         cp = 0 if cg == 1 else int(rng.choice([0, 0, 1, 2]))
         out.append(dict(
-            i=i, M=size(), N=size(), K=size(), dtype=dtype,
+            i=i, M=size(mn_max), N=size(mn_max), K=max(size(), k_min), dtype=dtype,
             acc16=dtype == "f16" and rng.random() < 0.2,
             a_layout=int(rng.integers(0, 2)), b_layout=int(rng.integers(0, 2)),
-            cg=cg, cp=cp, schedule=int(rng.choice([0, 0, 1, 2, 3])),
+            cg=cg, cp=cp, schedule=int(rng.choice(list(schedules))),
             pad=[int(rng.choice([0, 8, 64])) for _ in range(3)],
             ints=rng.random() < 0.3))
     return out
 
 
-CASES = _configs()
+# the first 48 as before; 24 more that force split pieces (every option and
+# type with each tile cut along k, wherever the tiles leave room for two pieces)
+CASES = _configs() + [dict(c, i=100 + c["i"]) for c in _configs(24, 20261204, (4,), mn_max=1200, k_min=200)]
 
 
 @pytest.fixture(autouse=True)
