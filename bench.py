@@ -53,7 +53,7 @@ from dense_fp16_gemm_gb300 import inputs  # noqa: E402
 METRIC = "fp16 NT GEMM TFLOP/s and % of GB300 dense fp16 tensor peak"
 UNIT = "TFLOP/s"
 KERNEL_SOURCES = ["dense_fp16_gemm_gb300/csrc/gemm_f16_nt.cu", "dense_fp16_gemm_gb300/csrc/ptx.cuh",
-                  "dense_fp16_gemm_gb300/csrc/sched.cuh"]
+                  "dense_fp16_gemm_gb300/csrc/sched.cuh", "dense_fp16_gemm_gb300/csrc/small_tile.cuh"]
 # DRAM bytes per launch from an Nsight Compute capture, written by
 # `bench.py --record-traffic`; used only while the kernel sources hash the same
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")

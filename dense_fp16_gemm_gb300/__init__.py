@@ -55,7 +55,8 @@ class Options(ctypes.Structure):
                 ("timeout_ns", ctypes.c_uint64), ("schedule", ctypes.c_int32),
                 ("trace_items", ctypes.c_int32), ("trace", ctypes.c_void_p),
                 ("cluster_pairs", ctypes.c_int32), ("a_layout", ctypes.c_int32),
-                ("b_layout", ctypes.c_int32), ("accumulate", ctypes.c_int32)]
+                ("b_layout", ctypes.c_int32), ("accumulate", ctypes.c_int32),
+                ("tile_n", ctypes.c_int32)]
 
 
 class Plan(ctypes.Structure):
@@ -70,7 +71,7 @@ class Plan(ctypes.Structure):
                 ("sk_tiles", ctypes.c_int32), ("cluster_pairs", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("tail_tiles", ctypes.c_int32),
                 ("tail_split", ctypes.c_int32), ("split_k_off", ctypes.c_int32),
-                ("split_pieces", ctypes.c_int32)]
+                ("split_pieces", ctypes.c_int32), ("kernel", ctypes.c_int32)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -916,6 +916,12 @@ __global__ void zero_fill_kernel(uint16_t* C, int64_t M, int64_t N, int64_t ldc)
     }
 }
 
+}  // namespace g16
+
+#include "small_tile.cuh"
+
+namespace g16 {
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -926,6 +932,19 @@ using Cfg2Bf = KCfg<2, 256, 6, 1, true>;    // the same with bf16 operands and r
 using Cfg1Bf = KCfg<1, 256, 4, 1, true>;
 using Cfg2A16 = KCfg<2, 256, 6, 1, false, true>;   // the fp16 ones with an fp16 accumulator
 using Cfg1A16 = KCfg<1, 256, 4, 1, false, true>;
+// The small-problem kernel's tiles: 128·CG × BN, one per cluster.
+using S1n32 = SCfg<1, 32, 8>;
+using S1n64 = SCfg<1, 64, 8>;
+using S1n128 = SCfg<1, 128, 6>;
+using S2n32 = SCfg<2, 32, 8>;
+using S2n64 = SCfg<2, 64, 8>;
+using S2n128 = SCfg<2, 128, 8>;
+using S1n32Bf = SCfg<1, 32, 8, true>;
+using S1n64Bf = SCfg<1, 64, 8, true>;
+using S1n128Bf = SCfg<1, 128, 6, true>;
+using S2n32Bf = SCfg<2, 32, 8, true>;
+using S2n64Bf = SCfg<2, 64, 8, true>;
+using S2n128Bf = SCfg<2, 128, 8, true>;
 #if G16_MCAST_LIB
 using Cfg2x2 = KCfg<2, 256, 6, 2>; // two CTA pairs per cluster sharing A: 256×512 cluster tile
 using Cfg2x2Bf = KCfg<2, 256, 6, 2, true>;
@@ -936,6 +955,11 @@ template <class Cfg>
 bool allow_smem() {
     return cudaFuncSetAttribute(gemm_f16_nt_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 Cfg::kSmemBytes) == cudaSuccess;
+}
+template <class... Cfgs>
+bool allow_smem_small() {
+    return ((cudaFuncSetAttribute(gemm_f16_nt_small_kernel<Cfgs>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  Cfgs::kSmemBytes) == cudaSuccess) && ...);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -1008,7 +1032,9 @@ gemm_status_t setup_device(int dev, DeviceState& st) {
         g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
     if (!allow_smem<Cfg2>() || !allow_smem<Cfg1>() || !allow_smem<Cfg2Bf>() || !allow_smem<Cfg1Bf>() ||
-        !allow_smem<Cfg2A16>() || !allow_smem<Cfg1A16>()) {
+        !allow_smem<Cfg2A16>() || !allow_smem<Cfg1A16>() ||
+        !allow_smem_small<S1n32, S1n64, S1n128, S2n32, S2n64, S2n128, S1n32Bf, S1n64Bf, S1n128Bf, S2n32Bf,
+                          S2n64Bf, S2n128Bf>()) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
@@ -1216,13 +1242,97 @@ gemm_status_t check_local_operands(const DeviceState& st, int dev, int64_t M, in
 // The options with every "auto" (zero) CTA-group and cluster choice resolved.
 gemm_f16_nt_options_t resolve_options(const gemm_f16_nt_options_t* o, int64_t N, int64_t lda, int64_t ldb) {
     gemm_f16_nt_options_t r = o ? *o : gemm_f16_nt_options_t{};
-    if (r.cta_group == 0) r.cta_group = 2;
-    if (r.cluster_pairs == 0) r.cluster_pairs = auto_cluster_pairs(r.cta_group, N, lda, ldb);
+    // cta_group stays 0 (automatic): the plan picks the small-problem kernel's
+    // CTA group itself; the persistent kernel reads 0 as 2.
+    if (r.cluster_pairs == 0) r.cluster_pairs = auto_cluster_pairs(r.cta_group ? r.cta_group : 2, N, lda, ldb);
     return r;
 }
 
 int resident_clusters_for(const DeviceState& st, const gemm_f16_nt_options_t& r) {
     return r.cta_group == 1 ? st.max_ctas1 : (r.cluster_pairs == 2 ? st.max_clusters4 : st.max_clusters2);
+}
+
+// ---- the small-problem kernel's plan ----
+
+bool small_tile_n_valid(int tn) { return tn == 0 || tn == 32 || tn == 64 || tn == 128; }
+
+// Ring depth, shared memory and tensor-memory columns of SCfg<cg, bn>.
+void small_cfg_info(int cg, int bn, int32_t* stages, int32_t* smem, int32_t* tmem) {
+#define G16_SMALL_INFO(C, N, T)                  \
+    if (cg == C && bn == N) {                     \
+        *stages = T::kStages;                     \
+        *smem = T::kSmemBytes;                    \
+        *tmem = T::kTmemCols;                     \
+        return;                                   \
+    }
+    G16_SMALL_INFO(1, 32, S1n32)
+    G16_SMALL_INFO(1, 64, S1n64)
+    G16_SMALL_INFO(1, 128, S1n128)
+    G16_SMALL_INFO(2, 32, S2n32)
+    G16_SMALL_INFO(2, 64, S2n64)
+    G16_SMALL_INFO(2, 128, S2n128)
+#undef G16_SMALL_INFO
+    *stages = *smem = *tmem = 0;
+}
+
+// The small kernel's automatic tile width: the narrowest of 32, 64 and 128
+// columns whose 128·cg × bn tiles fit on the SMs in one wave (more, smaller
+// tiles: less of A and B for each SM to load, less k-loop per tile), 0 if none
+// does.  Measured on GB300 (L2 flushed, time the GEMM adds after a flush): at
+// 256³ 32-wide tiles on 16 SMs took 2.2 us against 3.0 (64) and 4.1 (128); at
+// 1024³, where 32-wide tiles need two waves, 64-wide ones 6.1 us against 10.3.
+int small_tile_n(int64_t M, int64_t N, int cg, int32_t num_sms) {
+    const int64_t slots = num_sms / cg;
+    const int64_t mt = cdiv(M, int64_t(kBlockM) * cg);
+    for (int bn = 32; bn <= 128; bn *= 2)
+        if (mt * cdiv(N, bn) <= slots) return bn;
+    return 0;
+}
+
+// Deepest k (in 64-wide k-blocks) for which the automatic plan takes the small
+// kernel; deeper problems with few tiles go to the persistent kernel's split
+// pieces, which spread k over more SMs.
+constexpr int64_t kSmallMaxKb = 128;
+
+// Whether the automatic plan takes the small-problem kernel: every automatic
+// option (no CTA group, schedule, raster, grid or tile width asked for), the
+// kernel's operand forms, one wave of tiles and k no deeper than kSmallMaxKb.
+// Where it applies, the persistent kernel would leave most CTA pairs idle.
+// Measured against the persistent kernel's default plan (us, L2 flushed):
+// 256³ 2.2 against 6.1, 1024³ 6.1 against 10.2, 512×4096×4096 18.7 against
+// 26.5, 128×4096×4096 14.4 against 22.7, 1024×1024×8192 26.7 against 26.9;
+// 2048³ and 4096×1024×1024 need more than one wave and stay persistent.
+bool small_kernel_pays(int64_t M, int64_t N, int64_t K, const gemm_f16_nt_options_t* o, bool small_ok,
+                       int32_t num_sms) {
+    if (!small_ok) return false;
+    if (o && (o->cta_group != 0 || o->swizzle != 0 || o->max_clusters != 0 || o->schedule != 0 ||
+              o->cluster_pairs > 1 || o->tile_n != 0))
+        return false;
+    return cdiv(K, kBlockK) <= kSmallMaxKb && small_tile_n(M, N, 1, num_sms) != 0;
+}
+
+gemm_status_t small_plan(int64_t M, int64_t N, int64_t K, int cg, int bn, gemm_f16_nt_plan_t* pl) {
+    memset(pl, 0, sizeof(*pl));
+    const int64_t mt = cdiv(M, int64_t(kBlockM) * cg), nt = cdiv(N, bn);
+    const int64_t tiles = mt * nt;
+    if (tiles * cg >= (int64_t(1) << 31)) return GEMM_ERR_INVALID_VALUE;
+    pl->kernel = 1;
+    pl->cta_group = cg;
+    pl->cluster_pairs = 1;
+    pl->tile_m = kBlockM * cg;
+    pl->tile_n = bn;
+    pl->block_k = kBlockK;
+    small_cfg_info(cg, bn, &pl->stages, &pl->smem_bytes, &pl->tmem_cols);
+    pl->m_tiles = int32_t(mt);
+    pl->n_tiles = int32_t(nt);
+    pl->k_blocks = int32_t(cdiv(K, kBlockK));
+    pl->num_tiles = tiles;
+    pl->swizzle = 1;
+    pl->clusters = int32_t(tiles);
+    pl->grid_ctas = int32_t(tiles * cg);
+    pl->tail_split = 1;
+    pl->split_pieces = 1;
+    return GEMM_OK;
 }
 
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t max_resident,
@@ -1236,9 +1346,21 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
     const int sched = o ? o->schedule : 0;
     const int cp = (o && o->cluster_pairs) ? o->cluster_pairs : 1;
     const int acc = o ? o->accumulate : 0;
+    const int tn = o ? o->tile_n : 0;
     if ((cg != 1 && cg != 2) || sw < 1 || sw > 64 || (o && o->max_clusters < 0) || sched < 0 ||
-        sched > 4 || cp < 1 || cp > 2 || (cp == 2 && (cg != 2 || !G16_MCAST_LIB)) || acc < 0 || acc > 1)
+        sched > 5 || cp < 1 || cp > 2 || (cp == 2 && (cg != 2 || !G16_MCAST_LIB)) || acc < 0 || acc > 1 ||
+        !small_tile_n_valid(tn))
         return GEMM_ERR_INVALID_VALUE;
+    // The small-problem kernel: K-major A and B, fp32 accumulator, one pair
+    // (or CTA) per cluster, no trace.
+    const bool small_ok = cp == 1 && acc == 0 && !(o && (o->a_layout != 0 || o->b_layout != 0 || o->trace));
+    if (sched == 5 && !small_ok) return GEMM_ERR_INVALID_VALUE;
+    if (sched == 5 || (K > 0 && small_kernel_pays(M, N, K, o, small_ok, num_sms))) {
+        const int scg = (o && o->cta_group) ? o->cta_group : 1;
+        int bn = tn ? tn : small_tile_n(M, N, scg, num_sms);
+        if (bn == 0) bn = 128;   // forced on a problem too large for one wave: widest tiles
+        return small_plan(M, N, K, scg, bn, pl);
+    }
     memset(pl, 0, sizeof(*pl));
     pl->cta_group = cg;
     pl->cluster_pairs = cp;
@@ -1449,6 +1571,69 @@ gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t
     return GEMM_OK;
 }
 
+template <class Cfg>
+gemm_status_t launch_small(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t K, const uint16_t* A,
+                           int64_t lda, const uint16_t* B, int64_t ldb, uint16_t* C, int64_t ldc,
+                           cudaStream_t stream, const gemm_f16_nt_options_t* o, uint32_t* watchdog) {
+    SmallParams p;
+    memset(&p, 0, sizeof(p));
+    gemm_status_t s;
+    const CUtensorMapDataType dt = Cfg::kBF ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if ((s = encode_2d(&p.tmA, dt, A, uint64_t(K), uint64_t(M), uint64_t(lda), kBlockK, kBlockM)) != GEMM_OK ||
+        (s = encode_2d(&p.tmB, dt, B, uint64_t(K), uint64_t(N), uint64_t(ldb), kBlockK, Cfg::kBRows)) != GEMM_OK)
+        return s;
+    p.C = C;
+    p.ldc = ldc;
+    p.M = int32_t(M);
+    p.N = int32_t(N);
+    p.m_tiles = uint32_t(pl.m_tiles);
+    p.num_kb = uint32_t(pl.k_blocks);
+    p.timeout_ns = (o && o->timeout_ns) ? o->timeout_ns : kDefaultTimeoutNs;
+    p.item_timeout_ns = p.timeout_ns + uint64_t(pl.k_blocks) * kItemWaitNsPerKb;
+    p.watchdog = watchdog;
+    p.inject_stall = o ? o->inject_stall : 0;
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    cfg.gridDim = dim3(uint32_t(pl.grid_ctas), 1, 1);
+    cfg.blockDim = dim3(kSmallThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 1;
+    if (Cfg::kCG == 2) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
+    if (cudaLaunchKernelEx(&cfg, gemm_f16_nt_small_kernel<Cfg>, p) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    return GEMM_OK;
+}
+
+template <bool BF>
+gemm_status_t launch_small_any(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t K, const uint16_t* A,
+                               int64_t lda, const uint16_t* B, int64_t ldb, uint16_t* C, int64_t ldc,
+                               cudaStream_t stream, const gemm_f16_nt_options_t* o, uint32_t* watchdog) {
+#define G16_SMALL_LAUNCH(CG, N_, S_)                                                                 \
+    if (pl.cta_group == CG && pl.tile_n == N_)                                                       \
+        return launch_small<SCfg<CG, N_, S_::kStages, BF>>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, o, watchdog);
+    G16_SMALL_LAUNCH(1, 32, S1n32)
+    G16_SMALL_LAUNCH(1, 64, S1n64)
+    G16_SMALL_LAUNCH(1, 128, S1n128)
+    G16_SMALL_LAUNCH(2, 32, S2n32)
+    G16_SMALL_LAUNCH(2, 64, S2n64)
+    G16_SMALL_LAUNCH(2, 128, S2n128)
+#undef G16_SMALL_LAUNCH
+    return GEMM_ERR_INVALID_VALUE;
+}
+
 // Why a call ran without the stream-K split that its shape would take
 // (gemm_f16_nt_plan_t.split_k_off).
 enum : int32_t { kSplitOn = 0, kSplitOffCapture = 1, kSplitOffNoWorkspace = 2 };
@@ -1459,7 +1644,8 @@ gemm_status_t check_options(const gemm_f16_nt_options_t* o, bool bf16) {
         o->accumulate > 1 || (bf16 && o->accumulate != 0))
         return GEMM_ERR_INVALID_VALUE;
     if ((o->cta_group != 0 && o->cta_group != 1 && o->cta_group != 2) || o->swizzle < 0 || o->swizzle > 64 ||
-        o->max_clusters < 0 || o->schedule < 0 || o->schedule > 4 || o->cluster_pairs < 0 ||
+        o->max_clusters < 0 || o->schedule < 0 || o->schedule > 5 || !small_tile_n_valid(o->tile_n) ||
+        o->cluster_pairs < 0 ||
         o->cluster_pairs > (G16_MCAST_LIB ? 2 : 1) || (o->cluster_pairs == 2 && o->cta_group == 1) ||
         o->trace_items < 0 || (o->trace && (reinterpret_cast<uintptr_t>(o->trace) & 7)))
         return GEMM_ERR_INVALID_VALUE;
@@ -1515,6 +1701,9 @@ using Cfg2x2A16_ = void;
 gemm_status_t launch_any(bool bf16, const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t K,
                          const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb, uint16_t* C, int64_t ldc,
                          cudaStream_t stream, const gemm_f16_nt_options_t* ro, uint32_t* watchdog, void* ws) {
+    if (pl.kernel == 1)
+        return bf16 ? launch_small_any<true>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, ro, watchdog)
+                    : launch_small_any<false>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, ro, watchdog);
     if (bf16)
         return launch_cfg<Cfg2Bf, Cfg2x2Bf_, Cfg1Bf>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, ro, watchdog, ws);
     if (ro->accumulate == 1)
@@ -1793,6 +1982,21 @@ G16_EXPORT gemm_status_t gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, i
     const gemm_status_t s = gemm_f16_nt_plan(M, N, K, num_sms, max_clusters, opts, &pl);
     if (s != GEMM_OK) return s;
     if (cluster < 0 || cluster >= pl.clusters) return GEMM_ERR_INVALID_VALUE;
+    if (pl.kernel == 1) {
+        // the small-problem kernel: cluster c computes tile c, all of k
+        if (max_items > 0) {
+            gemm_f16_nt_item_t& o = items[0];
+            memset(&o, 0, sizeof(o));
+            o.tile = cluster;
+            o.m_tile = cluster % pl.m_tiles;
+            o.n_tile = cluster / pl.m_tiles;
+            o.kb1 = pl.k_blocks;
+            o.parts = 1;
+            o.pieces = 1;
+        }
+        *n_items = 1;
+        return GEMM_OK;
+    }
     // the launch's schedule fields, set exactly as the launch sets them
     struct {
         uint32_t num_tiles, num_kb, sk_tiles;

@@ -21,6 +21,18 @@
  * Threading: every entry point may be called from any host thread.  Each GEMM
  * call is asynchronous on the given stream.
  *
+ * Two kernels.  The persistent kernel (256×256 tiles on CTA pairs, one
+ * persistent cluster per pair of SMs, a work schedule with stream-K, N-split
+ * and split pieces) computes every problem whose 128-row tiles would not fit
+ * on the SMs in one wave.  The small-problem kernel computes one 128×tile_n
+ * tile (tile_n = 32, 64 or 128, the narrowest whose tiles fit on the SMs at
+ * once) per CTA with all of k, for problems with K <= 8192 whose tiles do fit:
+ * there the persistent kernel's 256×256 tiles would leave most SMs idle and
+ * its fixed costs dominate.  The automatic choice applies when no persistent-
+ * kernel option is given (see gemm_f16_nt_ex); gemm_f16_nt_launch_plan reports
+ * which kernel a call gets (plan field `kernel`).  Both give results within the
+ * same bound; only the order of the fp32 additions can differ between them.
+ *
  * Two builds share this header.  libgemm_f16_nt.so is the library; it issues
  * no multicast copy and may be loaded by each of several processes on several
  * GPUs.  libgemm_f16_nt_mcast.so, built only on request, is the same library
@@ -162,8 +174,13 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  * selects the default that gemm_f16_nt uses.
  *
  *   cta_group     2: a CTA pair computes one 256×256 tile with 2-SM MMAs and
- *                 each CTA loads half of the shared B tile (default);
- *                 1: one CTA computes a 128×256 tile on its own.
+ *                 each CTA loads half of the shared B tile (the persistent
+ *                 kernel's default); 1: one CTA computes a 128×256 tile on
+ *                 its own.  0 (automatic): the small-problem kernel where it
+ *                 applies (one CTA per tile), else 2.  A nonzero value selects
+ *                 the persistent kernel unless schedule is 5, where it is the
+ *                 small-problem kernel's CTA group (2: 256×tile_n tiles on a
+ *                 CTA pair, each CTA loading tile_n/2 rows of B).
  *   swizzle       width, in N tiles, of the groups of the tile raster; tiles
  *                 in a group are visited row-major so that concurrently
  *                 running tiles share B columns in L2 (Tilus tutorial
@@ -207,7 +224,14 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  *                 over the clusters, owners adding their partners'
  *                 partials); 3: N-split whenever possible (tests); 4: split
  *                 pieces whenever there is room for two a tile (tests; pieces
- *                 of one k-block allowed).
+ *                 of one k-block allowed); 5: the small-problem kernel for any
+ *                 problem (K-major A and B, fp32 accumulator, one pair per
+ *                 cluster, no trace; GEMM_ERR_INVALID_VALUE otherwise).
+ *                 The automatic plan (schedule 0 with cta_group, swizzle,
+ *                 max_clusters and tile_n 0, cluster_pairs at most 1) takes the
+ *                 small-problem kernel when those conditions hold, K is at most
+ *                 8192 (128 k-blocks) and its 128×32, 128×64 or 128×128 tiles
+ *                 fit on the device's SMs in one wave.
  *                 N-split: when the stream-K rule does not split the problem
  *                 and either there are fewer tiles than clusters or k is
  *                 shallow (at most 32 k-blocks), the R tiles of the last wave
@@ -264,6 +288,11 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  *                 row-major: layouts (0,1) give C = A·B for a row-major [K, N]
  *                 B, (1,0) give C = Aᵀ·Bᵀ-style transposed storage, etc.  The
  *                 tensor cores read M/N-contiguous tiles as MN-major operands.
+ *   tile_n        the small-problem kernel's tile width: 32, 64 or 128
+ *                 columns; 0 (default) = the narrowest whose tiles fit on the
+ *                 SMs in one wave (128 if none does).  Any other value returns
+ *                 GEMM_ERR_INVALID_VALUE; a nonzero value keeps the automatic
+ *                 plan on the persistent kernel (use it with schedule 5).
  *   accumulate    0 (default): fp32 accumulator, rounded once to fp16 at the
  *                 end (the method as the tutorial pages define it);
  *                 1: fp16 accumulator (fp16 operands only: gemm_f16_nt_ex).
@@ -293,6 +322,7 @@ typedef struct {
     int32_t a_layout;
     int32_t b_layout;
     int32_t accumulate;
+    int32_t tile_n;
 } gemm_f16_nt_options_t;
 
 /* gemm_f16_nt with options (opts may be NULL).  Same arguments, layout,
@@ -405,6 +435,10 @@ typedef struct {
     int32_t split_pieces;  /* > 1: every tile is cut along k into split_pieces equal pieces,
                               one per cluster, which reduce each other's fp32 partials
                               (clusters = num_tiles · split_pieces); 1 = not used */
+    int32_t kernel;        /* 0: the persistent kernel; 1: the small-problem kernel: one
+                              tile_m × tile_n tile per cluster (CTA or CTA pair), all
+                              of k, clusters = num_tiles, tile c at m_tile =
+                              c % m_tiles, n_tile = c / m_tiles; no workspace */
 } gemm_f16_nt_plan_t;
 
 gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms,
@@ -453,7 +487,9 @@ typedef struct {
  * `cluster` of the launch gemm_f16_nt_ex(M, N, K, …, opts) would run on a GPU
  * with `num_sms` SMs and at most `max_clusters` resident clusters (0: as many
  * as fit), from the same plan (gemm_f16_nt_plan) and the same schedule code
- * the kernel runs.  Host only, for tests and tools; no GPU is needed.
+ * the kernel runs.  For a plan on the small-problem kernel (kernel = 1) each
+ * cluster has one item: tile `cluster`, all of k.  Host only, for tests and
+ * tools; no GPU is needed.
  *   items      caller-owned array of max_items entries (may be NULL if 0);
  *              the first min(n, max_items) items are written.
  *   n_items    receives n, the cluster's total number of items.

@@ -35,7 +35,8 @@ def _operands(M, N, K, seed):
 @pytest.mark.parametrize("M,N,K", [(1024, 1024, 8192), (256, 256, 8192)])
 def test_captured_gemm_replays_with_new_inputs(M, N, K):
     lim = g.device_limits()
-    pl = g.plan(M, N, K, num_sms=lim["sms"], max_clusters=lim["resident_pairs"])
+    # (cta_group 2: the persistent kernel, whose split in k the capture must turn off)
+    pl = g.plan(M, N, K, num_sms=lim["sms"], max_clusters=lim["resident_pairs"], options=g.Options(cta_group=2))
     assert pl["sk_tiles"] > 0 or pl["split_pieces"] > 1     # split in k when called directly
     A0, B0 = _operands(M, N, K, 700)
     As = torch.from_numpy(A0).cuda()
@@ -43,7 +44,7 @@ def test_captured_gemm_replays_with_new_inputs(M, N, K):
     Cs = torch.empty((M, N), dtype=torch.float16, device="cuda")
     items = 64
     trace = torch.zeros((lim["resident_pairs"] * items * 8,), dtype=torch.int64, device="cuda")
-    opts = g.Options(trace=trace.data_ptr(), trace_items=items)
+    opts = g.Options(trace=trace.data_ptr(), trace_items=items, cta_group=2)
     g.gemm_f16_nt(As, Bs, Cs, options=opts)          # warm-up outside the capture
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()

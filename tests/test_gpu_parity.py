@@ -108,13 +108,14 @@ def test_n_split(shape, max_clusters, schedule, split):
     M, N, K = shape
     A = inputs.draw((M, K), inputs.U, 95 + M)
     B = inputs.draw((N, K), inputs.U, 96 + N)
-    o = g.Options(cluster_pairs=1, max_clusters=max_clusters, schedule=schedule)
+    # (cta_group 2: the persistent kernel; small problems default to the small-problem kernel)
+    o = g.Options(cluster_pairs=1, cta_group=2, max_clusters=max_clusters, schedule=schedule)
     pl = g.plan(M, N, K, options=o)
     assert pl["tail_split"] == split and pl["sk_tiles"] == 0
     C = run(A, B, options=o)
     check_close(C, oracle.gemm_f16_nt(A, B), K, f"N-split {shape}")
     # each output's k order is the same whatever the MMA width: identical to whole tiles
-    whole = run(A, B, options=g.Options(cluster_pairs=1, max_clusters=max_clusters, schedule=1))
+    whole = run(A, B, options=g.Options(cluster_pairs=1, cta_group=2, max_clusters=max_clusters, schedule=1))
     assert np.array_equal(C.view(np.uint16), whole.view(np.uint16))
 
 
@@ -122,7 +123,7 @@ def test_n_split_integers_and_fp16_accumulator():
     M, N, K = 1300, 1000, 320                     # 24 tiles of 5 k-blocks: all cut in two
     A = inputs.draw((M, K), inputs.I2, 97)
     B = inputs.draw((N, K), inputs.I2, 98)
-    one = g.Options(cluster_pairs=1)
+    one = g.Options(cluster_pairs=1, cta_group=2)
     assert g.plan(M, N, K, options=one)["tail_split"] == 2
     check_bitexact(run(A, B, options=one), oracle.gemm_f16_nt(A, B), "N-split int")
     A16 = (A * (np.arange(K) % 4 == 0)).astype(np.float16)   # partial sums exact in fp16

@@ -130,7 +130,9 @@ def test_plan_stream_k_schedule():
     # wave of whole tiles left; shallow last waves take the N-split instead
     assert g.plan(6144, 4096, 4096, num_sms=152)["sk_tiles"] == 4 + 76
     assert g.plan(4096, 11008, 4096, num_sms=152)["sk_tiles"] == 4 + 76   # 9.5 % of slots idle
-    p = g.plan(512, 4096, 4096, num_sms=152)              # 32 tiles of 64 k-blocks: two split pieces each
+    pers = g.Options(cta_group=2)                         # the persistent kernel (small problems
+    # default to the small-problem kernel; test_plan_small_kernel)
+    p = g.plan(512, 4096, 4096, num_sms=152, options=pers)  # 32 tiles of 64 k-blocks: two split pieces each
     assert (p["sk_tiles"], p["tail_split"], p["split_pieces"], p["clusters"]) == (0, 1, 2, 64)
     p = g.plan(4096, 4096, 1024, num_sms=152)             # 16 k-blocks
     assert (p["sk_tiles"], p["tail_split"], p["tail_tiles"]) == (0, 2, 28)
@@ -151,7 +153,7 @@ def test_plan_stream_k_schedule():
     assert (p["sk_tiles"], p["tail_split"]) == (0, 1)
     # fewer tiles than pairs and deep k (>= 48 k-blocks): every tile cut into
     # s = 2, 4 or 8 split pieces, the largest with tiles * s <= pairs
-    one = g.Options(cluster_pairs=1)
+    one = g.Options(cluster_pairs=1, cta_group=2)
     p = g.plan(1024, 1024, 8192, options=one)             # 16 tiles x 128 k-blocks: 4 pieces
     assert (p["sk_tiles"], p["split_pieces"], p["clusters"], p["tail_split"]) == (0, 4, 64, 1)
     assert p["workspace_bytes"] == 64 * 2 * 4 * 8 + 64 * 2 * 128 * 256 * 4
@@ -172,17 +174,18 @@ def test_plan_stream_k_schedule():
     p = g.plan(256, 256, 4096, options=g.Options(schedule=2))   # forced: one k-block per pair
     assert (p["sk_tiles"], p["clusters"], p["split_pieces"]) == (1, 64, 1)
     with pytest.raises(g.GemmError):
-        g.plan(256, 256, 256, options=g.Options(schedule=5))
+        g.plan(256, 256, 256, options=g.Options(schedule=6))
 
 
 def test_plan_n_split():
     # fewer tiles than pairs and too few k-blocks for stream-K: each tile is cut
     # along N into s = 2 or 4 slices, the largest with tiles·s <= pairs
-    p = g.plan(256, 256, 256)                             # 1 tile x 4 k-blocks
+    pers = g.Options(cta_group=2)                         # the persistent kernel
+    p = g.plan(256, 256, 256, options=pers)               # 1 tile x 4 k-blocks
     assert (p["tail_tiles"], p["tail_split"], p["clusters"], p["grid_ctas"], p["sk_tiles"]) == (1, 4, 4, 8, 0)
-    p = g.plan(300, 520, 328, options=g.Options(cluster_pairs=1))   # 6 tiles x 6 k-blocks
+    p = g.plan(300, 520, 328, options=g.Options(cluster_pairs=1, cta_group=2))   # 6 tiles x 6 k-blocks
     assert (p["tail_tiles"], p["tail_split"], p["clusters"]) == (6, 4, 24)
-    p = g.plan(256 * 6, 256 * 5, 256)                     # 30 tiles: 30·2 <= 76 < 30·4
+    p = g.plan(256 * 6, 256 * 5, 256, options=pers)       # 30 tiles: 30·2 <= 76 < 30·4
     assert (p["tail_tiles"], p["tail_split"], p["clusters"]) == (30, 2, 60)
     # not for full waves (a narrower MMA is not faster per k-block), unless forced (3)
     for shape in ((8192, 8192, 8192), (16384, 14336, 4096)):
@@ -239,7 +242,7 @@ def test_plan_edges_and_options():
     # the default build has one pair per cluster for every pitch
     p = g.plan(4000, 3000, 5000)
     assert (p["cluster_pairs"], p["m_tiles"], p["n_tiles"]) == (1, 16, 12)
-    p = g.plan(100, 100, 8)                        # one pair tile, rank-1 rows all out of range,
+    p = g.plan(100, 100, 8, options=g.Options(cta_group=2))   # one pair tile, rank-1 rows all out of range,
     # cut into four 64-column slices (the last two lie wholly past N and store nothing)
     assert (p["num_tiles"], p["clusters"], p["grid_ctas"], p["tail_split"]) == (1, 4, 8, 4)
     p = g.plan(100, 100, 8, options=g.Options(schedule=1))
@@ -339,3 +342,49 @@ def test_noalloc_scratch_limit_condition():
                 assert g.plan(*shape, num_sms=sms, options=o)["workspace_bytes"] <= limit
     big = g.plan(4096, 4096, 4096, num_sms=176, options=g.Options(schedule=2))
     assert big["workspace_bytes"] > limit
+
+
+def test_plan_small_kernel():
+    # problems whose 128-row tiles fit on the SMs in one wave take the small-
+    # problem kernel: one CTA per 128 x bn tile, bn the narrowest of 32, 64, 128
+    # that fits, all of k in one CTA
+    for (M, N, K), (bn, tiles) in {(256, 256, 256): (32, 16), (64, 64, 64): (32, 2), (1024, 1024, 1024): (64, 128),
+                                   (512, 4096, 4096): (128, 128), (128, 4096, 4096): (32, 128),
+                                   (768, 768, 2048): (32, 144), (1000, 1000, 1000): (64, 128),
+                                   (1024, 1024, 8192): (64, 128)}.items():
+        p = g.plan(M, N, K, num_sms=152)
+        assert (p["kernel"], p["cta_group"], p["tile_m"], p["tile_n"]) == (1, 1, 128, bn), (M, N, K)
+        assert (p["num_tiles"], p["clusters"], p["grid_ctas"]) == (tiles, tiles, tiles), (M, N, K)
+        assert (p["sk_tiles"], p["split_pieces"], p["tail_split"], p["workspace_bytes"]) == (0, 1, 1, 0)
+        assert p["k_blocks"] == -(-K // 64) and p["smem_bytes"] <= 232448
+        assert p["tmem_cols"] == max(32, bn)
+    # more than one wave, or k deeper than 128 k-blocks: the persistent kernel
+    for M, N, K in ((2048, 2048, 2048), (4096, 1024, 1024), (8192, 8192, 8192), (256, 256, 8256), (256, 256, 1 << 16)):
+        assert g.plan(M, N, K, num_sms=152)["kernel"] == 0, (M, N, K)
+    # the wave is counted on the given SM count
+    assert g.plan(1024, 1024, 1024, num_sms=100)["tile_n"] == 128
+    # any persistent-kernel option keeps the persistent kernel
+    for o in (g.Options(cta_group=2), g.Options(cta_group=1), g.Options(swizzle=4), g.Options(max_clusters=8),
+              g.Options(schedule=1), g.Options(schedule=3), g.Options(a_layout=1), g.Options(b_layout=1),
+              g.Options(accumulate=1)):
+        assert g.plan(256, 256, 256, options=o)["kernel"] == 0
+    # forced (schedule 5): any shape, CTA group and tile width asked for
+    p = g.plan(8192, 8192, 8192, options=g.Options(schedule=5))
+    assert (p["kernel"], p["cta_group"], p["tile_n"], p["num_tiles"]) == (1, 1, 128, 64 * 64)
+    p = g.plan(300, 520, 328, options=g.Options(schedule=5, cta_group=2, tile_n=64))
+    assert (p["kernel"], p["cta_group"], p["tile_m"], p["tile_n"], p["m_tiles"], p["n_tiles"]) == (1, 2, 256, 64, 2, 9)
+    assert (p["clusters"], p["grid_ctas"]) == (18, 36)
+    for bad in (g.Options(schedule=5, tile_n=48), g.Options(schedule=5, tile_n=256), g.Options(tile_n=16),
+                g.Options(schedule=5, a_layout=1), g.Options(schedule=5, b_layout=1),
+                g.Options(schedule=5, accumulate=1)):
+        with pytest.raises(g.GemmError):
+            g.plan(256, 256, 256, options=bad)
+    mc = g.library_mcast()
+    with pytest.raises(g.GemmError):
+        g.plan(256, 256, 256, options=g.Options(schedule=5, cluster_pairs=2), lib=mc)
+    # the multicast build plans the same small-problem kernel
+    assert g.plan(256, 256, 256, lib=mc)["kernel"] == 1
+    # its schedule: cluster c computes tile c (column-major), all of k
+    items = [g.schedule(300, 520, 328, c, options=g.Options(schedule=5, cta_group=2, tile_n=64)) for c in range(18)]
+    assert [(it[0]["m_tile"], it[0]["n_tile"], it[0]["kb0"], it[0]["kb1"]) for it in items] == \
+        [(c % 2, c // 2, 0, 6) for c in range(18)]

@@ -12,6 +12,10 @@ on without checking it itself:
   - the stream-K ranges are balanced across clusters to one k-block;
   - the plan's N-split is what the clusters run;
   - each item's coordinates are the raster's.
+Small problems default to the small-problem kernel, whose plan has one tile
+per cluster (tile c at m_tile = c % m_tiles, n_tile = c / m_tiles, all of k);
+the same checks cover it, and the cases that name cta_group 2 keep the
+persistent kernel for those shapes.
 """
 import pytest
 
@@ -27,10 +31,14 @@ CASES = [
     (8192, 8192, 8192, {}, 76),                       # whole tiles
     (8192, 8192, 8192, {"schedule": 2}, 76),          # stream-K forced
     (8192, 8192, 8192, {"schedule": 3}, 76),          # N-split tail forced
-    (256, 256, 256, {}, 76),                          # N-split in four
-    (256, 256, 8192, {}, 76),                         # one tile cut in k
-    (1024, 1024, 8192, {}, 64),                       # 16 tiles cut in k
-    (1024, 1024, 1024, {}, 76),
+    (256, 256, 256, {}, 76),                          # small-problem kernel: 16 tiles of 128 x 32
+    (256, 256, 256, {"cta_group": 2}, 76),            # persistent: N-split in four
+    (256, 256, 8192, {"cta_group": 2}, 76),           # one tile cut in k
+    (1024, 1024, 8192, {"cta_group": 2}, 64),         # 16 tiles cut in k
+    (1024, 1024, 1024, {}, 76),                       # small-problem kernel: 128 tiles of 128 x 64
+    (1024, 1024, 1024, {"cta_group": 2}, 76),
+    (512, 4096, 4096, {}, 76),                        # small-problem kernel: 128 x 128 tiles
+    (300, 520, 328, {"schedule": 5, "cta_group": 2, "tile_n": 64}, 76),   # forced: pairs, 256 x 64
     (4096, 4096, 1024, {}, 76),                       # shallow last wave: N-split
     (4000, 3000, 5000, {"_lib": "mcast"}, 36),        # two pairs per cluster (multicast build's default)
     (4000, 3000, 5000, {}, 76),                       # one pair: the default build
@@ -40,10 +48,12 @@ CASES = [
     (700, 900, 1000, {"cta_group": 1}, 152),
     (700, 900, 1000, {"cta_group": 1, "schedule": 2}, 152),
     (1, 1, 1, {}, 76),
+    (1, 1, 1, {"cta_group": 2}, 76),
     (70000, 300, 64, {}, 76),
     (256, 512, 1 << 20, {}, 76),
-    (1024, 1024, 8192, {}, 76),                       # split pieces: 16 tiles x 4
-    (256, 256, 8192, {}, 76),                         # one tile in 8 pieces
+    (1024, 1024, 8192, {"cta_group": 2}, 76),         # split pieces: 16 tiles x 4
+    (256, 256, 8192, {"cta_group": 2}, 76),           # one tile in 8 pieces
+    (256, 256, 16384, {}, 76),                        # deeper than the small kernel takes: 8 pieces
     (300, 520, 328, {"schedule": 4}, 76),             # forced: pieces of 1 or 2 k-blocks
     (700, 900, 1000, {"cta_group": 1, "schedule": 4}, 152),
 ]
@@ -163,11 +173,29 @@ def check_balance_and_coordinates(pl, items, tile_coord=g.tile_coord):
         assert sum(sk) == pl["sk_tiles"] * pl["k_blocks"]
     for its in items:
         for it in its:
+            if pl["kernel"] == 1:      # the small-problem kernel: column-major tile order
+                assert (it["m_tile"], it["n_tile"]) == (it["tile"] % pl["m_tiles"], it["tile"] // pl["m_tiles"])
+                continue
             assert (it["m_tile"], it["n_tile"]) == tile_coord(it["tile"], pl["m_tiles"], pl["n_tiles"],
                                                               pl["swizzle"])
 
 
+def check_small(pl, items):
+    """The small-problem kernel: one whole-k tile per cluster, cluster c on tile c,
+    as many clusters as tiles of 128·cta_group × tile_n."""
+    if pl["kernel"] != 1:
+        return
+    assert pl["clusters"] == pl["num_tiles"] and pl["grid_ctas"] == pl["num_tiles"] * pl["cta_group"]
+    assert pl["tile_m"] == 128 * pl["cta_group"] and pl["tile_n"] in (32, 64, 128)
+    assert (pl["sk_tiles"], pl["tail_split"], pl["split_pieces"], pl["workspace_bytes"]) == (0, 1, 1, 0)
+    for c, its in enumerate(items):
+        assert len(its) == 1
+        it = its[0]
+        assert (it["tile"], it["kb0"], it["kb1"], it["kind"], it["parts"]) == (c, 0, pl["k_blocks"], WHOLE, 1)
+
+
 def check_schedule(pl, items, tile_coord=g.tile_coord):
+    check_small(pl, items)
     check_coverage(pl, items)
     check_partials_and_owners(pl, items)
     check_balance_and_coordinates(pl, items, tile_coord)

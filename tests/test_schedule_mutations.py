@@ -71,9 +71,9 @@ CASES = [
     (4096, 4096, 4096, {}, 76),
     (8192, 8192, 8192, {"schedule": 2}, 76),
     (8192, 8192, 8192, {"schedule": 3}, 76),
-    (256, 256, 256, {}, 76),
-    (256, 256, 8192, {}, 76),
-    (1024, 1024, 8192, {}, 64),
+    (256, 256, 256, {"cta_group": 2}, 76),            # (the persistent kernel: small problems
+    (256, 256, 8192, {"cta_group": 2}, 76),           #  default to the small-problem kernel)
+    (1024, 1024, 8192, {"cta_group": 2}, 64),
     (4096, 4096, 1024, {}, 76),
     (4000, 3000, 5000, {}, 36),
     (1300, 1000, 320, {"schedule": 3, "cluster_pairs": 1}, 76),
@@ -82,6 +82,7 @@ CASES = [
     (300, 520, 328, {"schedule": 4}, 76),             # split pieces of 1 or 2 k-blocks
     (256, 256, 8192, {"schedule": 4}, 76),            # one tile in 8 pieces
 ]
+assert all(g.plan(M, N, K, max_clusters=mc, options=g.Options(**o))["kernel"] == 0 for M, N, K, o, mc in CASES)
 
 MUTATIONS = {
     "stream_k_ranges_rounded_per_cluster": ("return p.sk_units * c / G;", "return p.sk_units / G * c;"),

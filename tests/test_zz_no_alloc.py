@@ -34,10 +34,11 @@ def _call(fn, A, B, C, stream):
 
 
 @pytest.mark.parametrize("M,N,K,uses_scratch,ints", [
-    (1024, 1024, 8192, True, False),     # 16 pair tiles, each in 4 split pieces over 64 pairs
+    (1024, 1024, 12288, True, False),    # 16 pair tiles, each in 4 split pieces over 64 pairs
     (6144, 4096, 4096, True, False),     # 384 tiles: last wave 4/76 full, deep k: stream-K part
-    (1024, 1024, 8192, True, True),      # integers: exact, whatever the summation order
-    (300, 520, 328, False, False),       # whole tiles, no scratch needed
+    (1024, 1024, 12288, True, True),     # integers: exact, whatever the summation order
+    (300, 520, 328, False, False),       # the small-problem kernel: no scratch needed
+    (1024, 1024, 1024, False, True),     # the same, 128 tiles of 128 x 64, integers
 ])
 def test_noalloc_matches_oracle_and_gemm_f16_nt_on_two_calls(M, N, K, uses_scratch, ints):
     if not torch.cuda.is_available():
@@ -76,7 +77,7 @@ def test_noalloc_call_under_capture_replays_with_new_inputs():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     lib = g.library()
-    M, N, K = 1024, 1024, 8192                    # split in k when called directly
+    M, N, K = 1024, 1024, 12288                   # split in k when called directly
     assert g.launch_plan(M, N, K)["workspace_bytes"] > 0
     Ad = torch.empty((M, K), dtype=torch.float16, device="cuda")
     Bd = torch.empty((N, K), dtype=torch.float16, device="cuda")
