@@ -932,19 +932,14 @@ using Cfg2Bf = KCfg<2, 256, 6, 1, true>;    // the same with bf16 operands and r
 using Cfg1Bf = KCfg<1, 256, 4, 1, true>;
 using Cfg2A16 = KCfg<2, 256, 6, 1, false, true>;   // the fp16 ones with an fp16 accumulator
 using Cfg1A16 = KCfg<1, 256, 4, 1, false, true>;
-// The small-problem kernel's tiles: 128·CG × BN, one per cluster.
+// The small-problem kernel's tiles: 128·CG × BN, one per cluster (each also
+// built for bf16 and for split-K: SCfg's last two parameters).
 using S1n32 = SCfg<1, 32, 8>;
 using S1n64 = SCfg<1, 64, 8>;
 using S1n128 = SCfg<1, 128, 6>;
 using S2n32 = SCfg<2, 32, 8>;
 using S2n64 = SCfg<2, 64, 8>;
 using S2n128 = SCfg<2, 128, 8>;
-using S1n32Bf = SCfg<1, 32, 8, true>;
-using S1n64Bf = SCfg<1, 64, 8, true>;
-using S1n128Bf = SCfg<1, 128, 6, true>;
-using S2n32Bf = SCfg<2, 32, 8, true>;
-using S2n64Bf = SCfg<2, 64, 8, true>;
-using S2n128Bf = SCfg<2, 128, 8, true>;
 #if G16_MCAST_LIB
 using Cfg2x2 = KCfg<2, 256, 6, 2>; // two CTA pairs per cluster sharing A: 256×512 cluster tile
 using Cfg2x2Bf = KCfg<2, 256, 6, 2, true>;
@@ -960,6 +955,13 @@ template <class... Cfgs>
 bool allow_smem_small() {
     return ((cudaFuncSetAttribute(gemm_f16_nt_small_kernel<Cfgs>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   Cfgs::kSmemBytes) == cudaSuccess) && ...);
+}
+// every small-kernel configuration of one operand type, with and without split-K
+template <bool BF, bool SP>
+bool allow_smem_small_all() {
+    return allow_smem_small<SCfg<1, 32, S1n32::kStages, BF, SP>, SCfg<1, 64, S1n64::kStages, BF, SP>,
+                            SCfg<1, 128, S1n128::kStages, BF, SP>, SCfg<2, 32, S2n32::kStages, BF, SP>,
+                            SCfg<2, 64, S2n64::kStages, BF, SP>, SCfg<2, 128, S2n128::kStages, BF, SP>>();
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -1033,8 +1035,8 @@ gemm_status_t setup_device(int dev, DeviceState& st) {
     }
     if (!allow_smem<Cfg2>() || !allow_smem<Cfg1>() || !allow_smem<Cfg2Bf>() || !allow_smem<Cfg1Bf>() ||
         !allow_smem<Cfg2A16>() || !allow_smem<Cfg1A16>() ||
-        !allow_smem_small<S1n32, S1n64, S1n128, S2n32, S2n64, S2n128, S1n32Bf, S1n64Bf, S1n128Bf, S2n32Bf,
-                          S2n64Bf, S2n128Bf>()) {
+        !allow_smem_small_all<false, false>() || !allow_smem_small_all<false, true>() ||
+        !allow_smem_small_all<true, false>() || !allow_smem_small_all<true, true>()) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
@@ -1108,6 +1110,11 @@ int64_t flags_bytes(int ctas, int64_t clusters) {
 int64_t workspace_bytes(int ctas, int64_t clusters) {
     return flags_bytes(ctas, clusters) + clusters * ctas * int64_t(kBlockM) * kCtaTileN * 4;
 }
+// The small-problem kernel's split-K workspace: the same flags, then one
+// 128 × bn fp32 partial tile per CTA.
+int64_t small_workspace_bytes(int ctas, int bn, int64_t clusters) {
+    return flags_bytes(ctas, clusters) + clusters * ctas * int64_t(kBlockM) * bn * 4;
+}
 
 // Workspace slots to reserve: GEMM_F16_NT_WORKSPACE_SLOTS (0..8) if set to a
 // number, else 4.
@@ -1127,6 +1134,8 @@ void setup_workspace(DeviceState& st) {
     int64_t need = workspace_bytes(2, st.max_clusters2);
     if (workspace_bytes(1, st.max_ctas1) > need) need = workspace_bytes(1, st.max_ctas1);
     if (workspace_bytes(4, st.max_clusters4) > need) need = workspace_bytes(4, st.max_clusters4);
+    for (int cg = 1; cg <= 2; ++cg)   // the small kernel's split-K: at most one wave of 128-wide tiles
+        if (small_workspace_bytes(cg, 128, st.sms / cg) > need) need = small_workspace_bytes(cg, 128, st.sms / cg);
     const int want = workspace_slots_setting();
     int got = 0;
     for (; got < want; ++got) {
@@ -1256,13 +1265,15 @@ int resident_clusters_for(const DeviceState& st, const gemm_f16_nt_options_t& r)
 
 bool small_tile_n_valid(int tn) { return tn == 0 || tn == 32 || tn == 64 || tn == 128; }
 
-// Ring depth, shared memory and tensor-memory columns of SCfg<cg, bn>.
-void small_cfg_info(int cg, int bn, int32_t* stages, int32_t* smem, int32_t* tmem) {
+// Ring depth, shared memory, tensor-memory columns and most split-K pieces of
+// SCfg<cg, bn>.
+void small_cfg_info(int cg, int bn, int32_t* stages, int32_t* smem, int32_t* tmem, int32_t* max_pieces) {
 #define G16_SMALL_INFO(C, N, T)                  \
     if (cg == C && bn == N) {                     \
         *stages = T::kStages;                     \
         *smem = T::kSmemBytes;                    \
         *tmem = T::kTmemCols;                     \
+        *max_pieces = T::kMaxPieces;              \
         return;                                   \
     }
     G16_SMALL_INFO(1, 32, S1n32)
@@ -1272,7 +1283,7 @@ void small_cfg_info(int cg, int bn, int32_t* stages, int32_t* smem, int32_t* tme
     G16_SMALL_INFO(2, 64, S2n64)
     G16_SMALL_INFO(2, 128, S2n128)
 #undef G16_SMALL_INFO
-    *stages = *smem = *tmem = 0;
+    *stages = *smem = *tmem = *max_pieces = 0;
 }
 
 // The small kernel's automatic tile width: the narrowest of 32, 64 and 128
@@ -1289,10 +1300,32 @@ int small_tile_n(int64_t M, int64_t N, int cg, int32_t num_sms) {
     return 0;
 }
 
-// Deepest k (in 64-wide k-blocks) for which the automatic plan takes the small
-// kernel; deeper problems with few tiles go to the persistent kernel's split
-// pieces, which spread k over more SMs.
+// Deepest k per CTA (in 64-wide k-blocks) for which the automatic plan takes the
+// small kernel; deeper problems go to the persistent kernel.
 constexpr int64_t kSmallMaxKb = 128;
+// Split-K in the small kernel: each piece at least kSmallMinPieceKb k-blocks
+// long, all tiles' pieces in one wave, at most as many pieces as the owner can
+// take the others' partials of into its idle ring at once (8 for 32-wide
+// tiles, 4 for 64- and 128-wide ones).
+constexpr int64_t kSmallMinPieceKb = 8;
+// ... and only from kSmallMinSplitKb k-blocks: the exchange of partials costs
+// about 2.5 us (write, flag, load back: L2 round trips), about 15 k-blocks of
+// a piece's main loop.  Measured at 256×256×1024 (16 k-blocks): 9.5 us in two
+// pieces.
+constexpr int64_t kSmallMinSplitKb = 32;
+
+// The number of split-K pieces per tile: the largest power of two within
+// those limits.  Few tiles and deep k: at 256×256×4096, 16 tiles of 128×32
+// and 64 k-blocks become 128 pieces of 8.
+int64_t small_pieces(int64_t tiles, int64_t kb, int cg, int bn, int32_t num_sms) {
+    int32_t st, sm, tm, max_pieces;
+    small_cfg_info(cg, bn, &st, &sm, &tm, &max_pieces);
+    const int64_t slots = num_sms / cg;
+    int64_t s = 1;
+    while (kb >= kSmallMinSplitKb && s < max_pieces && tiles * s * 2 <= slots && kb >= s * 2 * kSmallMinPieceKb)
+        s *= 2;
+    return s;
+}
 
 // Whether the automatic plan takes the small-problem kernel: every automatic
 // option (no CTA group, schedule, raster, grid or tile width asked for), the
@@ -1308,30 +1341,38 @@ bool small_kernel_pays(int64_t M, int64_t N, int64_t K, const gemm_f16_nt_option
     if (o && (o->cta_group != 0 || o->swizzle != 0 || o->max_clusters != 0 || o->schedule != 0 ||
               o->cluster_pairs > 1 || o->tile_n != 0))
         return false;
-    return cdiv(K, kBlockK) <= kSmallMaxKb && small_tile_n(M, N, 1, num_sms) != 0;
+    const int bn = small_tile_n(M, N, 1, num_sms);
+    if (bn == 0) return false;
+    const int64_t tiles = cdiv(M, kBlockM) * cdiv(N, bn), kb = cdiv(K, kBlockK);
+    return cdiv(kb, small_pieces(tiles, kb, 1, bn, num_sms)) <= kSmallMaxKb;
 }
 
-gemm_status_t small_plan(int64_t M, int64_t N, int64_t K, int cg, int bn, gemm_f16_nt_plan_t* pl) {
+gemm_status_t small_plan(int64_t M, int64_t N, int64_t K, int cg, int bn, int32_t num_sms, bool allow_split_k,
+                         gemm_f16_nt_plan_t* pl) {
     memset(pl, 0, sizeof(*pl));
     const int64_t mt = cdiv(M, int64_t(kBlockM) * cg), nt = cdiv(N, bn);
     const int64_t tiles = mt * nt;
     if (tiles * cg >= (int64_t(1) << 31)) return GEMM_ERR_INVALID_VALUE;
+    const int64_t kb = cdiv(K, kBlockK);
+    const int64_t pieces = allow_split_k ? small_pieces(tiles, kb, cg, bn, num_sms) : 1;
     pl->kernel = 1;
     pl->cta_group = cg;
     pl->cluster_pairs = 1;
     pl->tile_m = kBlockM * cg;
     pl->tile_n = bn;
     pl->block_k = kBlockK;
-    small_cfg_info(cg, bn, &pl->stages, &pl->smem_bytes, &pl->tmem_cols);
+    int32_t max_pieces = 0;
+    small_cfg_info(cg, bn, &pl->stages, &pl->smem_bytes, &pl->tmem_cols, &max_pieces);
     pl->m_tiles = int32_t(mt);
     pl->n_tiles = int32_t(nt);
     pl->k_blocks = int32_t(cdiv(K, kBlockK));
     pl->num_tiles = tiles;
     pl->swizzle = 1;
-    pl->clusters = int32_t(tiles);
-    pl->grid_ctas = int32_t(tiles * cg);
+    pl->clusters = int32_t(tiles * pieces);
+    pl->grid_ctas = int32_t(tiles * pieces * cg);
     pl->tail_split = 1;
-    pl->split_pieces = 1;
+    pl->split_pieces = int32_t(pieces);
+    pl->workspace_bytes = pieces > 1 ? small_workspace_bytes(cg, bn, tiles * pieces) : 0;
     return GEMM_OK;
 }
 
@@ -1359,7 +1400,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
         const int scg = (o && o->cta_group) ? o->cta_group : 1;
         int bn = tn ? tn : small_tile_n(M, N, scg, num_sms);
         if (bn == 0) bn = 128;   // forced on a problem too large for one wave: widest tiles
-        return small_plan(M, N, K, scg, bn, pl);
+        return small_plan(M, N, K, scg, bn, num_sms, allow_split_k && acc == 0, pl);
     }
     memset(pl, 0, sizeof(*pl));
     pl->cta_group = cg;
@@ -1574,7 +1615,8 @@ gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t
 template <class Cfg>
 gemm_status_t launch_small(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t K, const uint16_t* A,
                            int64_t lda, const uint16_t* B, int64_t ldb, uint16_t* C, int64_t ldc,
-                           cudaStream_t stream, const gemm_f16_nt_options_t* o, uint32_t* watchdog) {
+                           cudaStream_t stream, const gemm_f16_nt_options_t* o, uint32_t* watchdog,
+                           void* workspace) {
     SmallParams p;
     memset(&p, 0, sizeof(p));
     gemm_status_t s;
@@ -1592,6 +1634,14 @@ gemm_status_t launch_small(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, i
     p.item_timeout_ns = p.timeout_ns + uint64_t(pl.k_blocks) * kItemWaitNsPerKb;
     p.watchdog = watchdog;
     p.inject_stall = o ? o->inject_stall : 0;
+    p.pieces = uint32_t(pl.split_pieces > 1 ? pl.split_pieces : 1);
+    if (p.pieces > 1) {
+        if (!workspace) return GEMM_ERR_INVALID_VALUE;
+        uint8_t* ws = static_cast<uint8_t*>(workspace);
+        p.flags = reinterpret_cast<uint64_t*>(ws);
+        p.partials = reinterpret_cast<float*>(ws + flags_bytes(Cfg::kCG, pl.clusters));
+    }
+    p.launch_id = ++g_launch_seq;
 
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
@@ -1620,10 +1670,14 @@ gemm_status_t launch_small(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, i
 template <bool BF>
 gemm_status_t launch_small_any(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t K, const uint16_t* A,
                                int64_t lda, const uint16_t* B, int64_t ldb, uint16_t* C, int64_t ldc,
-                               cudaStream_t stream, const gemm_f16_nt_options_t* o, uint32_t* watchdog) {
-#define G16_SMALL_LAUNCH(CG, N_, S_)                                                                 \
-    if (pl.cta_group == CG && pl.tile_n == N_)                                                       \
-        return launch_small<SCfg<CG, N_, S_::kStages, BF>>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, o, watchdog);
+                               cudaStream_t stream, const gemm_f16_nt_options_t* o, uint32_t* watchdog, void* ws) {
+#define G16_SMALL_LAUNCH(CG, N_, S_)                                                                    \
+    if (pl.cta_group == CG && pl.tile_n == N_)                                                          \
+        return pl.split_pieces > 1                                                                      \
+                   ? launch_small<SCfg<CG, N_, S_::kStages, BF, true>>(pl, M, N, K, A, lda, B, ldb, C, ldc, \
+                                                                        stream, o, watchdog, ws)         \
+                   : launch_small<SCfg<CG, N_, S_::kStages, BF, false>>(pl, M, N, K, A, lda, B, ldb, C, ldc, \
+                                                                         stream, o, watchdog, ws);
     G16_SMALL_LAUNCH(1, 32, S1n32)
     G16_SMALL_LAUNCH(1, 64, S1n64)
     G16_SMALL_LAUNCH(1, 128, S1n128)
@@ -1702,8 +1756,8 @@ gemm_status_t launch_any(bool bf16, const gemm_f16_nt_plan_t& pl, int64_t M, int
                          const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb, uint16_t* C, int64_t ldc,
                          cudaStream_t stream, const gemm_f16_nt_options_t* ro, uint32_t* watchdog, void* ws) {
     if (pl.kernel == 1)
-        return bf16 ? launch_small_any<true>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, ro, watchdog)
-                    : launch_small_any<false>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, ro, watchdog);
+        return bf16 ? launch_small_any<true>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, ro, watchdog, ws)
+                    : launch_small_any<false>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, ro, watchdog, ws);
     if (bf16)
         return launch_cfg<Cfg2Bf, Cfg2x2Bf_, Cfg1Bf>(pl, M, N, K, A, lda, B, ldb, C, ldc, stream, ro, watchdog, ws);
     if (ro->accumulate == 1)
@@ -1983,14 +2037,20 @@ G16_EXPORT gemm_status_t gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, i
     if (s != GEMM_OK) return s;
     if (cluster < 0 || cluster >= pl.clusters) return GEMM_ERR_INVALID_VALUE;
     if (pl.kernel == 1) {
-        // the small-problem kernel: cluster c computes tile c, all of k
+        // the small-problem kernel: cluster c computes piece c % s of tile c / s
+        // (s = split_pieces, 1 without split-K); piece 0 owns the tile and adds
+        // the others' partials, each piece covers an equal share of the k-blocks
         if (max_items > 0) {
+            const int64_t np = pl.split_pieces, t = cluster / np, pc = cluster % np;
             gemm_f16_nt_item_t& o = items[0];
             memset(&o, 0, sizeof(o));
-            o.tile = cluster;
-            o.m_tile = cluster % pl.m_tiles;
-            o.n_tile = cluster / pl.m_tiles;
-            o.kb1 = pl.k_blocks;
+            o.tile = int32_t(t);
+            o.m_tile = int32_t(t % pl.m_tiles);
+            o.n_tile = int32_t(t / pl.m_tiles);
+            o.kb0 = int32_t(pl.k_blocks * pc / np);
+            o.kb1 = int32_t(pl.k_blocks * (pc + 1) / np);
+            o.kind = np == 1 ? g16::kItemWhole : (pc == 0 ? g16::kItemOwner : g16::kItemPartialOut);
+            o.partners = (np > 1 && pc == 0) ? int32_t(np - 1) : 0;
             o.parts = 1;
             o.pieces = 1;
         }

@@ -16,7 +16,13 @@
 //     loop with one elected lane issuing, then all four warps drain the accumulator — warp w
 //     reads tensor-memory lanes 32w..32w+31, which are rows of the tile — and
 //     store their rows of C straight from registers, 16 bytes at a time;
-//   - tensor memory: BN columns, one accumulator; shared memory: the ring.
+//   - tensor memory: BN columns, one accumulator; shared memory: the ring;
+//   - with few tiles and deep k, each tile's k range is cut into `pieces`
+//     equal pieces on consecutive clusters (split-K): the first piece owns
+//     the tile; the others write their fp32 partial tiles to the workspace
+//     and publish per-warp flags tagged with the launch's id, and the owner
+//     adds them to its own accumulator in piece order (k order) before the
+//     rounding, so results do not depend on timing.
 // A and B are K-major ([M, K] and [N, K] rows); the accumulator is fp32 and the
 // result fp16 or bf16, rounded to nearest even, as in the persistent kernel.
 // The operation and the tile loop are those of the Tilus tutorial's kernels
@@ -31,9 +37,10 @@ namespace g16 {
 
 constexpr int kSmallThreads = 128;   // 4 warps: producer lane, MMA lane, then all four drain
 
-template <int CG, int BN, int STAGES, bool BF = false>
+template <int CG, int BN, int STAGES, bool BF = false, bool SPLIT = false>
 struct SCfg {
     static constexpr int kCG = CG;
+    static constexpr bool kSplit = SPLIT;            // split-K: the launch's tiles are cut into pieces
     static constexpr int kBN = BN;
     static constexpr int kStages = STAGES;
     static constexpr bool kBF = BF;
@@ -45,6 +52,12 @@ struct SCfg {
     static constexpr int kTmemCols = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
     static constexpr int kRingBytes = STAGES * (kABytes + kBBytes);
     static constexpr int kCtlBytes = 256;
+    // split-K: each warp's scratch in the (idle by then) ring, and the most
+    // pieces a tile whose partials fit in it at once (a power of two, <= 8)
+    static constexpr int kScratchBytes = kRingBytes / 4;
+    static constexpr int kPartialBytes = BN * 32 * 4;             // one warp's 32 rows x BN fp32
+    static constexpr int kMaxPieces = (kScratchBytes / kPartialBytes + 1) >= 8 ? 8
+                                    : (kScratchBytes / kPartialBytes + 1) >= 4 ? 4 : 2;
     static constexpr int kSmemBytes = 1024 + kRingBytes + kCtlBytes;
     // kind::f16 instruction descriptor: D fp32, A/B fp16 or bf16, both K-major,
     // N>>3 at bit 17, M>>4 at bit 24 (as in KCfg).
@@ -56,6 +69,7 @@ struct SCfg {
     static_assert(kBRows % 8 == 0, "B rows per CTA must fill whole 8-row swizzle atoms");
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "stages stay 1 KB aligned");
     static_assert(kSmemBytes <= 232448, "dynamic shared memory limit per CTA");
+    static_assert(kPartialBytes <= kScratchBytes, "a partial tile fits in a warp's scratch");
 };
 
 template <int STAGES>
@@ -64,6 +78,7 @@ struct SmallCtl {
     uint64_t empty[STAGES];   // stage consumed (each CTA's own copy)
     uint64_t acc_full;        // accumulator complete
     uint64_t mma_done;        // every MMA retired (teardown)
+    uint64_t xfer[4];         // split-K: the other pieces' partials landed in a warp's scratch
     uint32_t tmem_base;
     uint32_t abort_flag;
 };
@@ -81,6 +96,11 @@ struct SmallParams {
     uint64_t item_timeout_ns;
     uint32_t* watchdog;
     int32_t inject_stall;
+    // split-K (pieces > 1): cluster c runs piece c % pieces of tile c / pieces
+    uint32_t pieces;
+    float* partials;       // [cluster][cta rank][warp][BN/4][32 rows] float4: a piece's partial tile
+    uint64_t* flags;       // [cluster][cta rank][warp]: launch_id once that warp's partial is written
+    uint64_t launch_id;    // unique per launch, so stale flags never match
 };
 
 template <class Cfg>
@@ -99,7 +119,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) gemm_f16_nt_small_kernel(con
     const uint32_t warp = __shfl_sync(0xffffffffu, threadIdx.x >> 5, 0);
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t prank = CG == 2 ? ptx::cluster_ctarank() : 0u;   // rank in the pair
-    const uint32_t tile = CG == 2 ? ptx::cluster_id_x() : blockIdx.x;
+    const uint32_t cluster = CG == 2 ? ptx::cluster_id_x() : blockIdx.x;
 
     const uint32_t full0 = ptx::smem_u32(&ctl->full[0]);
     const uint32_t empty0 = ptx::smem_u32(&ctl->empty[0]);
@@ -113,6 +133,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) gemm_f16_nt_small_kernel(con
         }
         ptx::mbar_init(acc_full, 1);
         ptx::mbar_init(mma_done, 1);
+        for (int q = 0; q < 4; ++q) ptx::mbar_init(ptx::smem_u32(&ctl->xfer[q]), 1);
         ctl->abort_flag = 0u;
         ptx::fence_mbarrier_init();
     }
@@ -144,6 +165,12 @@ __global__ void __launch_bounds__(kSmallThreads, 1) gemm_f16_nt_small_kernel(con
     Watch wi = w;   // waits that can span the whole main loop
     wi.limit_ns = p.item_timeout_ns;
 
+    // this cluster's tile and k-block range [kb0, kb1) (all of k without split-K)
+    const uint32_t tile = Cfg::kSplit ? cluster / p.pieces : cluster;
+    const uint32_t piece = Cfg::kSplit ? cluster - tile * p.pieces : 0u;
+    const uint32_t kb0 = Cfg::kSplit ? p.num_kb * piece / p.pieces : 0u;
+    const uint32_t kb1 = Cfg::kSplit ? p.num_kb * (piece + 1) / p.pieces : p.num_kb;
+    const uint32_t nkb = kb1 - kb0;
     const uint32_t mt = tile % p.m_tiles, nt = tile / p.m_tiles;
     const int32_t m0 = int32_t(mt * Cfg::kTileM + prank * kBlockM);   // this CTA's first row
     const int32_t n0 = int32_t(nt * BN);                               // the tile's first column
@@ -155,15 +182,15 @@ __global__ void __launch_bounds__(kSmallThreads, 1) gemm_f16_nt_small_kernel(con
             const int32_t b0 = n0 + int32_t(prank) * Cfg::kBRows;
             uint32_t issued = 0;
             bool ok = true;
-            for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
-                const uint32_t s = kb % uint32_t(S), ph = (kb / uint32_t(S)) & 1u;
+            for (uint32_t i = 0; i < nkb; ++i) {
+                const uint32_t s = i % uint32_t(S), ph = (i / uint32_t(S)) & 1u;
                 // (a fresh barrier's phase of parity 1 counts as complete: no wait on the first pass)
                 if (!wait(empty0 + 8 * s, ph ^ 1u, wi, kSiteProducerEmpty)) {
                     ok = false;
                     break;
                 }
                 if (prank == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * s, uint32_t(Cfg::kTxBytes));
-                const int32_t k0 = int32_t(kb * kBlockK);
+                const int32_t k0 = int32_t((kb0 + i) * kBlockK);
                 const uint32_t bar = full_tgt + 8 * s;
                 if constexpr (CG == 2) {
                     ptx::tma_load_2d_pair(sA + s * Cfg::kABytes, &p.tmA, k0, m0, bar);
@@ -179,8 +206,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1) gemm_f16_nt_small_kernel(con
                 if (prank == 0) {
                     const uint32_t n = issued < uint32_t(S) ? issued : uint32_t(S);
                     for (uint32_t i = 0; i < n; ++i) {
-                        const uint32_t kb = issued - 1u - i;
-                        if (!wait_drain(full0 + 8 * (kb % uint32_t(S)), (kb / uint32_t(S)) & 1u, p.timeout_ns))
+                        const uint32_t j = issued - 1u - i;
+                        if (!wait_drain(full0 + 8 * (j % uint32_t(S)), (j / uint32_t(S)) & 1u, p.timeout_ns))
                             atomicOr(p.watchdog, 1u | (1u << (7u + kSiteProducerDrain)));
                     }
                 } else {
@@ -201,7 +228,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) gemm_f16_nt_small_kernel(con
             const uint64_t ad0 = sdesc_sw128(sA), bd0 = sdesc_sw128(sB);
             uint32_t s = 0, ph = 0;
             bool ok = true;
-            for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+            for (uint32_t i = 0; i < nkb; ++i) {
                 const bool got = wait(full0 + 8 * s, ph, w, kSiteMmaFull);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
@@ -215,7 +242,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) gemm_f16_nt_small_kernel(con
 #pragma unroll
                     for (int k = 0; k < kBlockK / kUmmaK; ++k)   // 16 k = 32 bytes along the row: +2
                         ptx::mma_f16<CG>(tmem_base, ad + 2u * uint32_t(k), bd + 2u * uint32_t(k), Cfg::kIdesc,
-                                         (kb != 0 || k != 0) ? 1u : 0u);
+                                         (i != 0 || k != 0) ? 1u : 0u);
                     if constexpr (CG == 2) ptx::mma_commit_pair(empty0 + 8 * s, 0x3);
                     else ptx::mma_commit(empty0 + 8 * s);
                 }
@@ -245,13 +272,64 @@ __global__ void __launch_bounds__(kSmallThreads, 1) gemm_f16_nt_small_kernel(con
         uint32_t ok = 0;
         if (lane == 0) ok = wait(acc_full, 0, wi, kSiteEpiAccFull) ? 1u : 0u;
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok) {
+        const uint32_t taddr = tmem_base + ((warp * 32u) << 16);   // lanes 32w.. = rows 32w..
+        // this warp's partial tile and flag (split-K): [BN/4 column groups][32 rows]
+        // float4, so that the 32 lanes (rows) of one access cover 512 contiguous bytes
+        const uint32_t slot = (cluster * CG + prank) * 4u + warp;
+        constexpr uint32_t kSlotF4 = uint32_t(BN / 4) * 32u;           // float4 per warp partial
+        float4* const part = reinterpret_cast<float4*>(p.partials) + size_t(slot) * kSlotF4 + lane;
+        // a warp's scratch in the ring (split-K), same layout as its partial slot
+        const uint32_t scr = sA + warp * uint32_t(Cfg::kScratchBytes);
+        const uint32_t xfer = ptx::smem_u32(&ctl->xfer[warp]);
+        if (Cfg::kSplit && ok && piece != 0) {
+            // a partial piece: the fp32 partial tile through scratch to the
+            // workspace with one bulk copy a warp, then the flag once it is complete
             ptx::tc_fence_after();
-            const uint32_t taddr = tmem_base + ((warp * 32u) << 16);   // lanes 32w.. = rows 32w..
+#pragma unroll
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t v[32];
+                ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c0), v);
+                ptx::tmem_wait_ld();
+                ptx::reg_fence(v);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)   // float4 group c0/4 + e of this lane's row
+                    ptx::st_shared_v4(scr + ((uint32_t(c0 / 4 + e) * 32u + lane) << 4), v[4 * e], v[4 * e + 1],
+                                      v[4 * e + 2], v[4 * e + 3]);
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::bulk_store(part - lane, scr, uint32_t(Cfg::kPartialBytes));
+                ptx::bulk_commit_group();
+                ptx::bulk_wait_group_all();           // the partial is in global memory
+                ptx::fence_proxy_async_global();
+                ptx::st_release_u64(p.flags + slot, p.launch_id);
+            }
+        } else if (ok) {
+            ptx::tc_fence_after();
+            // the tile's owner: with split-K, lane i waits for piece i's same warp
+            // (all at once), then lane 0 loads their partials into scratch together
+            uint32_t okf = 1;
+            if constexpr (Cfg::kSplit) {
+                if (lane >= 1 && lane < p.pieces)
+                    okf = wait_flag(p.flags + slot + lane * uint32_t(CG) * 4u, p.launch_id, wi, kSiteStreamK) ? 1u : 0u;
+                okf = __all_sync(0xffffffffu, okf) ? 1u : 0u;
+                if (okf && lane == 0) {
+                    ptx::fence_proxy_async_global();
+                    ptx::mbar_arrive_expect_tx(xfer, (p.pieces - 1) * uint32_t(Cfg::kPartialBytes));
+                    for (uint32_t i = 1; i < p.pieces; ++i)
+                        ptx::bulk_load(scr + (i - 1) * uint32_t(Cfg::kPartialBytes),
+                                       part - lane + size_t(i) * uint32_t(CG) * 4u * kSlotF4,
+                                       uint32_t(Cfg::kPartialBytes), xfer);
+                }
+                if (okf && !wait(xfer, 0, wi, kSiteStreamK)) okf = 0;
+                okf = __all_sync(0xffffffffu, okf) ? 1u : 0u;
+            }
             const int32_t r = m0 + int32_t(warp * 32u + lane);
             uint16_t* crow = p.C + int64_t(r) * p.ldc;
 #pragma unroll
             for (int c0 = 0; c0 < BN; c0 += 64) {
+                if (!okf) break;
                 // up to 64 columns in registers per wait
                 constexpr int kPer = BN < 64 ? BN : 64;
                 uint32_t v[2][32];
@@ -260,6 +338,22 @@ __global__ void __launch_bounds__(kSmallThreads, 1) gemm_f16_nt_small_kernel(con
                 ptx::tmem_wait_ld();
                 ptx::reg_fence(v[0]);
                 if constexpr (kPer == 64) ptx::reg_fence(v[1]);
+                // the other pieces' partials, in piece order (k order) after this one
+                for (uint32_t i = 1; Cfg::kSplit && i < p.pieces; ++i) {
+                    // (plain loads, so that the compiler issues them together)
+                    const float4* src = reinterpret_cast<const float4*>(
+                        smem_raw + (scr - raw) + (i - 1) * uint32_t(Cfg::kPartialBytes)) + lane;
+#pragma unroll
+                    for (int h = 0; h < kPer / 32; ++h)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float4 t = src[(c0 / 4 + h * 8 + e) * 32];
+                            v[h][4 * e] = __float_as_uint(__uint_as_float(v[h][4 * e]) + t.x);
+                            v[h][4 * e + 1] = __float_as_uint(__uint_as_float(v[h][4 * e + 1]) + t.y);
+                            v[h][4 * e + 2] = __float_as_uint(__uint_as_float(v[h][4 * e + 2]) + t.z);
+                            v[h][4 * e + 3] = __float_as_uint(__uint_as_float(v[h][4 * e + 3]) + t.w);
+                        }
+                }
 #pragma unroll
                 for (int h = 0; h < kPer / 32; ++h) {
                     uint32_t q[16];

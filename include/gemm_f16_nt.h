@@ -26,9 +26,14 @@
  * and split pieces) computes every problem whose 128-row tiles would not fit
  * on the SMs in one wave.  The small-problem kernel computes one 128×tile_n
  * tile (tile_n = 32, 64 or 128, the narrowest whose tiles fit on the SMs at
- * once) per CTA with all of k, for problems with K <= 8192 whose tiles do fit:
- * there the persistent kernel's 256×256 tiles would leave most SMs idle and
- * its fixed costs dominate.  The automatic choice applies when no persistent-
+ * once) per CTA, for problems whose tiles do fit: there the persistent
+ * kernel's 256×256 tiles would leave most SMs idle and its fixed costs
+ * dominate.  With few tiles and k of at least 2048 (32 k-blocks) it cuts each
+ * tile along k into up to 8 pieces on their own CTAs (split-K, at least 8
+ * k-blocks a piece, all in one wave); the first piece owns the tile and adds
+ * the others' fp32 partials, which they pass through the workspace, in k
+ * order, so results do not depend on timing.  It takes problems with at most
+ * 128 k-blocks a piece.  The automatic choice applies when no persistent-
  * kernel option is given (see gemm_f16_nt_ex); gemm_f16_nt_launch_plan reports
  * which kernel a call gets (plan field `kernel`).  Both give results within the
  * same bound; only the order of the fp32 additions can differ between them.
@@ -229,9 +234,11 @@ gemm_status_t gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K,
  *                 cluster, no trace; GEMM_ERR_INVALID_VALUE otherwise).
  *                 The automatic plan (schedule 0 with cta_group, swizzle,
  *                 max_clusters and tile_n 0, cluster_pairs at most 1) takes the
- *                 small-problem kernel when those conditions hold, K is at most
- *                 8192 (128 k-blocks) and its 128×32, 128×64 or 128×128 tiles
- *                 fit on the device's SMs in one wave.
+ *                 small-problem kernel when those conditions hold, its 128×32,
+ *                 128×64 or 128×128 tiles fit on the device's SMs in one wave
+ *                 and each CTA's k range (after its split-K, if any) is at
+ *                 most 128 k-blocks.  Its split-K, like stream-K, needs a
+ *                 workspace slot and is off under stream capture.
  *                 N-split: when the stream-K rule does not split the problem
  *                 and either there are fewer tiles than clusters or k is
  *                 shallow (at most 32 k-blocks), the R tiles of the last wave
@@ -433,12 +440,16 @@ typedef struct {
                               split is not taken: 1 the stream is capturing, 2 no workspace
                               was reserved on the device */
     int32_t split_pieces;  /* > 1: every tile is cut along k into split_pieces equal pieces,
-                              one per cluster, which reduce each other's fp32 partials
-                              (clusters = num_tiles · split_pieces); 1 = not used */
+                              one per cluster (clusters = num_tiles · split_pieces);
+                              the persistent kernel's pieces reduce each other's fp32
+                              partials, the small-problem kernel's first piece adds
+                              the others'; 1 = not used */
     int32_t kernel;        /* 0: the persistent kernel; 1: the small-problem kernel: one
-                              tile_m × tile_n tile per cluster (CTA or CTA pair), all
-                              of k, clusters = num_tiles, tile c at m_tile =
-                              c % m_tiles, n_tile = c / m_tiles; no workspace */
+                              tile_m × tile_n tile per cluster (CTA or CTA pair), or
+                              with split_pieces = s > 1 one of s k-pieces of it:
+                              clusters = num_tiles · s, cluster c on piece c % s of
+                              tile t = c / s at m_tile = t % m_tiles, n_tile =
+                              t / m_tiles; piece 0 owns the tile (schedule kind 2) */
 } gemm_f16_nt_plan_t;
 
 gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms,

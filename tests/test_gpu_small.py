@@ -6,7 +6,8 @@ ragged edges in M, N and K, k deep enough for the stage ring to wrap several
 times, and padded pitches whose padding holds NaN (a read of it would poison
 the result); C's padding columns and a row past M must come back untouched.
 Chosen by default for small problems (checked through the launch plan), also
-under stream capture, where it needs no workspace.  Bars as everywhere:
+under stream capture, where it needs no workspace; with few tiles and deep k
+it splits each tile along k (split-K, owner adds the pieces in k order).  Bars as everywhere:
 small-integer inputs bit-exact, others within 2 ulps of the output format +
 1e-4·sqrt(K).
 """
@@ -184,3 +185,81 @@ def test_small_kernel_captured_and_replayed_with_new_inputs():
         graph.replay()
         torch.cuda.synchronize()
         check_bitexact(Cs.cpu().numpy(), oracle.gemm_f16_nt(A, B), f"replay {rep + 1}")
+
+
+@pytest.mark.parametrize("M,N,K,s,ints", [
+    (256, 256, 4096, 8, False),     # 16 tiles x 8 pieces of 8 k-blocks
+    (256, 256, 4096, 8, True),      # integers: bit-exact, whatever the order of the pieces
+    (300, 200, 3000, 4, False),     # 21 ragged tiles x 4 pieces of 11-12 k-blocks
+    (512, 512, 8192, 2, False),     # 64 tiles x 2 pieces
+    (100, 60, 2000, 4, True),       # 2 tiles of 32 k-blocks: 4 pieces of 8 (8 would leave 4)
+])
+def test_split_k_small_kernel_matches_oracle(M, N, K, s, ints):
+    pl = g.launch_plan(M, N, K)
+    assert (pl["kernel"], pl["split_pieces"]) == (1, s) and pl["workspace_bytes"] > 0
+    A, B, ref = _reference(M, N, K, ints)
+    got = _run(A.view(np.uint16), B.view(np.uint16), None)
+    if ints:
+        check_bitexact(got.view(np.float16), ref, f"split-K {M}x{N}x{K}")
+    else:
+        check_close(got.view(np.float16), ref, K, f"split-K {M}x{N}x{K}")
+    # the owner adds the pieces in k order: the same bits on every call
+    assert np.array_equal(got, _run(A.view(np.uint16), B.view(np.uint16), None))
+
+
+@pytest.mark.parametrize("cg,bn", [(2, 64), (1, 128), (2, 32)])
+def test_split_k_forced_variants_and_bf16(cg, bn):
+    M, N, K = 300, 200, 3000
+    o = g.Options(schedule=5, cta_group=cg, tile_n=bn)
+    pl = g.plan(M, N, K, options=o)
+    assert pl["split_pieces"] > 1
+    A, B, ref = _reference(M, N, K, False)
+    check_close(_run(A.view(np.uint16), B.view(np.uint16), o).view(np.float16), ref, K, f"split-K {cg}x{bn}")
+    Ab = inputs.draw_bf16((M, K), inputs.U, 4401)
+    Bb = inputs.draw_bf16((N, K), inputs.U, 4402)
+    got = _run(Ab, Bb, o, bf16=True)
+    check_close(bf16_to_f64(got), bf16_to_f64(oracle.gemm_bf16_nt(Ab, Bb)), K, "split-K bf16", ulp=ulp_bf16)
+
+
+def test_split_k_small_kernel_under_capture_runs_unsplit():
+    """Under stream capture the split is off (its flags are tagged per launch,
+    and a replay repeats the launch): one piece a tile, still the oracle's result."""
+    M, N, K = 256, 256, 4096
+    assert g.launch_plan(M, N, K)["split_pieces"] == 8
+    As = torch.empty((M, K), dtype=torch.float16, device="cuda")
+    Bs = torch.empty((N, K), dtype=torch.float16, device="cuda")
+    Cs = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    g.gemm_f16_nt(As, Bs, Cs)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=s):
+        pl = g.launch_plan(M, N, K, stream=s)
+        g.gemm_f16_nt(As, Bs, Cs, stream=s)
+    assert (pl["kernel"], pl["split_pieces"], pl["split_k_off"], pl["workspace_bytes"]) == (1, 1, 1, 0)
+    A, B = _operands(M, N, K, True)
+    As.copy_(torch.from_numpy(A))
+    Bs.copy_(torch.from_numpy(B))
+    torch.cuda.synchronize()
+    for _ in range(2):
+        Cs.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        check_bitexact(Cs.cpu().numpy(), oracle.gemm_f16_nt(A, B), "captured split-K shape")
+
+
+def test_stalled_split_k_small_kernel_reports_timeout():
+    M, N, K = 256, 256, 4096
+    A, B, ref = _reference(M, N, K, False)
+    Ad, Bd = to_device(A), to_device(B)
+    C, _ = empty_out(M, N)
+    g.gemm_f16_nt(Ad, Bd, C, options=g.Options(schedule=5, inject_stall=1, timeout_ns=20_000_000))
+    word = g.device_status()
+    assert word & 1, f"watchdog word {word:#x}"
+    sites = {s for s in range(1, 8) if word & (1 << (7 + s))}
+    assert sites and sites <= {2, 4, 7}, f"unexpected wait sites in {word:#x}"
+    assert np.isnan(to_host(C).astype(np.float32)).all(), "C was written by a stalled kernel"
+    g.gemm_f16_nt(Ad, Bd, C)
+    torch.cuda.synchronize()
+    assert g.device_status() == 0
+    check_close(to_host(C), ref, K, "after the stall")

@@ -358,8 +358,20 @@ def test_plan_small_kernel():
         assert (p["sk_tiles"], p["split_pieces"], p["tail_split"], p["workspace_bytes"]) == (0, 1, 1, 0)
         assert p["k_blocks"] == -(-K // 64) and p["smem_bytes"] <= 232448
         assert p["tmem_cols"] == max(32, bn)
-    # more than one wave, or k deeper than 128 k-blocks: the persistent kernel
-    for M, N, K in ((2048, 2048, 2048), (4096, 1024, 1024), (8192, 8192, 8192), (256, 256, 8256), (256, 256, 1 << 16)):
+    # few tiles and deep k: split-K, s pieces a tile (s <= 8, a power of two, all
+    # pieces in one wave, >= 8 k-blocks a piece); piece 0 owns the tile
+    for (M, N, K), (bn, tiles, s) in {(256, 256, 4096): (32, 16, 8), (256, 256, 1 << 16): (32, 16, 8),
+                                      (512, 512, 8192): (32, 64, 2), (300, 200, 3000): (32, 21, 4),
+                                      (256, 256, 1024): (32, 16, 1), (256, 256, 2048): (32, 16, 4), (100, 100, 600): (32, 4, 1)}.items():
+        p = g.plan(M, N, K, num_sms=152)
+        assert (p["kernel"], p["tile_n"], p["num_tiles"], p["split_pieces"]) == (1, bn, tiles, s), (M, N, K)
+        assert (p["clusters"], p["grid_ctas"], p["sk_tiles"], p["tail_split"]) == (tiles * s, tiles * s, 0, 1)
+        # the workspace: per-warp flags (256-byte aligned), then one fp32 128 x bn partial per CTA
+        flags = -(-tiles * s * 4 * 8 // 256) * 256
+        assert p["workspace_bytes"] == (flags + tiles * s * 128 * bn * 4 if s > 1 else 0)
+    # more than one wave, or more than 128 k-blocks a piece: the persistent kernel
+    for M, N, K in ((2048, 2048, 2048), (4096, 1024, 1024), (8192, 8192, 8192), (256, 256, 1 << 17),
+                    (1024, 1024, 8256)):
         assert g.plan(M, N, K, num_sms=152)["kernel"] == 0, (M, N, K)
     # the wave is counted on the given SM count
     assert g.plan(1024, 1024, 1024, num_sms=100)["tile_n"] == 128

@@ -53,7 +53,9 @@ CASES = [
     (256, 512, 1 << 20, {}, 76),
     (1024, 1024, 8192, {"cta_group": 2}, 76),         # split pieces: 16 tiles x 4
     (256, 256, 8192, {"cta_group": 2}, 76),           # one tile in 8 pieces
-    (256, 256, 16384, {}, 76),                        # deeper than the small kernel takes: 8 pieces
+    (256, 256, 16384, {}, 76),                        # small-problem kernel, split-K: 16 tiles x 8 pieces
+    (300, 200, 3000, {}, 76),                         # small-problem kernel, split-K: 21 tiles x 4 pieces
+    (256, 256, 1 << 17, {}, 76),                      # too deep a piece: persistent split pieces
     (300, 520, 328, {"schedule": 4}, 76),             # forced: pieces of 1 or 2 k-blocks
     (700, 900, 1000, {"cta_group": 1, "schedule": 4}, 152),
 ]
@@ -100,7 +102,8 @@ def check_coverage(pl, items):
     for c, its in enumerate(items):
         for it in its:
             assert it["parts"] in (1, pl["tail_split"]), it
-            assert (it["kind"] == SPLIT) == (pl["split_pieces"] > 1), it
+            # (the persistent kernel's split pieces; the small kernel's split-K uses owners)
+            assert (it["kind"] == SPLIT) == (pl["split_pieces"] > 1 and pl["kernel"] == 0), it
             if it["parts"] > 1:
                 sliced += 1
                 assert it["tile"] >= pl["num_tiles"] - pl["tail_tiles"], it
@@ -132,17 +135,20 @@ def check_split_pieces(pl, items):
 def check_partials_and_owners(pl, items):
     """One partial piece per cluster at most, as its first item; owners add exactly
     the partial pieces of their tile, held by the next clusters, contiguous in k."""
-    if pl["split_pieces"] > 1:
+    if pl["split_pieces"] > 1 and pl["kernel"] == 0:
         check_split_pieces(pl, items)
         return
     kb = pl["k_blocks"]
+    # tiles that may be split in k: the stream-K tiles, or (small-problem kernel
+    # with split-K) every tile
+    split_tiles = pl["num_tiles"] if pl["kernel"] == 1 and pl["split_pieces"] > 1 else pl["sk_tiles"]
     partial_of = {}                                   # tile -> [(cluster, kb0, kb1)]
     for c, its in enumerate(items):
         partials = [i for i, it in enumerate(its) if it["kind"] == PARTIAL]
         assert partials in ([], [0]), (c, its)        # one workspace slot per cluster
         for it in its:
             if it["kind"] != WHOLE:
-                assert it["parts"] == 1 and it["tile"] < pl["sk_tiles"]
+                assert it["parts"] == 1 and it["tile"] < split_tiles
             if it["kind"] == PARTIAL:
                 assert 0 < it["kb0"] < it["kb1"] <= kb     # a middle piece ends inside the tile
                 partial_of.setdefault(it["tile"], []).append((c, it["kb0"], it["kb1"]))
@@ -161,7 +167,7 @@ def check_partials_and_owners(pl, items):
             edges = [it["kb1"]] + [p[2] for p in parts]
             assert [p[1] for p in parts] == edges[:-1] and edges[-1] == kb   # k order, no gap
     assert not partial_of                              # every partial piece has an owner
-    if pl["sk_tiles"] == 0:
+    if split_tiles == 0:
         assert owners == 0
 
 
@@ -181,17 +187,26 @@ def check_balance_and_coordinates(pl, items, tile_coord=g.tile_coord):
 
 
 def check_small(pl, items):
-    """The small-problem kernel: one whole-k tile per cluster, cluster c on tile c,
-    as many clusters as tiles of 128·cta_group × tile_n."""
+    """The small-problem kernel: one item per cluster; with s = split_pieces
+    pieces a tile, cluster c runs piece c % s of tile c // s over an equal share
+    of the k-blocks, piece 0 owning the tile (adding the s - 1 clusters after it)
+    and the others writing partials; without split-K every cluster is one whole
+    tile."""
     if pl["kernel"] != 1:
         return
-    assert pl["clusters"] == pl["num_tiles"] and pl["grid_ctas"] == pl["num_tiles"] * pl["cta_group"]
+    s, kb = pl["split_pieces"], pl["k_blocks"]
+    assert pl["clusters"] == pl["num_tiles"] * s and pl["grid_ctas"] == pl["clusters"] * pl["cta_group"]
     assert pl["tile_m"] == 128 * pl["cta_group"] and pl["tile_n"] in (32, 64, 128)
-    assert (pl["sk_tiles"], pl["tail_split"], pl["split_pieces"], pl["workspace_bytes"]) == (0, 1, 1, 0)
+    assert (pl["sk_tiles"], pl["tail_split"]) == (0, 1) and (pl["workspace_bytes"] > 0) == (s > 1)
+    assert s in (1, 2, 4, 8) and (s == 1 or kb // s >= 8)
     for c, its in enumerate(items):
         assert len(its) == 1
         it = its[0]
-        assert (it["tile"], it["kb0"], it["kb1"], it["kind"], it["parts"]) == (c, 0, pl["k_blocks"], WHOLE, 1)
+        t, pc = c // s, c % s
+        kind = WHOLE if s == 1 else (OWNER if pc == 0 else PARTIAL)
+        partners = s - 1 if s > 1 and pc == 0 else 0
+        assert (it["tile"], it["kb0"], it["kb1"], it["kind"], it["parts"], it["partners"]) == \
+            (t, kb * pc // s, kb * (pc + 1) // s, kind, 1, partners)
 
 
 def check_schedule(pl, items, tile_coord=g.tile_coord):

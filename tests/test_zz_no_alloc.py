@@ -37,6 +37,7 @@ def _call(fn, A, B, C, stream):
     (1024, 1024, 12288, True, False),    # 16 pair tiles, each in 4 split pieces over 64 pairs
     (6144, 4096, 4096, True, False),     # 384 tiles: last wave 4/76 full, deep k: stream-K part
     (1024, 1024, 12288, True, True),     # integers: exact, whatever the summation order
+    (256, 256, 4096, True, True),        # the small-problem kernel's split-K: 16 tiles x 8 pieces
     (300, 520, 328, False, False),       # the small-problem kernel: no scratch needed
     (1024, 1024, 1024, False, True),     # the same, 128 tiles of 128 x 64, integers
 ])
