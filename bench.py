@@ -18,9 +18,13 @@ clocks seen during the timed region, and the CPU oracle timed on a bounded
 sample of the same workload.  Beside the headline, on rank 0: every other
 workload (256³, 4096³, the ragged shape with float and integer inputs, the MLP
 shape) timed the same way through the C ABI, each with cuBLAS beside it and its
-own clock record ("workloads"), and a sustained window of back-to-back 8192³
-launches lasting seconds, long enough for the board's power cap to set the
-clock ("sustained").
+own clock record ("workloads"); three small, latency-bound shapes (1024³,
+512×4096×4096, 256×256×4096) the same way ("small_shapes"); and a sustained
+window of back-to-back 8192³ launches lasting seconds, long enough for the
+board's power cap to set the clock ("sustained").  Workloads whose operands
+fit in L2 are timed with a flush before each launch; they also report the GPU
+time a launch adds after a flush (a difference of long event-timed regions,
+free of the per-launch events' resolution).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -52,13 +56,17 @@ from dense_fp16_gemm_gb300 import inputs  # noqa: E402
 
 METRIC = "fp16 NT GEMM TFLOP/s and % of GB300 dense fp16 tensor peak"
 UNIT = "TFLOP/s"
+# The persistent kernel's sources (the traffic records are of that kernel;
+# small_tile.cuh holds the small-problem kernel only)
 KERNEL_SOURCES = ["dense_fp16_gemm_gb300/csrc/gemm_f16_nt.cu", "dense_fp16_gemm_gb300/csrc/ptx.cuh",
-                  "dense_fp16_gemm_gb300/csrc/sched.cuh", "dense_fp16_gemm_gb300/csrc/small_tile.cuh"]
+                  "dense_fp16_gemm_gb300/csrc/sched.cuh"]
 # DRAM bytes per launch from an Nsight Compute capture, written by
 # `bench.py --record-traffic`; used only while the kernel sources hash the same
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 SIDE_WORKLOADS = ["gemm_256", "gemm_4096", "ragged_4000x3000x5000", "ragged_int_4000x3000x5000",
                   "mlp_up_16384x14336x4096"]
+# small, latency-bound shapes beside the configs (the small-problem kernel's range)
+SMALL_SHAPES = ["gemm_1024", "gemm_512x4096x4096", "gemm_256x256x4096"]
 FALLBACK_PEAK_TFLOPS = 1900.0   # one earlier GB300 bf16 burst measurement
 L2_BYTES = 129 * 10**6
 SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -462,6 +470,31 @@ def time_steps(step, steps: int, stream, flush=None, sampler=None):
     return ms, (w0, time.time())
 
 
+def time_added_after_flush(step, stream, flush, n: int = 200, reps: int = 3) -> float:
+    """The GPU time one launch adds after an L2 flush, in ms: n x (flush, launch)
+    timed with CUDA events around the whole loop, less n flushes alone; the
+    median of `reps` repeats.  At a few microseconds a launch the per-launch
+    events of time_steps move in steps of the event timer's resolution
+    (about 2 us on GB300); this difference of long regions does not."""
+    import torch
+
+    def region(with_step: bool) -> float:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for i in range(n):
+            flush.fill_(i & 255)
+            if with_step:
+                step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    region(False)
+    vals = sorted(region(True) - region(False) for _ in range(reps))
+    return vals[len(vals) // 2]
+
+
 def cublas_step(A_d, B_d, out):
     import torch
 
@@ -519,6 +552,7 @@ def measure_workload(lib, name: str, device, stream, steps: int, warmup: int, co
     if flushed and w.flops < 1e9:   # a few microseconds a launch: more samples for the median
         steps = max(steps, 200)
     ms, win = time_steps(step, steps, stream, flush, sampler)
+    add = time_added_after_flush(step, stream, flush) if flushed and w.flops < 1e11 else None
     if g.device_status(stream) != 0:
         raise SystemExit(f"bench.py: {name}: watchdog word set during the timed region")
     out = torch.empty_like(Cd)
@@ -528,6 +562,7 @@ def measure_workload(lib, name: str, device, stream, steps: int, warmup: int, co
             cb()
         time.sleep(cooldown)
         ms_cb, win_cb = time_steps(cb, steps, stream, flush, sampler)
+        add_cb = time_added_after_flush(cb, stream, flush) if add is not None else None
     pl = g.launch_plan(w.M, w.N, w.K, stream=stream, lib=lib)
     peak, peak_sus = peaks
     tf = w.flops / (ms * 1e-3) / 1e12
@@ -538,8 +573,14 @@ def measure_workload(lib, name: str, device, stream, steps: int, warmup: int, co
            "frac_of_sustained_peak": round(tf / peak_sus, 4) if peak_sus else None,
            "l2": "flushed between launches (per-launch events)" if flushed
                  else "operands larger than L2, launches back to back",
-           "plan": {k: pl[k] for k in ("cluster_pairs", "clusters", "num_tiles", "sk_tiles", "tail_split")},
+           "plan": {k: pl[k] for k in ("kernel", "cta_group", "tile_n", "cluster_pairs", "clusters", "num_tiles",
+                                       "sk_tiles", "tail_split", "split_pieces")},
            "cublas_tflops": round(tf_cb, 2), "ours_over_cublas": round(tf / tf_cb, 4)}
+    if add is not None:
+        # what a launch adds to the GPU's time after a flush (launch latency overlapped)
+        rec["us_added_after_flush"] = round(add * 1e3, 2)
+        rec["cublas_us_added_after_flush"] = round(add_cb * 1e3, 2)
+        rec["ours_over_cublas_added_after_flush"] = round(add_cb / add, 4)
     del Ad, Bd, Cd, out, flush
     torch.cuda.empty_cache()
     return rec, win, win_cb
@@ -568,7 +609,8 @@ def fresh_process_headlines(args):
     cmd = [sys.executable, os.path.abspath(__file__), "--steps", str(args.steps), "--warmup", str(args.warmup),
            "--no-workloads", "--sustained-seconds", "0", "--no-cpu-baseline", "--no-cublas",
            "--cooldown", str(args.cooldown), "--cooldown-first", "--fresh-processes", "0",
-           "--workload", args.workload, "--dtype", args.dtype, "--accumulate", args.accumulate]
+           "--workload", args.workload, "--dtype", args.dtype, "--accumulate", args.accumulate,
+           "--kernel", args.kernel]
     if args.shape:
         cmd += ["--shape", args.shape]
     if args.ld:
@@ -690,11 +732,20 @@ def run_ours(args, w):
     else:
         lib = g.library()
     acc16 = args.accumulate == "f16"
-    if acc16:   # the fp16-accumulation variant, through the options entry point
-        acc_opts = g.Options(accumulate=1)
+    # options: the fp16-accumulation variant, or a kernel asked for by name
+    kopts = {}
+    if acc16:
+        kopts["accumulate"] = 1
+    if args.kernel == "persistent":
+        kopts["cta_group"] = 2
+    elif args.kernel == "small":
+        kopts["schedule"] = 5
+    popts = g.Options(**kopts)
+    if kopts:
+        entry_ex = lib.gemm_bf16_nt_ex if bf16 else lib.gemm_f16_nt_ex
 
         def entry(*a):
-            return lib.gemm_f16_nt_ex(*a, ctypes.byref(acc_opts))
+            return entry_ex(*a, ctypes.byref(popts))
     else:
         entry = lib.gemm_bf16_nt if bf16 else lib.gemm_f16_nt
 
@@ -787,7 +838,7 @@ def run_ours(args, w):
     peaks = (peak, peak_sustained)
     windows = {}
     extras = rank == 0 and world == 1 and w.name == "gemm_8192" and not bf16 and not acc16 \
-        and args.library == "default"
+        and args.library == "default" and args.kernel == "auto"
     # Every other workload, timed the same way through the C ABI, each with
     # cuBLAS beside it and its own clock record.
     side = {}
@@ -796,6 +847,13 @@ def run_ours(args, w):
             rec, win, win_cb = measure_workload(lib, name, device, stream, args.workload_steps, args.warmup,
                                                 args.cooldown, peaks, sampler)
             side[name] = rec
+            windows[name] = (win, win_cb)
+    small = {}
+    if extras and not args.no_workloads:
+        for name in SMALL_SHAPES:
+            rec, win, win_cb = measure_workload(lib, name, device, stream, args.workload_steps, args.warmup,
+                                                args.cooldown, peaks, sampler)
+            small[name] = rec
             windows[name] = (win, win_cb)
     # A sustained window: seconds of back-to-back launches at the headline
     # shape, long enough for the board's power limit to settle the clock.
@@ -816,7 +874,7 @@ def run_ours(args, w):
     if sampler:
         sampler.stop()
         clocks = sampler.summary(head_windows)
-        for name, rec in side.items():
+        for name, rec in list(side.items()) + list(small.items()):
             rec["clocks"] = sampler.summary([windows[name][0]])
             rec["cublas_clocks"] = sampler.summary([windows[name][1]])
         if sustained is not None:
@@ -835,13 +893,18 @@ def run_ours(args, w):
 
     if rank == 0:
         traffic, traffic_rec = recorded_traffic(w.name) if not bf16 and not acc16 else (None, None)
-        popts = g.Options(accumulate=1 if acc16 else 0)
         pl = g.launch_plan(w.M, w.N, w.K, stream=stream, options=popts, lib=lib)
-        kernel_desc = (f"gemm_f16_nt_kernel<KCfg<{pl['cta_group']},256,{pl['stages']},{pl['cluster_pairs']},"
-                       f"{int(bf16)},{int(acc16)}>>: "
-                       f"{pl['clusters']} clusters x {pl['grid_ctas'] // pl['clusters']} CTAs, "
-                       f"{pl['tile_m']}x{pl['tile_n']} cluster tiles, {pl['sk_tiles']} of {pl['num_tiles']} "
-                       f"split in k")
+        if pl["kernel"] == 1:
+            kernel_desc = (f"gemm_f16_nt_small_kernel<SCfg<{pl['cta_group']},{pl['tile_n']},{pl['stages']},"
+                           f"{int(bf16)},{int(pl['split_pieces'] > 1)}>>: {pl['clusters']} clusters x "
+                           f"{pl['cta_group']} CTAs, {pl['tile_m']}x{pl['tile_n']} tiles, "
+                           f"{pl['split_pieces']} k-piece(s) a tile")
+        else:
+            kernel_desc = (f"gemm_f16_nt_kernel<KCfg<{pl['cta_group']},256,{pl['stages']},{pl['cluster_pairs']},"
+                           f"{int(bf16)},{int(acc16)}>>: "
+                           f"{pl['clusters']} clusters x {pl['grid_ctas'] // pl['clusters']} CTAs, "
+                           f"{pl['tile_m']}x{pl['tile_n']} cluster tiles, {pl['sk_tiles']} of {pl['num_tiles']} "
+                           f"split in k")
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
@@ -874,6 +937,7 @@ def run_ours(args, w):
             "sustained": sustained,
             "fresh_processes": fresh,
             "workloads": side or None,
+            "small_shapes": small or None,
             "cpu_baseline": cpu,
             "context": context,
         }
@@ -963,6 +1027,9 @@ def main(argv=None):
                     help="timed launches per other workload (the pages time 30 iterations)")
     ap.add_argument("--sustained-seconds", type=float, default=2.5,
                     help="length of the sustained back-to-back window at 8192^3 (0: skip)")
+    ap.add_argument("--kernel", choices=["auto", "persistent", "small"], default="auto",
+                    help="auto: the library's own choice; persistent: the persistent kernel (cta_group 2); "
+                         "small: the small-problem kernel (schedule 5)")
     ap.add_argument("--library", choices=["default", "mcast"], default="default",
                     help="mcast: the single-GPU multicast build (refused with --gpus > 1)")
     ap.add_argument("--record-command", default="",

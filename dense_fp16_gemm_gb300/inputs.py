@@ -55,6 +55,11 @@ WORKLOADS = {
                                           I2, I2, 9, 10),
     "mlp_up_16384x14336x4096": Workload("mlp_up_16384x14336x4096", 16384, 14336, 4096,
                                         ("normal", 0.0, 1.0), ("normal", 0.0, 0.02), 11, 12),
+    # small, latency-bound shapes beside the configs: square, short-and-wide,
+    # and few tiles with deep k
+    "gemm_1024": Workload("gemm_1024", 1024, 1024, 1024, U, U, 13, 14),
+    "gemm_512x4096x4096": Workload("gemm_512x4096x4096", 512, 4096, 4096, U, U, 15, 16),
+    "gemm_256x256x4096": Workload("gemm_256x256x4096", 256, 256, 4096, U, U, 17, 18),
 }
 
 
