@@ -126,6 +126,33 @@ __global__ void __launch_bounds__(kSmallThreads, 1) gemm_f16_nt_small_kernel(con
     const uint32_t acc_full = ptx::smem_u32(&ctl->acc_full);
     const uint32_t mma_done = ptx::smem_u32(&ctl->mma_done);
 
+    // this cluster's tile and k-block range [kb0, kb1) (all of k without split-K)
+    const uint32_t tile = Cfg::kSplit ? cluster / p.pieces : cluster;
+    const uint32_t piece = Cfg::kSplit ? cluster - tile * p.pieces : 0u;
+    const uint32_t kb0 = Cfg::kSplit ? p.num_kb * piece / p.pieces : 0u;
+    const uint32_t kb1 = Cfg::kSplit ? p.num_kb * (piece + 1) / p.pieces : p.num_kb;
+    const uint32_t nkb = kb1 - kb0;
+    const uint32_t mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+    const int32_t m0 = int32_t(mt * Cfg::kTileM + prank * kBlockM);   // this CTA's first row
+    const int32_t n0 = int32_t(nt * BN);                               // the tile's first column
+    const int32_t b0 = n0 + int32_t(prank) * Cfg::kBRows;              // this CTA's first B row
+
+    // The producer's k-block loads: stage s of the ring, k-block kb0 + i.
+    auto load_stage = [&](uint32_t s, uint32_t i) {
+        const uint32_t full_tgt = CG == 2 ? ptx::mapa(full0, 0) : full0;
+        if (prank == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * s, uint32_t(Cfg::kTxBytes));
+        const int32_t k0 = int32_t((kb0 + i) * kBlockK);
+        const uint32_t bar = full_tgt + 8 * s;
+        if constexpr (CG == 2) {
+            ptx::tma_load_2d_pair(sA + s * Cfg::kABytes, &p.tmA, k0, m0, bar);
+            ptx::tma_load_2d_pair(sB + s * Cfg::kBBytes, &p.tmB, k0, b0, bar);
+        } else {
+            ptx::tma_load_2d(sA + s * Cfg::kABytes, &p.tmA, k0, m0, bar);
+            ptx::tma_load_2d(sB + s * Cfg::kBBytes, &p.tmB, k0, b0, bar);
+        }
+    };
+
+    uint32_t pre = 0;   // k-blocks the producer issued before the CTA-wide sync
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(full0 + 8 * s, 1);    // the first CTA's expect-tx arrive
@@ -136,8 +163,20 @@ __global__ void __launch_bounds__(kSmallThreads, 1) gemm_f16_nt_small_kernel(con
         for (int q = 0; q < 4; ++q) ptx::mbar_init(ptx::smem_u32(&ctl->xfer[q]), 1);
         ctl->abort_flag = 0u;
         ptx::fence_mbarrier_init();
+        // One CTA: the barriers are this thread's own, so it fills the empty
+        // ring at once (after the previous kernel on the stream has completed),
+        // while the others allocate tensor memory and meet at the sync.  A pair's
+        // loads complete on the first CTA's barriers, which the cluster sync
+        // must show to the other CTA first.
+        if constexpr (CG == 1) {
+            if (!p.inject_stall) {
+                ptx::griddep_wait();
+                pre = nkb < uint32_t(S) ? nkb : uint32_t(S);
+                for (uint32_t i = 0; i < pre; ++i) load_stage(i, i);
+            }
+        }
     }
-    if (warp == 0 && lane == 0) {
+    if (warp == 0 && lane == 0 && pre == 0) {
         ptx::prefetch_tensormap(&p.tmA);
         ptx::prefetch_tensormap(&p.tmB);
     }
@@ -165,40 +204,19 @@ __global__ void __launch_bounds__(kSmallThreads, 1) gemm_f16_nt_small_kernel(con
     Watch wi = w;   // waits that can span the whole main loop
     wi.limit_ns = p.item_timeout_ns;
 
-    // this cluster's tile and k-block range [kb0, kb1) (all of k without split-K)
-    const uint32_t tile = Cfg::kSplit ? cluster / p.pieces : cluster;
-    const uint32_t piece = Cfg::kSplit ? cluster - tile * p.pieces : 0u;
-    const uint32_t kb0 = Cfg::kSplit ? p.num_kb * piece / p.pieces : 0u;
-    const uint32_t kb1 = Cfg::kSplit ? p.num_kb * (piece + 1) / p.pieces : p.num_kb;
-    const uint32_t nkb = kb1 - kb0;
-    const uint32_t mt = tile % p.m_tiles, nt = tile / p.m_tiles;
-    const int32_t m0 = int32_t(mt * Cfg::kTileM + prank * kBlockM);   // this CTA's first row
-    const int32_t n0 = int32_t(nt * BN);                               // the tile's first column
-
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && !p.inject_stall) {
-            const uint32_t full_tgt = CG == 2 ? ptx::mapa(full0, 0) : full0;
-            const int32_t b0 = n0 + int32_t(prank) * Cfg::kBRows;
-            uint32_t issued = 0;
+            uint32_t issued = pre;
             bool ok = true;
-            for (uint32_t i = 0; i < nkb; ++i) {
+            for (uint32_t i = pre; i < nkb; ++i) {
                 const uint32_t s = i % uint32_t(S), ph = (i / uint32_t(S)) & 1u;
                 // (a fresh barrier's phase of parity 1 counts as complete: no wait on the first pass)
                 if (!wait(empty0 + 8 * s, ph ^ 1u, wi, kSiteProducerEmpty)) {
                     ok = false;
                     break;
                 }
-                if (prank == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * s, uint32_t(Cfg::kTxBytes));
-                const int32_t k0 = int32_t((kb0 + i) * kBlockK);
-                const uint32_t bar = full_tgt + 8 * s;
-                if constexpr (CG == 2) {
-                    ptx::tma_load_2d_pair(sA + s * Cfg::kABytes, &p.tmA, k0, m0, bar);
-                    ptx::tma_load_2d_pair(sB + s * Cfg::kBBytes, &p.tmB, k0, b0, bar);
-                } else {
-                    ptx::tma_load_2d(sA + s * Cfg::kABytes, &p.tmA, k0, m0, bar);
-                    ptx::tma_load_2d(sB + s * Cfg::kBBytes, &p.tmB, k0, b0, bar);
-                }
+                load_stage(s, i);
                 ++issued;
             }
             if (!ok && issued) {
