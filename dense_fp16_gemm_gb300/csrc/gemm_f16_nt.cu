@@ -933,13 +933,17 @@ using Cfg1Bf = KCfg<1, 256, 4, 1, true>;
 using Cfg2A16 = KCfg<2, 256, 6, 1, false, true>;   // the fp16 ones with an fp16 accumulator
 using Cfg1A16 = KCfg<1, 256, 4, 1, false, true>;
 // The small-problem kernel's tiles: 128·CG × BN, one per cluster (each also
-// built for bf16 and for split-K: SCfg's last two parameters).
-using S1n32 = SCfg<1, 32, 8>;
-using S1n64 = SCfg<1, 64, 8>;
-using S1n128 = SCfg<1, 128, 6>;
-using S2n32 = SCfg<2, 32, 8>;
-using S2n64 = SCfg<2, 64, 8>;
-using S2n128 = SCfg<2, 128, 8>;
+// built for bf16 and for split-K: SCfg's last two parameters), with as many
+// ring stages as fit in a CTA's shared memory: the main loop streams the
+// operands at what one SM ingests with the ring's bytes in flight (measured,
+// µs added after an L2 flush: 1024³ 4.8 with 9 stages against 5.2 with 8,
+// 512×4096×4096 16.7 with 7 against 18.4 with 6).
+using S1n32 = SCfg<1, 32, 11>;
+using S1n64 = SCfg<1, 64, 9>;
+using S1n128 = SCfg<1, 128, 7>;
+using S2n32 = SCfg<2, 32, 12>;
+using S2n64 = SCfg<2, 64, 11>;
+using S2n128 = SCfg<2, 128, 9>;
 #if G16_MCAST_LIB
 using Cfg2x2 = KCfg<2, 256, 6, 2>; // two CTA pairs per cluster sharing A: 256×512 cluster tile
 using Cfg2x2Bf = KCfg<2, 256, 6, 2, true>;
