@@ -24,7 +24,9 @@ window of back-to-back 8192³ launches lasting seconds, long enough for the
 board's power cap to set the clock ("sustained").  Workloads whose operands
 fit in L2 are timed with a flush before each launch; they also report the GPU
 time a launch adds after a flush (a difference of long event-timed regions,
-free of the per-launch events' resolution).
+free of the per-launch events' resolution).  Last, the timing protocol of
+the Tilus pages: the headline again in three fresh processes, each after 3 s
+of idle, and their median ("fresh_processes").
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -603,12 +605,12 @@ def measure_sustained(step, cb_step, flops: float, ms_hint: float, seconds: floa
 
 def fresh_process_headlines(args):
     """Run the headline alone in `args.fresh_processes` new processes (one after
-    another, each idling `args.cooldown` s before its timed region) and return
+    another, each idling `args.fresh_cooldown` s before its timed region) and return
     their values and median: the timing protocol the Tilus pages describe
     (median of three fresh processes, a cooldown before each measurement)."""
     cmd = [sys.executable, os.path.abspath(__file__), "--steps", str(args.steps), "--warmup", str(args.warmup),
            "--no-workloads", "--sustained-seconds", "0", "--no-cpu-baseline", "--no-cublas",
-           "--cooldown", str(args.cooldown), "--cooldown-first", "--fresh-processes", "0",
+           "--cooldown", str(args.fresh_cooldown), "--cooldown-first", "--fresh-processes", "0",
            "--workload", args.workload, "--dtype", args.dtype, "--accumulate", args.accumulate,
            "--kernel", args.kernel]
     if args.shape:
@@ -623,7 +625,7 @@ def fresh_process_headlines(args):
             raise SystemExit("bench.py: a fresh-process headline failed:\n" + out.stderr[-2000:])
         values.append(json.loads(out.stdout.strip().splitlines()[-1])["value"])
     return {"values": values, "median": statistics.median(values), "unit": UNIT,
-            "protocol": f"{len(values)} fresh processes, {args.cooldown} s idle before each timed region "
+            "protocol": f"{len(values)} fresh processes, {args.fresh_cooldown} s idle before each timed region "
                         f"of {args.steps} launches"}
 
 
@@ -881,8 +883,9 @@ def run_ours(args, w):
             sustained["clocks"] = sampler.summary([windows["sustained"][0]])
             sustained["cublas_clocks"] = sampler.summary([windows["sustained"][1]])
 
-    # The pages' protocol, on request: the headline measured again in fresh
-    # processes, each after a cooldown, and the median reported beside it.
+    # The pages' protocol (by default in the full run): the headline measured
+    # again in fresh processes, each after a cooldown, and the median reported
+    # beside it.
     fresh = None
     if rank == 0 and world == 1 and args.fresh_processes > 0:
         fresh = fresh_process_headlines(args)
@@ -1010,9 +1013,12 @@ def main(argv=None):
     ap.add_argument("--repeat", type=int, default=1,
                     help="timed regions of K steps per process (the median is reported)")
     ap.add_argument("--cooldown", type=float, default=1.0, help="seconds of idle before each repeat")
-    ap.add_argument("--fresh-processes", type=int, default=0,
-                    help="also time the headline in this many fresh processes (with --cooldown before each) "
-                         "and report their median, the pages' protocol (e.g. 3 with --cooldown 3)")
+    ap.add_argument("--fresh-processes", type=int, default=None,
+                    help="also time the headline in this many fresh processes (with --fresh-cooldown before "
+                         "each) and report their median, the pages' protocol (default 3, or 0 with "
+                         "--no-workloads; 0: off)")
+    ap.add_argument("--fresh-cooldown", type=float, default=3.0,
+                    help="seconds of idle before each fresh process's timed region")
     ap.add_argument("--cooldown-first", action="store_true",
                     help="also idle --cooldown seconds between the warm-up and the first timed region")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU oracle sample budget")
@@ -1042,6 +1048,8 @@ def main(argv=None):
         ap.error("--warmup must be at least 3")
     if args.accumulate == "f16" and args.dtype == "bf16":
         ap.error("--accumulate f16 needs fp16 operands")
+    if args.fresh_processes is None:
+        args.fresh_processes = 0 if args.no_workloads else 3
     world, _, _ = dist_env()
     if args.gpus != world and world > 1:
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
