@@ -58,9 +58,9 @@ from dense_fp16_gemm_gb300 import inputs  # noqa: E402
 
 METRIC = "fp16 NT GEMM TFLOP/s and % of GB300 dense fp16 tensor peak"
 UNIT = "TFLOP/s"
-# The persistent kernel's sources (the traffic records are of that kernel;
-# small_tile.cuh holds the small-problem kernel only)
-KERNEL_SOURCES = ["dense_fp16_gemm_gb300/csrc/gemm_f16_nt.cu", "dense_fp16_gemm_gb300/csrc/ptx.cuh",
+# The persistent kernel's device sources (the traffic records are of that
+# kernel; gemm_f16_nt.cu is host code, small_tile.cuh the small-problem kernel)
+KERNEL_SOURCES = ["dense_fp16_gemm_gb300/csrc/persistent.cuh", "dense_fp16_gemm_gb300/csrc/ptx.cuh",
                   "dense_fp16_gemm_gb300/csrc/sched.cuh"]
 # DRAM bytes per launch from an Nsight Compute capture, written by
 # `bench.py --record-traffic`; used only while the kernel sources hash the same

@@ -24,8 +24,9 @@ MCAST_LIB_NAME = "libgemm_f16_nt_mcast.so"
 MCAST_LIB_PATH = os.path.join(BUILD_DIR, MCAST_LIB_NAME)
 
 SOURCES = [os.path.join(CSRC, "gemm_f16_nt.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "sched.cuh"),
-                     os.path.join(CSRC, "small_tile.cuh"), os.path.join(INCLUDE, "gemm_f16_nt.h")]
+DEPENDS = SOURCES + [os.path.join(CSRC, "persistent.cuh"), os.path.join(CSRC, "ptx.cuh"),
+                     os.path.join(CSRC, "sched.cuh"), os.path.join(CSRC, "small_tile.cuh"),
+                     os.path.join(INCLUDE, "gemm_f16_nt.h")]
 MCAST_SOURCES = [os.path.join(CSRC, "mcast", "gemm_f16_nt_mcast.cu")]
 MCAST_DEPENDS = DEPENDS + MCAST_SOURCES + [os.path.join(CSRC, "mcast", "tma_multicast.cuh")]
 

@@ -33,6 +33,10 @@
 // sites and limits); on expiry the CTA stops, lets its copies and MMAs in
 // flight finish (bounded), frees its tensor memory and exits.
 
+#pragma once
+
+#include "persistent.cuh"   // tile constants, the watchdog and its waits, descriptors
+
 namespace g16 {
 
 constexpr int kSmallThreads = 128;   // 4 warps: producer lane, MMA lane, then all four drain
