@@ -71,7 +71,7 @@ class Plan(ctypes.Structure):
                 ("sk_tiles", ctypes.c_int32), ("cluster_pairs", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("tail_tiles", ctypes.c_int32),
                 ("tail_split", ctypes.c_int32), ("split_k_off", ctypes.c_int32),
-                ("split_pieces", ctypes.c_int32), ("kernel", ctypes.c_int32)]
+                ("split_pieces", ctypes.c_int32), ("kernel", ctypes.c_int32), ("k_order", ctypes.c_int32)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -82,7 +82,7 @@ class Item(ctypes.Structure):
     _fields_ = [("tile", ctypes.c_int32), ("m_tile", ctypes.c_int32), ("n_tile", ctypes.c_int32),
                 ("kb0", ctypes.c_int32), ("kb1", ctypes.c_int32), ("kind", ctypes.c_int32),
                 ("part", ctypes.c_int32), ("parts", ctypes.c_int32), ("partners", ctypes.c_int32),
-                ("piece", ctypes.c_int32), ("pieces", ctypes.c_int32)]
+                ("piece", ctypes.c_int32), ("pieces", ctypes.c_int32), ("k_down", ctypes.c_int32)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -174,6 +174,7 @@ struct Params {
     uint32_t tail_first;
     uint32_t tail_split;
     uint32_t split_pieces; // > 1: each cluster runs one split piece of tile cluster / split_pieces
+    uint32_t k_alternate;  // 1: whole tiles of odd rounds load k from the top down (item_k_down)
     uint64_t* trace;       // optional per-item timestamps (debugging)
     uint32_t trace_items;
 };
@@ -388,12 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                 const int32_t n0 = int32_t((nt * CP + pair) * BN + it.part * (BN / it.parts)) + prank * brows;
                 const uint32_t tx = it.parts == 1 ? uint32_t(Cfg::kTxBytes)
                                                   : uint32_t(Cfg::kABytes + Cfg::kBBytes / int32_t(it.parts)) * CG;
-                // A partial piece (a cluster's first item) loads its k-blocks from
-                // the last one down, so that at the start of a launch the pieces
-                // of all clusters read the same k-slab at the same time and
-                // neighbouring tiles share it in L2.  The MMA issuer consumes
-                // stages in ring order and needs no change.
-                const bool down = it.kind == kItemPartialOut;
+                // The k-block order (item_k_down): a partial piece, and a whole
+                // tile in an odd round, load from the last k-block down.  The MMA
+                // issuer consumes stages in ring order and needs no change.  An
+                // fp16 accumulator keeps k order: its rounding depends on it.
+                const bool down = !Cfg::kA16 && item_k_down(p, it, nclusters);
                 for (uint32_t i = it.kb0; i < it.kb1; ++i) {
                     const uint32_t kb = down ? it.kb1 - 1u - (i - it.kb0) : i;
                     if (!wait(empty0 + 8 * stage, phase ^ 1u, wi, kSiteProducerEmpty)) {

@@ -217,6 +217,25 @@ G16_HD bool work_next(Work& s, const P& p, Item& it) {
     return false;
 }
 
+// Whether the producer loads an item's k-blocks from the last one down.  A
+// partial stream-K piece does (so that at a launch's start the pieces of all
+// clusters read the same k-slab together).  A whole tile after the stream-K
+// region does in odd rounds, round = (tile - sk_tiles) / G: all clusters
+// stream k-blocks up in one round and down in the next, so a round begins on
+// the k-slabs of the A and B strips that the round before read last, which
+// are still in L2, instead of on those it read first, which a cache that
+// holds less than a round's strips has evicted (only when the launch's plan
+// says so, p.k_alternate: when one round's strips exceed the share of L2 that
+// holds them).  It is a function of the tile and the launch alone, so the same
+// tile takes the same k order in every schedule that runs it whole or in
+// column slices.
+template <class P>
+G16_HD bool item_k_down(const P& p, const Item& it, uint32_t G) {
+    if (it.kind == kItemPartialOut) return true;
+    if (!p.k_alternate || it.kind != kItemWhole || it.tile < p.sk_tiles) return false;
+    return (((it.tile - p.sk_tiles) / G) & 1u) != 0;
+}
+
 // The number of clusters after cluster c whose stream-K ranges start inside
 // `tile`: the partners whose partial tiles the owner of `tile` (cluster c, the
 // piece from k-block 0) adds, in cluster order, which is k order.
@@ -239,6 +258,7 @@ inline void set_schedule(P& p, const PlanT& pl) {
     p.tail_split = uint32_t(pl.tail_split > 1 ? pl.tail_split : 1);
     p.tail_first = uint32_t(pl.num_tiles - (pl.tail_split > 1 ? pl.tail_tiles : 0));
     p.split_pieces = uint32_t(pl.split_pieces > 1 ? pl.split_pieces : 1);
+    p.k_alternate = uint32_t(pl.k_order == 1 ? 1 : 0);
 }
 
 }  // namespace g16

@@ -450,6 +450,14 @@ typedef struct {
                               clusters = num_tiles · s, cluster c on piece c % s of
                               tile t = c / s at m_tile = t % m_tiles, n_tile =
                               t / m_tiles; piece 0 owns the tile (schedule kind 2) */
+    int32_t k_order;       /* persistent kernel, fp32 accumulator: 1 when whole tiles of
+                              odd rounds (round = (tile - sk_tiles) / clusters) load
+                              their k-blocks from the last one down, so that a round
+                              starts on the k-slabs the one before read last (taken
+                              when one round's A and B strips, about
+                              (clusters/swizzle + swizzle) strips of 256 rows × K,
+                              exceed 60 MB); 0: every whole tile from k-block 0 up.
+                              The k order of a sum changes only its rounding. */
 } gemm_f16_nt_plan_t;
 
 gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms,
@@ -491,6 +499,9 @@ typedef struct {
                            partial pieces it adds, in cluster order; else 0   */
     int32_t piece;      /* kind 3 (split piece): its index in the tile's      */
     int32_t pieces;     /*   pieces, 0 <= piece < pieces; else 0 and 1        */
+    int32_t k_down;     /* 1: the item's k-blocks are loaded from kb1 - 1 down
+                           to kb0 (kind 1, and kind 0 in odd rounds with
+                           plan.k_order = 1); 0: from kb0 up                  */
 } gemm_f16_nt_item_t;
 
 /*

@@ -155,6 +155,22 @@ def test_two_pairs_integers_bit_exact():
     check_bitexact(run(A, B, options=g.Options(cluster_pairs=2)), oracle.gemm_f16_nt(A, B), "two pairs int")
 
 
+def test_alternating_k_order_rounds():
+    """Whole tiles of odd rounds load their k-blocks from the last one down
+    (plan k_order 1): two rounds of 16 clusters at K = 16384, float inputs
+    against the oracle and integer inputs bit-exact."""
+    M, N, K = 1024, 2048, 16384
+    o = opts(2, max_clusters=16)
+    pl = g.plan(M, N, K, options=o)
+    assert (pl["k_order"], pl["num_tiles"], pl["clusters"], pl["sk_tiles"], pl["tail_split"]) == (1, 32, 16, 0, 1)
+    A = inputs.draw((M, K), inputs.U, 131)
+    B = inputs.draw((N, K), inputs.U, 132)
+    check_close(run(A, B, options=o), oracle.gemm_f16_nt(A, B), K, "alternating k order")
+    Ai = inputs.draw((M, K), inputs.I2, 133)
+    Bi = inputs.draw((N, K), inputs.I2, 134)
+    check_bitexact(run(Ai, Bi, options=o), oracle.gemm_f16_nt(Ai, Bi), "alternating k order int")
+
+
 def test_stream_k_integers_bit_exact_and_matches_whole_tiles():
     M, N, K = 1200, 1000, 2200
     A = inputs.draw((M, K), inputs.I2, 93)

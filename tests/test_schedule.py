@@ -209,11 +209,34 @@ def check_small(pl, items):
             (t, kb * pc // s, kb * (pc + 1) // s, kind, 1, partners)
 
 
+def check_k_order(pl, items):
+    """The order in which the producer loads an item's k-blocks (k_down).  A
+    partial piece loads from its last k-block down; an owner, a split piece and
+    a stream-K piece covering a whole tile load up.  The whole tiles after the
+    stream-K region go round by round (a cluster's j-th of them is in round j):
+    with plan k_order 0 all load up; with k_order 1 round 0 loads up and the
+    direction flips every round, the same for every cluster."""
+    if pl["kernel"] == 1:
+        assert all(it["k_down"] == 0 for its in items for it in its)
+        return
+    for its in items:
+        j = 0
+        for it in its:
+            if it["kind"] == PARTIAL:
+                assert it["k_down"] == 1, it
+            elif it["kind"] in (OWNER, SPLIT) or it["tile"] < pl["sk_tiles"]:
+                assert it["k_down"] == 0, it
+            elif it["parts"] == 1:
+                assert it["k_down"] == (j % 2 if pl["k_order"] else 0), (j, it)
+                j += 1
+
+
 def check_schedule(pl, items, tile_coord=g.tile_coord):
     check_small(pl, items)
     check_coverage(pl, items)
     check_partials_and_owners(pl, items)
     check_balance_and_coordinates(pl, items, tile_coord)
+    check_k_order(pl, items)
 
 
 @pytest.mark.parametrize("M,N,K,opts,mc", CASES, ids=lambda v: str(v))
@@ -229,6 +252,39 @@ def test_partial_pieces_and_owners(M, N, K, opts, mc):
 @pytest.mark.parametrize("M,N,K,opts,mc", CASES, ids=lambda v: str(v))
 def test_stream_k_balance_and_coordinates(M, N, K, opts, mc):
     check_balance_and_coordinates(*_all_items(M, N, K, opts, mc))
+
+
+@pytest.mark.parametrize("M,N,K,opts,mc", CASES, ids=lambda v: str(v))
+def test_k_order_of_items(M, N, K, opts, mc):
+    check_k_order(*_all_items(M, N, K, opts, mc))
+
+
+@pytest.mark.parametrize("M,N,K,opts,mc,k_order", [
+    (8192, 8192, 8192, {}, 76, 1),                   # a round's strips: 10 + 8 of 256 x 8192 = 75 MB
+    (16384, 14336, 4096, {}, 76, 0),                 # 38 MB: forward only
+    (4096, 4096, 4096, {}, 76, 0),
+    (4000, 3000, 5000, {}, 76, 0),                   # 46 MB
+    (4096, 4096, 16384, {}, 76, 1),
+    (1024, 2048, 16384, {"cta_group": 2}, 16, 1),    # 2 + 8 strips of 256 x 16384 = 84 MB, two rounds
+    (1024, 2048, 16384, {"cta_group": 2}, 32, 0),    # one round only: nothing to alternate
+    (8192, 8192, 8192, {"accumulate": 1}, 76, 0),    # an fp16 accumulator keeps k order
+])
+def test_plan_k_order(M, N, K, opts, mc, k_order):
+    assert g.plan(M, N, K, max_clusters=mc, options=g.Options(**opts))["k_order"] == k_order
+
+
+def test_n_split_tail_keeps_the_whole_tile_k_order():
+    """A tile cut into column slices loads its k-blocks in the order it has as a
+    whole tile, so that the two schedules give bit-identical results."""
+    M = N = K = 8192
+    split = _all_items(M, N, K, {"schedule": 3}, 76)
+    whole = _all_items(M, N, K, {"schedule": 1}, 76)
+    assert split[0]["tail_split"] > 1 and split[0]["k_order"] == whole[0]["k_order"] == 1
+    down_whole = {it["tile"]: it["k_down"] for its in whole[1] for it in its}
+    tail = [it for its in split[1] for it in its if it["parts"] > 1]
+    assert tail and {it["k_down"] for it in tail} <= {0, 1}
+    for it in tail:
+        assert it["k_down"] == down_whole[it["tile"]], it
 
 
 def test_schedule_rejects_a_cluster_out_of_range():

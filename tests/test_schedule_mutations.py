@@ -29,15 +29,15 @@ _HARNESS = r"""
 #include "sched.cuh"
 
 namespace {
-struct Sp { uint32_t num_tiles, num_kb, sk_tiles; uint64_t sk_units; uint32_t tail_first, tail_split, split_pieces; };
-struct Pl { int64_t num_tiles; int32_t k_blocks, sk_tiles, tail_split, tail_tiles, split_pieces; };
+struct Sp { uint32_t num_tiles, num_kb, sk_tiles; uint64_t sk_units; uint32_t tail_first, tail_split, split_pieces, k_alternate; };
+struct Pl { int64_t num_tiles; int32_t k_blocks, sk_tiles, tail_split, tail_tiles, split_pieces, k_order; };
 }
 
 extern "C" int32_t sched_items(int64_t num_tiles, int32_t k_blocks, int32_t sk_tiles, int32_t tail_split,
-                               int32_t tail_tiles, int32_t split_pieces, int32_t m_tiles, int32_t n_tiles,
-                               int32_t swizzle, int32_t clusters, int32_t cluster, int32_t* out,
+                               int32_t tail_tiles, int32_t split_pieces, int32_t k_order, int32_t m_tiles,
+                               int32_t n_tiles, int32_t swizzle, int32_t clusters, int32_t cluster, int32_t* out,
                                int32_t max_items) {
-    Pl pl{num_tiles, k_blocks, sk_tiles, tail_split, tail_tiles, split_pieces};
+    Pl pl{num_tiles, k_blocks, sk_tiles, tail_split, tail_tiles, split_pieces, k_order};
     Sp sp;
     g16::set_schedule(sp, pl);
     const g16::Raster r = g16::make_raster(uint32_t(m_tiles), uint32_t(n_tiles), uint32_t(swizzle));
@@ -49,13 +49,14 @@ extern "C" int32_t sched_items(int64_t num_tiles, int32_t k_blocks, int32_t sk_t
         if (n < max_items) {
             uint32_t mt, nt;
             g16::raster_coord(r, it.tile, mt, nt);
-            int32_t* o = out + 11 * n;
+            int32_t* o = out + 12 * n;
             o[0] = int32_t(it.tile); o[1] = int32_t(mt); o[2] = int32_t(nt);
             o[3] = int32_t(it.kb0); o[4] = int32_t(it.kb1); o[5] = int32_t(it.kind);
             o[6] = int32_t(it.part); o[7] = int32_t(it.parts);
             o[8] = it.kind == g16::kItemOwner
                        ? int32_t(g16::owner_partners(sp, it.tile, uint32_t(cluster), uint32_t(clusters))) : 0;
             o[9] = int32_t(it.piece); o[10] = int32_t(it.pieces);
+            o[11] = int32_t(g16::item_k_down(sp, it, uint32_t(clusters)));
         }
         ++n;
     }
@@ -63,7 +64,8 @@ extern "C" int32_t sched_items(int64_t num_tiles, int32_t k_blocks, int32_t sk_t
 }
 """
 
-_FIELDS = ("tile", "m_tile", "n_tile", "kb0", "kb1", "kind", "part", "parts", "partners", "piece", "pieces")
+_FIELDS = ("tile", "m_tile", "n_tile", "kb0", "kb1", "kind", "part", "parts", "partners", "piece", "pieces",
+           "k_down")
 
 # M, N, K, options, max_clusters: stream-K (last wave, forced, few tiles with
 # middle pieces), N-split (small problem, forced tail), two pairs, cta_group 1
@@ -81,6 +83,9 @@ CASES = [
     (6000, 7000, 3000, {}, 76),
     (300, 520, 328, {"schedule": 4}, 76),             # split pieces of 1 or 2 k-blocks
     (256, 256, 8192, {"schedule": 4}, 76),            # one tile in 8 pieces
+    (8192, 8192, 8192, {}, 76),                       # whole tiles, k order alternating by round
+    (1024, 2048, 16384, {"cta_group": 2}, 16),        # two rounds, k order alternating
+    (1024, 2048, 16384, {"cta_group": 2, "schedule": 2}, 12),   # stream-K, then alternating rounds
 ]
 assert all(g.plan(M, N, K, max_clusters=mc, options=g.Options(**o))["kernel"] == 0 for M, N, K, o, mc in CASES)
 
@@ -105,6 +110,11 @@ MUTATIONS = {
     "split_piece_tile_from_remainder": ("it.tile = s.t / np;", "it.tile = s.t % np;"),
     "split_piece_index_from_quotient": ("const uint32_t np = p.split_pieces, piece = s.t % np;",
                                         "const uint32_t np = p.split_pieces, piece = s.t / np;"),
+    "k_order_ignored": ("if (!p.k_alternate || it.kind != kItemWhole", "if (it.kind != kItemWhole"),
+    "k_order_by_tile_parity": ("return (((it.tile - p.sk_tiles) / G) & 1u) != 0;", "return (it.tile & 1u) != 0;"),
+    "k_order_in_even_rounds": ("return (((it.tile - p.sk_tiles) / G) & 1u) != 0;",
+                               "return (((it.tile - p.sk_tiles) / G) & 1u) == 0;"),
+    "stream_k_tiles_alternate": ("it.kind != kItemWhole || it.tile < p.sk_tiles", "it.kind != kItemWhole"),
     "piece_kinds_swapped": (
         "it.kind = kb0 > 0 ? kItemPartialOut : (kb1 < p.num_kb ? kItemOwner : kItemWhole);",
         "it.kind = kb1 < p.num_kb ? kItemPartialOut : (kb0 > 0 ? kItemOwner : kItemWhole);"),
@@ -129,20 +139,20 @@ def _build(tmp, source):
                     os.path.join(d, "harness.cpp")], check=True, capture_output=True)
     lib = ctypes.CDLL(out)
     lib.sched_items.restype = ctypes.c_int32
-    lib.sched_items.argtypes = [ctypes.c_int64] + [ctypes.c_int32] * 10 + [ctypes.POINTER(ctypes.c_int32),
+    lib.sched_items.argtypes = [ctypes.c_int64] + [ctypes.c_int32] * 11 + [ctypes.POINTER(ctypes.c_int32),
                                                                             ctypes.c_int32]
     return lib
 
 
 def _items(lib, pl):
     args = (pl["num_tiles"], pl["k_blocks"], pl["sk_tiles"], pl["tail_split"], pl["tail_tiles"],
-            pl["split_pieces"], pl["m_tiles"], pl["n_tiles"], pl["swizzle"], pl["clusters"])
+            pl["split_pieces"], pl["k_order"], pl["m_tiles"], pl["n_tiles"], pl["swizzle"], pl["clusters"])
     out = []
     for c in range(pl["clusters"]):
         n = lib.sched_items(*args, c, None, 0)
-        buf = (ctypes.c_int32 * (11 * max(n, 1)))()
+        buf = (ctypes.c_int32 * (12 * max(n, 1)))()
         lib.sched_items(*args, c, buf, n)
-        out.append([dict(zip(_FIELDS, buf[11 * i:11 * i + 11])) for i in range(n)])
+        out.append([dict(zip(_FIELDS, buf[12 * i:12 * i + 12])) for i in range(n)])
     return out
 
 
