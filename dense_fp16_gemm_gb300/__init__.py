@@ -71,7 +71,8 @@ class Plan(ctypes.Structure):
                 ("sk_tiles", ctypes.c_int32), ("cluster_pairs", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("tail_tiles", ctypes.c_int32),
                 ("tail_split", ctypes.c_int32), ("split_k_off", ctypes.c_int32),
-                ("split_pieces", ctypes.c_int32), ("kernel", ctypes.c_int32), ("k_order", ctypes.c_int32)]
+                ("split_pieces", ctypes.c_int32), ("kernel", ctypes.c_int32), ("k_order", ctypes.c_int32),
+                ("claimed_tiles", ctypes.c_int32)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -103,6 +103,7 @@ struct DeviceState {
     int max_ctas1 = 0;       // resident CTAs for Cfg1
     bool single_gpu = false; // the process sees exactly one CUDA device
     uint32_t* watchdog = nullptr;
+    unsigned long long* claim_words = nullptr;   // g_claim_words on this device
     bool ws_ready = false;
     int ws_slots = 0;        // workspace slots reserved (0: stream-K unavailable)
     int64_t ws_bytes = 0;    // bytes per slot
@@ -210,6 +211,12 @@ gemm_status_t setup_device(int dev, DeviceState& st) {
         return GEMM_ERR_LAUNCH;
     }
     st.watchdog = static_cast<uint32_t*>(wd);
+    void* cw = nullptr;
+    if (cudaGetSymbolAddress(&cw, g_claim_words) != cudaSuccess || !cw) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    st.claim_words = static_cast<unsigned long long*>(cw);
     st.sms = sms;
     return GEMM_OK;
 }
@@ -648,6 +655,14 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_
     // to 0.793 GB a launch, power-capped launches from 692.9 to 682.2 us and
     // bursts from 607.7 to 599.6 us; on the MLP shape (38 MB) it cost 0.3 %.
     // An fp16 accumulator keeps k order (its rounding depends on it).
+    // The last, partial wave of whole tiles is claimed at run time: per-cluster
+    // tile times differ systematically by about 4 % on this GPU (the same
+    // clusters are the slow ones launch after launch), and the static deal
+    // gives the extra tile to clusters 0.. whatever their speed.
+    pl->claimed_tiles = 0;
+    if (allow_split_k && sk_tiles == 0 && tail_split == 1 && split_pieces == 1 && clusters > 0 &&
+        tiles > clusters && tiles % clusters != 0)
+        pl->claimed_tiles = int32_t(tiles % clusters);
     pl->k_order = 0;
     if (acc == 0 && tiles - sk_tiles > clusters && clusters > 0) {
         const int64_t w = pl->swizzle;
@@ -711,6 +726,14 @@ gemm_status_t launch(const gemm_f16_nt_plan_t& pl, int64_t M, int64_t N, int64_t
         p.partials = reinterpret_cast<float*>(ws + flags_bytes(Cfg::kCtas, pl.clusters));
     }
     p.launch_id = ++g_launch_seq;
+    if (pl.claimed_tiles > 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || !g_dev[dev].claim_words) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        p.claim = g_dev[dev].claim_words + (p.launch_id % uint64_t(kClaimWords));
+    }
     if (pl.tail_split > 1 &&
         (b_mn || Cfg::kCP != 1 ||
          (s = encode_2d(&p.tmBp, dt, B, uint64_t(K), uint64_t(N), uint64_t(ldb), kBlockK,
@@ -1195,7 +1218,7 @@ G16_EXPORT gemm_status_t gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, i
     struct {
         uint32_t num_tiles, num_kb, sk_tiles;
         uint64_t sk_units;
-        uint32_t tail_first, tail_split, split_pieces, k_alternate;
+        uint32_t tail_first, tail_split, split_pieces, k_alternate, dyn_first;
     } sp;
     g16::set_schedule(sp, pl);
     const g16::Raster r = g16::make_raster(uint32_t(pl.m_tiles), uint32_t(pl.n_tiles), uint32_t(pl.swizzle));

@@ -93,9 +93,16 @@ enum : uint32_t {
     kSiteProducerDrain = 5,
     kSiteMmaDrain = 6,
     kSiteStreamK = 7,
+    kSiteClaim = 8,
 };
 
 __device__ uint32_t g_watchdog_word;
+
+// Counters of the last-wave claims (Params::claim): a launch takes the word
+// of its id modulo kClaimWords, so that launches running at the same time on
+// other streams use other words (each word is tagged with its last launch).
+constexpr int kClaimWords = 256;
+__device__ unsigned long long g_claim_words[kClaimWords];
 
 template <int CG, int BN, int STAGES, int CP = 1, bool BF = false, bool A16 = false>
 struct KCfg {
@@ -140,6 +147,8 @@ struct Ctl {
     uint64_t acc_empty[2];      // accumulator drained               — leader CTA's copy is used
     uint64_t mma_done;          // all MMAs retired (teardown)
     uint64_t xfer[kEpiWarps];   // split pieces: partial slices landed in an epilogue warp's scratch
+    uint64_t claim_bar;         // the cluster's claim of a last-wave tile is in claim_tile
+    uint32_t claim_tile;
     uint32_t tmem_base;
     uint32_t abort_flag;
 };
@@ -175,6 +184,11 @@ struct Params {
     uint32_t tail_split;
     uint32_t split_pieces; // > 1: each cluster runs one split piece of tile cluster / split_pieces
     uint32_t k_alternate;  // 1: whole tiles of odd rounds load k from the top down (item_k_down)
+    // Whole tiles [dyn_first, num_tiles) (a last, partial wave) are claimed at
+    // run time, one at most per cluster, through the 64-bit word *claim: the
+    // launch's tag (launch_id, 48 bits) above a 16-bit count of tickets taken.
+    uint32_t dyn_first;
+    unsigned long long* claim;
     uint64_t* trace;       // optional per-item timestamps (debugging)
     uint32_t trace_items;
 };
@@ -200,15 +214,40 @@ __device__ __noinline__ void raise_abort(const Watch w, uint32_t site) {
     atomicOr(w.word, 1u | (1u << (7u + site)));
 }
 
+// A ticket for the last-wave tiles of the launch tagged `launch_id`.  The
+// 64-bit word holds the tag (48 bits) of the last launch that took one above
+// the count of tickets it has taken (16 bits): a launch's first claim finds
+// another tag and starts the count again, so the word needs no reset between
+// launches.  Returns the ticket, or kNoTicket if the compare-and-swap loop
+// got no turn in 2^20 tries.
+constexpr uint32_t kNoTicket = 0xFFFFFFFFu;
+__device__ __noinline__ uint32_t claim_ticket(unsigned long long* w, uint64_t launch_id) {
+    const unsigned long long tag = launch_id & 0xFFFFFFFFFFFFull;
+    unsigned long long v = atomicAdd(w, 0ull);
+    for (uint32_t i = 0; i < (1u << 20); ++i) {
+        const bool fresh = (v >> 16) != tag;
+        const unsigned long long nv = fresh ? ((tag << 16) | 1ull) : v + 1ull;
+        const unsigned long long old = atomicCAS(w, v, nv);
+        if (old == v) return fresh ? 0u : uint32_t(v & 0xFFFFull);
+        v = old;
+    }
+    return kNoTicket;
+}
+
 // Between checks of the watchdog, a waiting thread sleeps in the barrier
 // (woken when the phase completes) rather than polling shared memory, which
 // would take issue slots and shared-memory bandwidth from the tensor cores.
 constexpr uint32_t kWaitSleepNs = 20000;
 
+// (kCluster: the wait acquires at cluster scope, for a barrier that a thread
+// of another CTA arrives on after writing what the waiter then reads.)
+template <bool kCluster = false>
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Watch w, uint32_t site) {
     const uint64_t t0 = ptx::globaltimer();
     for (;;) {
-        if (ptx::mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+        if (kCluster ? ptx::mbar_try_wait_sleep_acq_cluster(bar, parity, kWaitSleepNs)
+                     : ptx::mbar_try_wait_sleep(bar, parity, kWaitSleepNs))
+            return true;
         if (*w.abort_flag) return false;
         if (ptx::globaltimer() - t0 > w.limit_ns) {
             raise_abort(w, site);
@@ -219,9 +258,10 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Watc
 
 // Wait for the phase of parity `parity` to complete; false if the watchdog
 // fired (here or elsewhere in the CTA).
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, const Watch& w, uint32_t site) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    return wait_slow(bar, parity, w, site);
+    if (kCluster ? ptx::mbar_try_wait_acq_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity)) return true;
+    return wait_slow<kCluster>(bar, parity, w, site);
 }
 
 // Teardown wait after an abort: ignores the abort flag, bounded by the limit.
@@ -326,6 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
         }
         ptx::mbar_init(mma_done, 1);
         for (int e = 0; e < kEpiWarps; ++e) ptx::mbar_init(ptx::smem_u32(&ctl->xfer[e]), 1);
+        ptx::mbar_init(ptx::smem_u32(&ctl->claim_bar), 1);   // the claiming producer's arrive
         ctl->abort_flag = 0u;
         ptx::fence_mbarrier_init();
     }
@@ -367,6 +408,37 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
     Watch wi = w;
     wi.limit_ns = p.item_timeout_ns;
 
+    // The last wave's tiles (work_next's `claim`).  The cluster's first
+    // producer (rank 0), once it has issued its share of loads, takes a ticket
+    // and publishes the tile it names (or num_tiles: none) to every CTA of the
+    // cluster; every other role of every CTA reads it there.  So the clusters
+    // that finish their share first run the last wave, whatever the speed of
+    // their SMs.
+    const uint32_t claim_bar = ptx::smem_u32(&ctl->claim_bar);
+    auto claim_take = [&]() -> uint32_t {
+        uint32_t tile = p.num_tiles;
+        const uint32_t ticket = claim_ticket(p.claim, p.launch_id);
+        if (ticket == kNoTicket)
+            atomicOr(p.watchdog, 1u | (1u << (7u + kSiteClaim)));   // a tile left undone: report it
+        else if (ticket < p.num_tiles - p.dyn_first)
+            tile = p.dyn_first + ticket;
+        if constexpr (NCTA > 1) {
+            const uint32_t slot = ptx::smem_u32(&ctl->claim_tile);
+            for (uint32_t r = 0; r < uint32_t(NCTA); ++r) {
+                ptx::st_cluster_u32(ptx::mapa(slot, r), tile);
+                ptx::mbar_arrive_cluster(ptx::mapa(claim_bar, r));
+            }
+        } else {
+            *reinterpret_cast<volatile uint32_t*>(&ctl->claim_tile) = tile;
+            ptx::mbar_arrive(claim_bar);
+        }
+        return tile;
+    };
+    auto claim_read = [&]() -> uint32_t {
+        if (!wait<(NCTA > 1)>(claim_bar, 0, wi, kSiteClaim)) return p.num_tiles;
+        return *reinterpret_cast<volatile uint32_t*>(&ctl->claim_tile);
+    };
+
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && !p.inject_stall) {
@@ -380,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
             Work work;
             Item it;
             work_init(work, p, cluster, nclusters);
-            while (ok && work_next(work, p, it)) {
+            while (ok && work_next(work, p, it, [&] { return rank == 0 ? claim_take() : claim_read(); })) {
                 uint32_t mt, nt;
                 raster_coord(p.raster, it.tile, mt, nt);
                 const int32_t m0 = int32_t(mt * Cfg::kTileM + prank * kBlockM);
@@ -491,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
                 Item it;
                 work_init(work, p, cluster, nclusters);
                 uint32_t item_no = 0;
-                while (ok && work_next(work, p, it)) {
+                while (ok && work_next(work, p, it, claim_read)) {
                     if (!wait(acce0 + 8 * acc, acc_phase ^ 1u, wi, kSiteMmaAccFree)) break;
                     ptx::tc_fence_after();
                     uint64_t* tr = (p.trace && item_no < p.trace_items)
@@ -593,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
         Item it;
         work_init(work, p, cluster, nclusters);
         uint32_t item_no = 0;
-        while (work_next(work, p, it)) {
+        while (work_next(work, p, it, claim_read)) {
             uint32_t mt, nt;
             raster_coord(p.raster, it.tile, mt, nt);
             const int32_t row0 = int32_t(mt * Cfg::kTileM + prank * kBlockM + q * 32u);

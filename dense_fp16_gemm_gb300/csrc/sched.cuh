@@ -144,6 +144,8 @@ struct Work {
     uint32_t t;          // next whole tile
     uint32_t q;          // next N-split tail item
     uint32_t G;          // clusters
+    uint32_t c;          // this cluster
+    uint32_t claimed;    // 1 once this cluster has asked for a last-wave tile
 };
 
 template <class P>
@@ -158,6 +160,8 @@ G16_HD void work_init(Work& s, const P& p, uint32_t c, uint32_t G) {
     s.t = p.sk_tiles + c;
     s.q = c;
     s.G = G;
+    s.c = c;
+    s.claimed = 0;
     if (p.split_pieces > 1) {   // one split piece per cluster, nothing else
         s.u = s.u_end = 0;
         s.t = c;                 // reused: this cluster's piece index in the launch
@@ -165,8 +169,13 @@ G16_HD void work_init(Work& s, const P& p, uint32_t c, uint32_t G) {
     }
 }
 
-template <class P>
-G16_HD bool work_next(Work& s, const P& p, Item& it) {
+// The next work item of a cluster.  Whole tiles in [dyn_first, num_tiles)
+// (the last, partial wave) are not dealt round-robin: once a cluster has run
+// its share, it asks `claim` for one, and gets a tile of that range or
+// num_tiles (none left); the kernel's claim hands them to the clusters that
+// finish first.
+template <class P, class Claim>
+G16_HD bool work_next(Work& s, const P& p, Item& it, Claim&& claim) {
     it.piece = 0;
     it.pieces = 1;
     if (p.split_pieces > 1) {
@@ -200,12 +209,18 @@ G16_HD bool work_next(Work& s, const P& p, Item& it) {
     it.kb0 = 0;
     it.kb1 = p.num_kb;
     it.kind = kItemWhole;
-    if (s.t < p.tail_first) {
+    it.part = 0;
+    it.parts = 1;
+    if (s.t < p.tail_first && s.t < p.dyn_first) {
         it.tile = s.t;
-        it.part = 0;
-        it.parts = 1;
         s.t += s.G;
         return true;
+    }
+    if (p.dyn_first < p.num_tiles) {   // (no N-split tail then)
+        if (s.claimed) return false;
+        s.claimed = 1;
+        it.tile = claim();
+        return it.tile < p.num_tiles;
     }
     if (s.q < (p.num_tiles - p.tail_first) * p.tail_split) {
         it.tile = p.tail_first + s.q / p.tail_split;
@@ -215,6 +230,17 @@ G16_HD bool work_next(Work& s, const P& p, Item& it) {
         return true;
     }
     return false;
+}
+
+// The same, with the claims of the last wave modelled as taken in cluster
+// order (cluster c gets the c-th tile of the range): one of the orders the
+// kernel can produce, for host-side enumeration and tests.
+template <class P>
+G16_HD bool work_next(Work& s, const P& p, Item& it) {
+    return work_next(s, p, it, [&]() -> uint32_t {
+        const uint32_t t = p.dyn_first + s.c;
+        return t < p.num_tiles ? t : p.num_tiles;
+    });
 }
 
 // Whether the producer loads an item's k-blocks from the last one down.  A
@@ -259,6 +285,7 @@ inline void set_schedule(P& p, const PlanT& pl) {
     p.tail_first = uint32_t(pl.num_tiles - (pl.tail_split > 1 ? pl.tail_tiles : 0));
     p.split_pieces = uint32_t(pl.split_pieces > 1 ? pl.split_pieces : 1);
     p.k_alternate = uint32_t(pl.k_order == 1 ? 1 : 0);
+    p.dyn_first = uint32_t(pl.num_tiles - (pl.claimed_tiles > 0 ? pl.claimed_tiles : 0));
 }
 
 }  // namespace g16

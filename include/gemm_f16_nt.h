@@ -115,7 +115,8 @@ typedef enum {
  * Stream capture: a call made while `stream` is being captured into a CUDA
  * graph is planned without the stream-K split (schedule 2 included), because
  * a replay repeats the launch's parameters and the split's completion flags
- * are tagged per launch (split_k_off = 1 in gemm_f16_nt_launch_plan).  The
+ * are tagged per launch (split_k_off = 1 in gemm_f16_nt_launch_plan); for the
+ * same reason its last wave is dealt round-robin, not claimed.  The
  * captured kernel then touches only A, B, C, the watchdog word and (if
  * requested) the trace buffer, so the graph can be replayed any number of
  * times.  Make the first call on a device outside any capture: it sets the
@@ -377,7 +378,9 @@ gemm_status_t gemm_bf16_nt_ex(int64_t M, int64_t N, int64_t K,
  * filled slot, 3 MMA issuer waiting for a free accumulator, 4 epilogue waiting
  * for a finished accumulator, 5 producer teardown waiting for its copies,
  * 6 MMA teardown waiting for its MMAs, 7 a stream-K owner waiting for a
- * partner's partial tile.  The word is shared by every call on that device.
+ * partner's partial tile, 8 a role waiting for its cluster's claim of a
+ * last-wave tile (or the claim itself failing).  The word is shared by every
+ * call on that device.
  */
 gemm_status_t gemm_f16_nt_device_status(void *stream, uint32_t *flags);
 
@@ -458,6 +461,16 @@ typedef struct {
                               (clusters/swizzle + swizzle) strips of 256 rows × K,
                               exceed 60 MB); 0: every whole tile from k-block 0 up.
                               The k order of a sum changes only its rounding. */
+    int32_t claimed_tiles; /* persistent kernel, whole tiles: the tiles of a last,
+                              partial wave (num_tiles - claimed_tiles onward), which
+                              are not dealt round-robin: each cluster, once it has
+                              run its share, claims one of them at run time (a
+                              launch-tagged counter in device memory), so that the
+                              clusters that finish first take them.  0: every tile
+                              dealt round-robin (stream-K, N-split, split pieces, a
+                              single wave, or a call under stream capture).  The
+                              schedule helper lists them as if cluster c took the
+                              c-th. */
 } gemm_f16_nt_plan_t;
 
 gemm_status_t gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms,

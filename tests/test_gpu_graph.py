@@ -63,3 +63,33 @@ def test_captured_gemm_replays_with_new_inputs(M, N, K):
         kinds = (trace.view(-1, items, 8)[:, :, 0].cpu().numpy() >> 32)
         used = trace.view(-1, items, 8)[:, :, 2].cpu().numpy() != 0
         assert used.any() and np.all(kinds[used] == 0), "the captured launch split tiles in k"
+
+
+def test_captured_gemm_with_a_partial_last_wave():
+    """A shape whose last, partial wave is claimed at run time when called
+    directly (45 tiles on 7 clusters, 3 left over): the captured launch deals
+    it round-robin instead (a replay repeats the launch's tag on the claim
+    counter), and every replay computes the product of its inputs."""
+    M, N, K = 1100, 2100, 520
+    opts = g.Options(cta_group=2, max_clusters=7, schedule=1)
+    assert g.plan(M, N, K, options=opts)["claimed_tiles"] == 45 % 7
+    A0, B0 = _operands(M, N, K, 800)
+    As = torch.from_numpy(A0).cuda()
+    Bs = torch.from_numpy(B0).cuda()
+    Cs = torch.empty((M, N + (-N) % 8), dtype=torch.float16, device="cuda")[:, :N]
+    g.gemm_f16_nt(As, Bs, Cs, options=opts)          # warm-up outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        inside = g.launch_plan(M, N, K, stream=torch.cuda.current_stream(), options=opts)
+        g.gemm_f16_nt(As, Bs, Cs, options=opts)
+    assert inside["claimed_tiles"] == 0
+    for r in range(3):
+        A, B = _operands(M, N, K, 810 + 10 * r)
+        As.copy_(torch.from_numpy(A))
+        Bs.copy_(torch.from_numpy(B))
+        graph.replay()
+        torch.cuda.synchronize()
+        exact = A.astype(np.float64) @ B.astype(np.float64).T
+        assert np.abs(exact).max() < 2048
+        assert np.array_equal(Cs.cpu().numpy().astype(np.float64), exact), f"replay {r}"

@@ -171,6 +171,26 @@ def test_alternating_k_order_rounds():
     check_bitexact(run(Ai, Bi, options=o), oracle.gemm_f16_nt(Ai, Bi), "alternating k order int")
 
 
+@pytest.mark.parametrize("cg,M,N,K,mc", [(2, 1100, 2100, 520, 7), (1, 700, 900, 1000, 5), (2, 4000, 3000, 600, 20)])
+def test_claimed_last_wave(cg, M, N, K, mc):
+    """The tiles of a last, partial wave are claimed at run time by the clusters
+    that finish first (one each at most): float inputs against the oracle,
+    the same bits on every repeat whichever clusters took them, integer inputs
+    bit-exact."""
+    o = opts(cg, max_clusters=mc, schedule=1)
+    pl = g.plan(M, N, K, options=o)
+    assert pl["claimed_tiles"] == pl["num_tiles"] % pl["clusters"] > 0
+    A = inputs.draw((M, K), inputs.U, 141 + M)
+    B = inputs.draw((N, K), inputs.U, 142 + N)
+    C1 = run(A, B, options=o)
+    check_close(C1, oracle.gemm_f16_nt(A, B), K, f"claimed last wave {M}x{N}x{K} cg{cg}")
+    for _ in range(4):
+        assert np.array_equal(run(A, B, options=o).view(np.uint16), C1.view(np.uint16))
+    Ai = inputs.draw((M, K), inputs.I2, 143 + M)
+    Bi = inputs.draw((N, K), inputs.I2, 144 + N)
+    check_bitexact(run(Ai, Bi, options=o), oracle.gemm_f16_nt(Ai, Bi), f"claimed last wave int cg{cg}")
+
+
 def test_stream_k_integers_bit_exact_and_matches_whole_tiles():
     M, N, K = 1200, 1000, 2200
     A = inputs.draw((M, K), inputs.I2, 93)

@@ -273,6 +273,40 @@ def test_plan_k_order(M, N, K, opts, mc, k_order):
     assert g.plan(M, N, K, max_clusters=mc, options=g.Options(**opts))["k_order"] == k_order
 
 
+@pytest.mark.parametrize("M,N,K,opts,mc,claimed", [
+    (8192, 8192, 8192, {}, 76, 1024 % 76),           # 13 rounds dealt, the last 36 tiles claimed
+    (16384, 14336, 4096, {}, 76, 3584 % 76),
+    (4096, 4096, 4096, {}, 76, 0),                   # stream-K takes the last wave
+    (4096, 4096, 4096, {"schedule": 1}, 76, 256 % 76),   # whole tiles only: 28 claimed
+    (1100, 2100, 520, {"cta_group": 2, "schedule": 1}, 7, 45 % 7),
+    (1024, 1024, 8192, {"cta_group": 2}, 64, 0),     # split pieces
+    (2048, 2048, 1024, {"cta_group": 2, "schedule": 1}, 76, 0),  # 64 tiles: one wave, nothing left over
+    (8192, 8192, 8192, {"schedule": 3}, 76, 0),      # N-split tail instead
+    (700, 900, 1000, {"cta_group": 1, "schedule": 1}, 5, 24 % 5),
+])
+def test_plan_claimed_tiles(M, N, K, opts, mc, claimed):
+    pl = g.plan(M, N, K, max_clusters=mc, options=g.Options(**opts))
+    assert pl["claimed_tiles"] == claimed
+    assert claimed < pl["clusters"]
+    if claimed:
+        assert (pl["sk_tiles"], pl["tail_split"], pl["split_pieces"]) == (0, 1, 1)
+        assert pl["num_tiles"] > pl["clusters"]
+
+
+def test_claimed_tiles_listed_in_cluster_order():
+    """The schedule helper lists the claimed tiles as if cluster c took the c-th:
+    each of the first claimed_tiles clusters ends on one tile of the last wave,
+    the others end on their last dealt tile."""
+    pl, items = _all_items(4096, 4096, 4096, {"schedule": 1}, 76)
+    rem, G, T = pl["claimed_tiles"], pl["clusters"], pl["num_tiles"]
+    assert rem == 256 % 76
+    for c, its in enumerate(items):
+        dealt = [it["tile"] for it in its if it["tile"] < T - rem]
+        assert dealt == list(range(c, T - rem, G))
+        last = [it["tile"] for it in its if it["tile"] >= T - rem]
+        assert last == ([T - rem + c] if c < rem else [])
+
+
 def test_n_split_tail_keeps_the_whole_tile_k_order():
     """A tile cut into column slices loads its k-blocks in the order it has as a
     whole tile, so that the two schedules give bit-identical results."""

@@ -29,15 +29,15 @@ _HARNESS = r"""
 #include "sched.cuh"
 
 namespace {
-struct Sp { uint32_t num_tiles, num_kb, sk_tiles; uint64_t sk_units; uint32_t tail_first, tail_split, split_pieces, k_alternate; };
-struct Pl { int64_t num_tiles; int32_t k_blocks, sk_tiles, tail_split, tail_tiles, split_pieces, k_order; };
+struct Sp { uint32_t num_tiles, num_kb, sk_tiles; uint64_t sk_units; uint32_t tail_first, tail_split, split_pieces, k_alternate, dyn_first; };
+struct Pl { int64_t num_tiles; int32_t k_blocks, sk_tiles, tail_split, tail_tiles, split_pieces, k_order, claimed_tiles; };
 }
 
 extern "C" int32_t sched_items(int64_t num_tiles, int32_t k_blocks, int32_t sk_tiles, int32_t tail_split,
-                               int32_t tail_tiles, int32_t split_pieces, int32_t k_order, int32_t m_tiles,
-                               int32_t n_tiles, int32_t swizzle, int32_t clusters, int32_t cluster, int32_t* out,
-                               int32_t max_items) {
-    Pl pl{num_tiles, k_blocks, sk_tiles, tail_split, tail_tiles, split_pieces, k_order};
+                               int32_t tail_tiles, int32_t split_pieces, int32_t k_order, int32_t claimed_tiles,
+                               int32_t m_tiles, int32_t n_tiles, int32_t swizzle, int32_t clusters, int32_t cluster,
+                               int32_t* out, int32_t max_items) {
+    Pl pl{num_tiles, k_blocks, sk_tiles, tail_split, tail_tiles, split_pieces, k_order, claimed_tiles};
     Sp sp;
     g16::set_schedule(sp, pl);
     const g16::Raster r = g16::make_raster(uint32_t(m_tiles), uint32_t(n_tiles), uint32_t(swizzle));
@@ -58,7 +58,7 @@ extern "C" int32_t sched_items(int64_t num_tiles, int32_t k_blocks, int32_t sk_t
             o[9] = int32_t(it.piece); o[10] = int32_t(it.pieces);
             o[11] = int32_t(g16::item_k_down(sp, it, uint32_t(clusters)));
         }
-        ++n;
+        if (++n >= (1 << 20)) return -1;   // a schedule that never ends
     }
     return n;
 }
@@ -115,6 +115,9 @@ MUTATIONS = {
     "k_order_in_even_rounds": ("return (((it.tile - p.sk_tiles) / G) & 1u) != 0;",
                                "return (((it.tile - p.sk_tiles) / G) & 1u) == 0;"),
     "stream_k_tiles_alternate": ("it.kind != kItemWhole || it.tile < p.sk_tiles", "it.kind != kItemWhole"),
+    "claimed_tiles_also_dealt": ("if (s.t < p.tail_first && s.t < p.dyn_first) {", "if (s.t < p.tail_first) {"),
+    "claim_asked_twice": ("        if (s.claimed) return false;\n", ""),
+    "claimed_range_off_by_one": ("const uint32_t t = p.dyn_first + s.c;", "const uint32_t t = p.dyn_first + s.c + 1;"),
     "piece_kinds_swapped": (
         "it.kind = kb0 > 0 ? kItemPartialOut : (kb1 < p.num_kb ? kItemOwner : kItemWhole);",
         "it.kind = kb1 < p.num_kb ? kItemPartialOut : (kb0 > 0 ? kItemOwner : kItemWhole);"),
@@ -139,14 +142,15 @@ def _build(tmp, source):
                     os.path.join(d, "harness.cpp")], check=True, capture_output=True)
     lib = ctypes.CDLL(out)
     lib.sched_items.restype = ctypes.c_int32
-    lib.sched_items.argtypes = [ctypes.c_int64] + [ctypes.c_int32] * 11 + [ctypes.POINTER(ctypes.c_int32),
+    lib.sched_items.argtypes = [ctypes.c_int64] + [ctypes.c_int32] * 12 + [ctypes.POINTER(ctypes.c_int32),
                                                                             ctypes.c_int32]
     return lib
 
 
 def _items(lib, pl):
     args = (pl["num_tiles"], pl["k_blocks"], pl["sk_tiles"], pl["tail_split"], pl["tail_tiles"],
-            pl["split_pieces"], pl["k_order"], pl["m_tiles"], pl["n_tiles"], pl["swizzle"], pl["clusters"])
+            pl["split_pieces"], pl["k_order"], pl["claimed_tiles"], pl["m_tiles"], pl["n_tiles"], pl["swizzle"],
+            pl["clusters"])
     out = []
     for c in range(pl["clusters"]):
         n = lib.sched_items(*args, c, None, 0)
