@@ -213,9 +213,9 @@ def check_k_order(pl, items):
     """The order in which the producer loads an item's k-blocks (k_down).  A
     partial piece loads from its last k-block down; an owner, a split piece and
     a stream-K piece covering a whole tile load up.  The whole tiles after the
-    stream-K region go round by round (a cluster's j-th of them is in round j):
-    with plan k_order 0 all load up; with k_order 1 round 0 loads up and the
-    direction flips every round, the same for every cluster."""
+    stream-K region go wave by wave (a cluster's j-th of them is in wave j):
+    with plan k_order 0 all load up; with k_order 1 the first wave loads up
+    and the direction flips every wave, the same for every cluster."""
     if pl["kernel"] == 1:
         assert all(it["k_down"] == 0 for its in items for it in its)
         return
