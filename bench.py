@@ -587,7 +587,7 @@ def measure_workload(lib, name: str, device, stream, steps: int, warmup: int, co
            "l2": "flushed between launches (per-launch events)" if flushed
                  else "operands larger than L2, launches back to back",
            "plan": {k: pl[k] for k in ("kernel", "cta_group", "tile_n", "cluster_pairs", "clusters", "num_tiles",
-                                       "sk_tiles", "tail_split", "split_pieces")},
+                                       "sk_tiles", "tail_split", "split_pieces", "claimed_tiles", "k_order")},
            "cublas_tflops": round(tf_cb, 2), "ours_over_cublas": round(tf / tf_cb, 4)}
     if add is not None:
         # what a launch adds to the GPU's time after a flush (launch latency overlapped)
@@ -918,7 +918,8 @@ def run_ours(args, w):
                            f"{int(bf16)},{int(acc16)}>>: "
                            f"{pl['clusters']} clusters x {pl['grid_ctas'] // pl['clusters']} CTAs, "
                            f"{pl['tile_m']}x{pl['tile_n']} cluster tiles, {pl['sk_tiles']} of {pl['num_tiles']} "
-                           f"split in k")
+                           f"split in k, {pl['claimed_tiles']} claimed at run time, k order "
+                           f"{'alternating by wave' if pl['k_order'] else 'up'}")
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
