@@ -186,7 +186,8 @@ struct Params {
     uint32_t k_alternate;  // 1: whole tiles of odd rounds load k from the top down (item_k_down)
     // Whole tiles [dyn_first, num_tiles) (a last, partial wave) are claimed at
     // run time, one at most per cluster, through the 64-bit word *claim: the
-    // launch's tag (launch_id, 48 bits) above a 16-bit count of tickets taken.
+    // launch's tag (the low 32 bits of launch_id) above a 32-bit count of
+    // tickets taken.
     uint32_t dyn_first;
     unsigned long long* claim;
     uint64_t* trace;       // optional per-item timestamps (debugging)
@@ -215,23 +216,29 @@ __device__ __noinline__ void raise_abort(const Watch w, uint32_t site) {
 }
 
 // A ticket for the last-wave tiles of the launch tagged `launch_id`.  The
-// 64-bit word holds the tag (48 bits) of the last launch that took one above
-// the count of tickets it has taken (16 bits): a launch's first claim finds
-// another tag and starts the count again, so the word needs no reset between
-// launches.  Returns the ticket, or kNoTicket if the compare-and-swap loop
-// got no turn in 2^20 tries.
+// 64-bit word holds the tag (the low 32 bits of the id) of the launch that
+// started its count above the count of tickets taken (32 bits).  Cluster 0
+// starts the count at the launch's start (claim_start); a claim is one atomic
+// add (the clusters claim at about the same time, and a contended
+// compare-and-swap loop costs microseconds of retries there).  An add that
+// finds an older launch's tag came before the start: the start overwrites its
+// increment, and the claimer waits for the new tag and adds again.  Returns
+// the ticket, or kNoTicket if the tag did not come within `limit_ns`.
 constexpr uint32_t kNoTicket = 0xFFFFFFFFu;
-__device__ __noinline__ uint32_t claim_ticket(unsigned long long* w, uint64_t launch_id) {
-    const unsigned long long tag = launch_id & 0xFFFFFFFFFFFFull;
-    unsigned long long v = atomicAdd(w, 0ull);
-    for (uint32_t i = 0; i < (1u << 20); ++i) {
-        const bool fresh = (v >> 16) != tag;
-        const unsigned long long nv = fresh ? ((tag << 16) | 1ull) : v + 1ull;
-        const unsigned long long old = atomicCAS(w, v, nv);
-        if (old == v) return fresh ? 0u : uint32_t(v & 0xFFFFull);
-        v = old;
+__device__ __forceinline__ void claim_start(unsigned long long* w, uint64_t launch_id) {
+    atomicExch(w, (launch_id & 0xFFFFFFFFull) << 32);
+}
+__device__ __noinline__ uint32_t claim_ticket(unsigned long long* w, uint64_t launch_id, uint64_t limit_ns) {
+    const unsigned long long tag = launch_id & 0xFFFFFFFFull;
+    const uint64_t t0 = ptx::globaltimer();
+    for (;;) {
+        const unsigned long long v = atomicAdd(w, 1ull);
+        if ((v >> 32) == tag) return uint32_t(v & 0xFFFFFFFFull);
+        while ((atomicAdd(w, 0ull) >> 32) != tag) {
+            if (ptx::globaltimer() - t0 > limit_ns) return kNoTicket;
+            __nanosleep(256);
+        }
     }
-    return kNoTicket;
 }
 
 // Between checks of the watchdog, a waiting thread sleeps in the barrier
@@ -391,6 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
     // completed and its writes are visible.
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
+    // this launch's count of claimed tiles starts at 0 (claim_ticket)
+    if (p.dyn_first < p.num_tiles && cluster == 0 && rank == 0 && threadIdx.x == 0) claim_start(p.claim, p.launch_id);
 
     Watch w;
     w.limit_ns = p.timeout_ns;
@@ -417,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_nt_kernel(const __grid_c
     const uint32_t claim_bar = ptx::smem_u32(&ctl->claim_bar);
     auto claim_take = [&]() -> uint32_t {
         uint32_t tile = p.num_tiles;
-        const uint32_t ticket = claim_ticket(p.claim, p.launch_id);
+        const uint32_t ticket = claim_ticket(p.claim, p.launch_id, wi.limit_ns);
         if (ticket == kNoTicket)
             atomicOr(p.watchdog, 1u | (1u << (7u + kSiteClaim)));   // a tile left undone: report it
         else if (ticket < p.num_tiles - p.dyn_first)
